@@ -1,0 +1,425 @@
+/*
+ * mla_oracle.c - plain, slow CPU oracle for paged, absorbed MLA decode.
+ *
+ * TEST INFRASTRUCTURE. Only tests/, __graft_entry__.smoke() and bench.py's
+ * cpu_baseline / reference leg may load this library. The CUDA path never
+ * calls it and shares no source with it.
+ *
+ * Arithmetic: every input arrives as float (the exact widening of the bf16
+ * values the GPU sees); every sum and every exp/log is done in double;
+ * outputs are double. Scalar loops, two-pass softmax, no tiling, no fusion
+ * beyond what the definitions below state. OpenMP only spreads independent
+ * (b, s, h) rows over cores.
+ *
+ * Sources (page title, then section or equation):
+ *  [V3]  "DeepSeek-V3 Multi-head Latent Attention (MLA) deep engineering:
+ *        low-rank KV cache compression" (ybb.press):
+ *        sec. 2.2 (k = W_UK c, v = W_UV c), sec. 2.4 (absorption: q^T W_UK c =
+ *        (W_UK^T q)^T c), sec. 3.1 (decoupled RoPE: a per-head rope query part
+ *        and a shared rope key part), sec. 4.1 (the tile-wise normalised online
+ *        softmax recurrence), sec. 4.3 (only the latent is cached, pages).
+ *  [FM]  "FlashMLA: efficient MLA decode kernel for Hopper GPUs" (wuwenjie.xyz):
+ *        features list (bf16 paged kv cache, block size 64) and usage example
+ *        (get_mla_metadata -> tile schedule + num_splits; flash_mla_with_kvcache
+ *        returns (o, lse)).
+ *  [DS1] "DeepSeek tech explainer (1): MLA" (sunshychen.top), sec. 1: causal
+ *        attention with a lower-triangular mask.
+ *
+ * Readings where the pages are silent or garbled (each is stated once more at
+ * the function that uses it):
+ *  - The rope part enters the score by concatenation: score = q_nope.k_nope +
+ *    q_rope.k_rope (the sum printed in [V3] sec. 3.1 adds vectors of different
+ *    lengths and cannot be meant literally). The scale is a caller argument.
+ *  - kv cache row layout: [c_KV (512) | k_rope (64)], one shared kv head.
+ *  - W_UK is [H, 128, 512] and used as q'[c] = sum_d q_nope[d] W_UK[h,d,c];
+ *    W_UV is [H, 512, 128] and used as out[j] = sum_c o_lat[c] W_UV[h,c,j].
+ *  - Causal alignment is bottom-right: query s of s_q sees keys t with
+ *    t <= seqlen - s_q + s.
+ *  - lse is the natural log of sum_t exp(scaled score). A row with no visible
+ *    key has o = 0 and lse = -inf.
+ *  - Split-KV combine: L = max_i lse_i, lse = L + ln sum_i exp(lse_i - L),
+ *    o = sum_i exp(lse_i - lse) o_i (the pages name num_splits and lse only).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_PAGE 64   /* tokens per page [FM] */
+#define ORC_DC 512    /* latent c_KV width [V3] sec. 2.3 */
+#define ORC_DR 64     /* decoupled rope width */
+#define ORC_DQK 576   /* absorbed query / key width = DC + DR */
+#define ORC_DN 128    /* per-head nope width d_h */
+#define ORC_DQ 192    /* per-head query width = DN + DR */
+#define ORC_DV 128    /* per-head value width after W_UV */
+
+/* Pointer to kv row of logical token t of a sequence, through its block table row. */
+static const float* kv_row(const float* kv, const int32_t* table_row, int64_t t) {
+    int64_t blk = table_row[t / ORC_PAGE];
+    return kv + (blk * ORC_PAGE + (t % ORC_PAGE)) * ORC_DQK;
+}
+
+/* Number of keys query s (of s_q) of a sequence with `seqlen` tokens may see. */
+static int64_t visible_keys(int64_t seqlen, int s_q, int s, int causal) {
+    int64_t n = causal ? seqlen - s_q + s + 1 : seqlen;
+    if (n < 0) n = 0;
+    if (n > seqlen) n = seqlen;
+    return n;
+}
+
+/*
+ * Absorption of the query [V3 sec. 2.4]: q'[c] = sum_d W_UK[h,d,c] q_nope[d]
+ * for c < 512, followed by the untouched rope part q_rope (64) [V3 sec. 3.1].
+ * q [R, H, 192] float, w_uk [H, 128, 512] float -> q_abs [R, H, 576] double.
+ */
+void orc_absorb_q(const float* q, const float* w_uk, int64_t R, int H, double* q_abs) {
+    #pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        for (int h = 0; h < H; ++h) {
+            const float* qr = q + (r * H + h) * ORC_DQ;
+            const float* w = w_uk + (int64_t)h * ORC_DN * ORC_DC;
+            double* out = q_abs + (r * H + h) * ORC_DQK;
+            for (int c = 0; c < ORC_DC; ++c) {
+                double acc = 0.0;
+                for (int d = 0; d < ORC_DN; ++d) acc += (double)qr[d] * (double)w[(int64_t)d * ORC_DC + c];
+                out[c] = acc;
+            }
+            for (int i = 0; i < ORC_DR; ++i) out[ORC_DC + i] = (double)qr[ORC_DN + i];
+        }
+    }
+}
+
+/*
+ * One absorbed query row against logical keys [t_lo, t_hi) of one sequence:
+ * score_t = scale * (q' . kv_t[0:576]); p = softmax(score) in two passes;
+ * o = sum_t p_t kv_t[0:512]; lse = max + ln sum exp(score - max).
+ * [V3 sec. 2.4]: the absorbed query is dotted with the cached latent directly.
+ */
+static void attend_absorbed_row(const double* qa, const float* kv, const int32_t* table_row,
+                                int64_t t_lo, int64_t t_hi, double scale, double* o, double* lse) {
+    for (int c = 0; c < ORC_DC; ++c) o[c] = 0.0;
+    if (t_hi <= t_lo) { *lse = -INFINITY; return; }
+    int64_t n = t_hi - t_lo;
+    double* sc = (double*)malloc((size_t)n * sizeof(double));
+    double mx = -INFINITY;
+    for (int64_t i = 0; i < n; ++i) {
+        const float* k = kv_row(kv, table_row, t_lo + i);
+        double dot = 0.0;
+        for (int c = 0; c < ORC_DQK; ++c) dot += qa[c] * (double)k[c];
+        sc[i] = scale * dot;
+        if (sc[i] > mx) mx = sc[i];
+    }
+    double l = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double p = exp(sc[i] - mx);
+        l += p;
+        const float* v = kv_row(kv, table_row, t_lo + i);
+        for (int c = 0; c < ORC_DC; ++c) o[c] += p * (double)v[c];
+    }
+    for (int c = 0; c < ORC_DC; ++c) o[c] /= l;
+    *lse = mx + log(l);
+    free(sc);
+}
+
+/*
+ * Absorbed-form paged attention for a whole batch.
+ * q_abs [B, s_q, H, 576] double; kv [num_blocks, 64, 576] float;
+ * block_table [B, mbps] int32; seqlens [B] int32 ->
+ * o_lat [B, s_q, H, 512] double, lse [B, s_q, H] double.
+ */
+void orc_attend_absorbed(const double* q_abs, const float* kv, const int32_t* block_table, int mbps,
+                         const int32_t* seqlens, int B, int s_q, int H, double scale, int causal,
+                         double* o_lat, double* lse) {
+    #pragma omp parallel for collapse(3) schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b)
+        for (int s = 0; s < s_q; ++s)
+            for (int h = 0; h < H; ++h) {
+                int64_t row = ((int64_t)b * s_q + s) * H + h;
+                int64_t n = visible_keys(seqlens[b], s_q, s, causal);
+                attend_absorbed_row(q_abs + row * ORC_DQK, kv, block_table + (int64_t)b * mbps, 0, n,
+                                    scale, o_lat + row * ORC_DC, lse + row);
+            }
+}
+
+/*
+ * Naive (decompress) form [V3 sec. 2.2, sec. 3.1, sec. 4.3]: for every visible
+ * token materialise the per-head key K_t = [W_UK[h] c_t (128) | k_rope_t (64)]
+ * and value V_t = W_UV[h]^T c_t (128), then ordinary softmax attention with the
+ * un-absorbed query q [B, s_q, H, 192]. out [B, s_q, H, 128], lse [B, s_q, H].
+ */
+void orc_attend_naive(const float* q, const float* kv, const int32_t* block_table, int mbps,
+                      const int32_t* seqlens, int B, int s_q, int H, const float* w_uk,
+                      const float* w_uv, double scale, int causal, double* out, double* lse) {
+    #pragma omp parallel for collapse(3) schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b)
+        for (int s = 0; s < s_q; ++s)
+            for (int h = 0; h < H; ++h) {
+                int64_t row = ((int64_t)b * s_q + s) * H + h;
+                const float* qr = q + row * ORC_DQ;
+                const int32_t* trow = block_table + (int64_t)b * mbps;
+                const float* wk = w_uk + (int64_t)h * ORC_DN * ORC_DC;
+                const float* wv = w_uv + (int64_t)h * ORC_DC * ORC_DV;
+                int64_t n = visible_keys(seqlens[b], s_q, s, causal);
+                double* o = out + row * ORC_DV;
+                for (int j = 0; j < ORC_DV; ++j) o[j] = 0.0;
+                if (n == 0) { lse[row] = -INFINITY; continue; }
+                double* sc = (double*)malloc((size_t)n * sizeof(double));
+                double mx = -INFINITY;
+                for (int64_t t = 0; t < n; ++t) {
+                    const float* c = kv_row(kv, trow, t);
+                    double dot = 0.0;
+                    for (int d = 0; d < ORC_DN; ++d) {
+                        double kd = 0.0;
+                        for (int cc = 0; cc < ORC_DC; ++cc) kd += (double)wk[(int64_t)d * ORC_DC + cc] * (double)c[cc];
+                        dot += (double)qr[d] * kd;
+                    }
+                    for (int i = 0; i < ORC_DR; ++i) dot += (double)qr[ORC_DN + i] * (double)c[ORC_DC + i];
+                    sc[t] = scale * dot;
+                    if (sc[t] > mx) mx = sc[t];
+                }
+                double l = 0.0;
+                for (int64_t t = 0; t < n; ++t) {
+                    double p = exp(sc[t] - mx);
+                    l += p;
+                    const float* c = kv_row(kv, trow, t);
+                    for (int j = 0; j < ORC_DV; ++j) {
+                        double vj = 0.0;
+                        for (int cc = 0; cc < ORC_DC; ++cc) vj += (double)wv[(int64_t)cc * ORC_DV + j] * (double)c[cc];
+                        o[j] += p * vj;
+                    }
+                }
+                for (int j = 0; j < ORC_DV; ++j) o[j] /= l;
+                lse[row] = mx + log(l);
+                free(sc);
+            }
+}
+
+/*
+ * Output up-projection [V3 sec. 2.2, W_UV side of the absorption]:
+ * out[r,h,j] = sum_c o_lat[r,h,c] W_UV[h,c,j].
+ * o_lat [R, H, 512] double, w_uv [H, 512, 128] float -> out [R, H, 128] double.
+ */
+void orc_out_proj(const double* o_lat, const float* w_uv, int64_t R, int H, double* out) {
+    #pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t r = 0; r < R; ++r)
+        for (int h = 0; h < H; ++h) {
+            const double* o = o_lat + (r * H + h) * ORC_DC;
+            const float* w = w_uv + (int64_t)h * ORC_DC * ORC_DV;
+            double* dst = out + (r * H + h) * ORC_DV;
+            for (int j = 0; j < ORC_DV; ++j) {
+                double acc = 0.0;
+                for (int c = 0; c < ORC_DC; ++c) acc += o[c] * (double)w[(int64_t)c * ORC_DV + j];
+                dst[j] = acc;
+            }
+        }
+}
+
+/*
+ * The pages' own streaming recurrence [V3 sec. 4.1], one key at a time, with a
+ * normalised accumulator: m_new = max(m, s); e = exp(m - m_new) l + exp(s - m_new);
+ * acc = acc * exp(m - m_new) l / e + v exp(s - m_new) / e; m = m_new; l = e.
+ * Written in double (the printed kernel uses half). Same shapes as
+ * orc_attend_absorbed; lse = m + ln l at the end.
+ */
+void orc_attend_streaming(const double* q_abs, const float* kv, const int32_t* block_table, int mbps,
+                          const int32_t* seqlens, int B, int s_q, int H, double scale, int causal,
+                          double* o_lat, double* lse) {
+    #pragma omp parallel for collapse(3) schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b)
+        for (int s = 0; s < s_q; ++s)
+            for (int h = 0; h < H; ++h) {
+                int64_t row = ((int64_t)b * s_q + s) * H + h;
+                const double* qa = q_abs + row * ORC_DQK;
+                const int32_t* trow = block_table + (int64_t)b * mbps;
+                int64_t n = visible_keys(seqlens[b], s_q, s, causal);
+                double* acc = o_lat + row * ORC_DC;
+                for (int c = 0; c < ORC_DC; ++c) acc[c] = 0.0;
+                double m = -INFINITY, l = 0.0;
+                for (int64_t t = 0; t < n; ++t) {
+                    const float* k = kv_row(kv, trow, t);
+                    double dot = 0.0;
+                    for (int c = 0; c < ORC_DQK; ++c) dot += qa[c] * (double)k[c];
+                    double sc = scale * dot;
+                    double m_new = sc > m ? sc : m;
+                    double keep = exp(m - m_new) * l;
+                    double e = keep + exp(sc - m_new);
+                    double a = keep / e, w = exp(sc - m_new) / e;
+                    for (int c = 0; c < ORC_DC; ++c) acc[c] = acc[c] * a + (double)k[c] * w;
+                    m = m_new;
+                    l = e;
+                }
+                lse[row] = n > 0 ? m + log(l) : -INFINITY;
+            }
+}
+
+/*
+ * Split-KV combine of n partial results of one query row (pieces over
+ * disjoint key ranges, each normalised by its own sum):
+ * L = max_i lse_i; lse = L + ln sum_i exp(lse_i - L); o = sum_i exp(lse_i - lse) o_i.
+ * o_parts [n, 512], lse_parts [n] -> o [512], *lse.
+ */
+void orc_combine(const double* o_parts, const double* lse_parts, int n, double* o, double* lse) {
+    for (int c = 0; c < ORC_DC; ++c) o[c] = 0.0;
+    double L = -INFINITY;
+    for (int i = 0; i < n; ++i) if (lse_parts[i] > L) L = lse_parts[i];
+    if (L == -INFINITY) { *lse = -INFINITY; return; }
+    double sum = 0.0;
+    for (int i = 0; i < n; ++i) sum += exp(lse_parts[i] - L);
+    double total = L + log(sum);
+    for (int i = 0; i < n; ++i) {
+        double w = exp(lse_parts[i] - total);
+        for (int c = 0; c < ORC_DC; ++c) o[c] += w * o_parts[(int64_t)i * ORC_DC + c];
+    }
+    *lse = total;
+}
+
+/*
+ * Tile/split schedule. The pages fix only the call shape
+ * [FM usage example: get_mla_metadata(cache_seqlens, ...) -> (tile_scheduler_metadata,
+ * num_splits), computed once per decode step]; the rule below is this
+ * project's own and is written out as the plainest walk over work units.
+ *
+ *  nblk_b  = ceil(seqlen_b / 64) pages (seqlen < 0 counts as 0).
+ *  cost_b  = nblk_b + ovh if nblk_b > 0, else 0;  start_b = sum_{b' < b} cost_b'.
+ *  total   = sum_b cost_b;  quota = max(1, ceil(total / num_parts)).
+ *  Units are (b, page j) in order. Key of a unit: a short batch
+ *  (nblk_b < min_split) puts every unit at key start_b, so it is never split;
+ *  a long batch puts page 0 at start_b and page j >= 1 at start_b + ovh + j.
+ *  A unit belongs to part floor(key / quota).
+ *  A piece is a maximal run of one batch's units inside one part. Pieces are
+ *  numbered in walk order (which is part order).
+ *  tile_meta[p] = {begin_b, begin_page, end_b, end_page (exclusive),
+ *                  first_piece, n_pieces, 0, 0}; an empty part is all zeros.
+ *  num_splits[b] = index of batch b's first piece (exclusive prefix sum of the
+ *  number of pieces per batch); num_splits[B] = total pieces.
+ * Returns 0, or -1 on bad arguments.
+ */
+int orc_metadata(const int32_t* seqlens, int B, int num_parts, int ovh, int min_split,
+                 int32_t* tile_meta, int32_t* num_splits) {
+    if (B < 0 || num_parts <= 0 || ovh < 0 || min_split < 1) return -1;
+    int64_t total = 0;
+    for (int b = 0; b < B; ++b) {
+        int64_t n = seqlens[b] > 0 ? ((int64_t)seqlens[b] + ORC_PAGE - 1) / ORC_PAGE : 0;
+        if (n > 0) total += n + ovh;
+    }
+    int64_t quota = (total + num_parts - 1) / num_parts;
+    if (quota < 1) quota = 1;
+    memset(tile_meta, 0, sizeof(int32_t) * 8 * (size_t)num_parts);
+    int32_t* pieces_of_batch = (int32_t*)calloc((size_t)(B > 0 ? B : 1), sizeof(int32_t));
+    int64_t start = 0;
+    int32_t piece_count = 0;
+    int last_part = -1, last_batch = -1;
+    for (int b = 0; b < B; ++b) {
+        int64_t n = seqlens[b] > 0 ? ((int64_t)seqlens[b] + ORC_PAGE - 1) / ORC_PAGE : 0;
+        if (n == 0) continue;
+        int is_long = n >= min_split;
+        for (int64_t j = 0; j < n; ++j) {
+            int64_t key = (!is_long || j == 0) ? start : start + ovh + j;
+            int p = (int)(key / quota);
+            int32_t* row = tile_meta + (size_t)8 * p;
+            if (p != last_part || b != last_batch) {
+                /* a new piece starts here */
+                if (row[5] == 0) {
+                    row[0] = b;
+                    row[1] = (int32_t)j;
+                    row[4] = piece_count;
+                }
+                row[5] += 1;
+                piece_count += 1;
+                pieces_of_batch[b] += 1;
+                last_part = p;
+                last_batch = b;
+            }
+            row[2] = b;
+            row[3] = (int32_t)(j + 1);
+        }
+        start += n + ovh;
+    }
+    num_splits[0] = 0;
+    for (int b = 0; b < B; ++b) num_splits[b + 1] = num_splits[b] + pieces_of_batch[b];
+    free(pieces_of_batch);
+    return 0;
+}
+
+/*
+ * Split-KV decode through a schedule: every piece of the schedule is attended
+ * on its own (absorbed form over the piece's pages), then each query row of a
+ * batch combines its pieces with orc_combine. Key ranges are clipped to the
+ * row's visible keys, so a piece past a causal limit contributes lse = -inf.
+ * Shapes as orc_attend_absorbed; tile_meta/num_splits from orc_metadata.
+ * Also returns the per-piece partials when o_parts/lse_parts are non-NULL:
+ * o_parts [total_pieces, s_q, H, 512], lse_parts [total_pieces, s_q, H].
+ */
+void orc_attend_split(const double* q_abs, const float* kv, const int32_t* block_table, int mbps,
+                      const int32_t* seqlens, int B, int s_q, int H, double scale, int causal,
+                      const int32_t* tile_meta, int num_parts, const int32_t* num_splits,
+                      double* o_lat, double* lse, double* o_parts_out, double* lse_parts_out) {
+    int total_pieces = num_splits[B];
+    int64_t rows_per_piece = (int64_t)s_q * H;
+    double* o_parts = o_parts_out ? o_parts_out
+                                  : (double*)malloc(sizeof(double) * (size_t)(total_pieces > 0 ? total_pieces : 1) * rows_per_piece * ORC_DC);
+    double* lse_parts = lse_parts_out ? lse_parts_out
+                                      : (double*)malloc(sizeof(double) * (size_t)(total_pieces > 0 ? total_pieces : 1) * rows_per_piece);
+    /* list the pieces: (batch, first page, end page) in piece order */
+    int32_t* pb = (int32_t*)malloc(sizeof(int32_t) * (size_t)(total_pieces > 0 ? total_pieces : 1) * 3);
+    for (int p = 0; p < num_parts; ++p) {
+        const int32_t* row = tile_meta + (size_t)8 * p;
+        if (row[5] == 0) continue;
+        int k = 0;
+        for (int b = row[0]; b <= row[2]; ++b) {
+            int64_t n = seqlens[b] > 0 ? ((int64_t)seqlens[b] + ORC_PAGE - 1) / ORC_PAGE : 0;
+            if (n == 0) continue;
+            int lo = (b == row[0]) ? row[1] : 0;
+            int hi = (b == row[2]) ? row[3] : (int)n;
+            int idx = row[4] + k;
+            pb[3 * idx + 0] = b;
+            pb[3 * idx + 1] = lo;
+            pb[3 * idx + 2] = hi;
+            k += 1;
+        }
+    }
+    #pragma omp parallel for collapse(3) schedule(dynamic, 1)
+    for (int i = 0; i < total_pieces; ++i)
+        for (int s = 0; s < s_q; ++s)
+            for (int h = 0; h < H; ++h) {
+                int b = pb[3 * i];
+                int64_t vis = visible_keys(seqlens[b], s_q, s, causal);
+                int64_t t_lo = (int64_t)pb[3 * i + 1] * ORC_PAGE;
+                int64_t t_hi = (int64_t)pb[3 * i + 2] * ORC_PAGE;
+                if (t_hi > vis) t_hi = vis;
+                int64_t row = ((int64_t)b * s_q + s) * H + h;
+                int64_t prow = ((int64_t)i * s_q + s) * H + h;
+                attend_absorbed_row(q_abs + row * ORC_DQK, kv, block_table + (int64_t)b * mbps, t_lo, t_hi,
+                                    scale, o_parts + prow * ORC_DC, lse_parts + prow);
+            }
+    #pragma omp parallel for collapse(3) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int s = 0; s < s_q; ++s)
+            for (int h = 0; h < H; ++h) {
+                int n = num_splits[b + 1] - num_splits[b];
+                int64_t row = ((int64_t)b * s_q + s) * H + h;
+                double* tmp_o = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * ORC_DC);
+                double* tmp_l = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+                for (int i = 0; i < n; ++i) {
+                    int64_t prow = ((int64_t)(num_splits[b] + i) * s_q + s) * H + h;
+                    memcpy(tmp_o + (int64_t)i * ORC_DC, o_parts + prow * ORC_DC, sizeof(double) * ORC_DC);
+                    tmp_l[i] = lse_parts[prow];
+                }
+                orc_combine(tmp_o, tmp_l, n, o_lat + row * ORC_DC, lse + row);
+                free(tmp_o);
+                free(tmp_l);
+            }
+    free(pb);
+    if (!o_parts_out) free(o_parts);
+    if (!lse_parts_out) free(lse_parts);
+}
+
+/* Threads the OpenMP runtime will use (1 when built without OpenMP). */
+int orc_num_threads(void) {
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
