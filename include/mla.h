@@ -1,0 +1,240 @@
+/*
+ * mla.h - C ABI of libmla: paged, absorbed Multi-head Latent Attention decode
+ * on one GB300 (sm_103a).
+ *
+ * The hot path of one decode step, one call per row of the path:
+ *
+ *   mla_get_metadata   split/tile schedule from cache_seqlens (once per step)
+ *   mla_absorb_q       q' = [W_UK^T q_nope | q_rope]          (per layer)
+ *   mla_decode_paged   attention of q' over the paged latent cache, with
+ *                      split-KV and the log-sum-exp combine     (per layer)
+ *   mla_out_proj       out = W_UV^T o_lat                      (per layer)
+ *
+ * Sources for what each call computes (page title, then section):
+ *  [V3] "DeepSeek-V3 Multi-head Latent Attention (MLA) deep engineering: low-rank
+ *       KV cache compression" (ybb.press): sec. 2.2 (k = W_UK c, v = W_UV c),
+ *       sec. 2.4 (absorption trick), sec. 3.1 (decoupled RoPE), sec. 4.3 (paged,
+ *       latent-only cache).
+ *  [FM] "FlashMLA: efficient MLA decode kernel for Hopper GPUs" (wuwenjie.xyz):
+ *       feature list (bf16 paged kv cache, block size 64) and usage example
+ *       (get_mla_metadata(cache_seqlens, s_q*h_q/h_kv, h_kv) once per step;
+ *       flash_mla_with_kvcache(q, kvcache, block_table, cache_seqlens, dv,
+ *       metadata, num_splits, causal) -> (o, lse) per layer).
+ *  [DS1] "DeepSeek tech explainer (1): MLA" (sunshychen.top), sec. 1 (causal mask).
+ *  [SC] cshb120.cn/d/6765100, the SC11 MLA decode fused operator article: the
+ *       absorb mode is used for decode; up-projection, attention and output
+ *       projection are the decode steps; page loads overlap compute (Fig. 2 text).
+ *
+ * Conventions shared by every call
+ *  - bf16 tensors are passed as `mla_bf16_t*` (raw 16-bit storage of IEEE
+ *    bfloat16). All tensors are dense, row-major, contiguous in the layouts
+ *    stated below, and device pointers unless said otherwise.
+ *  - Every device pointer that is read by the tensor-memory accelerator
+ *    (q, q_abs, kv_cache, w_uk, w_uv, o_lat) must be 16-byte aligned.
+ *  - Ownership: the caller owns every buffer; the library allocates no device
+ *    memory and keeps no pointer after a call returns (it caches only per-device
+ *    properties).
+ *  - Streams: `stream` is a cudaStream_t passed as `void*` (NULL = the legacy
+ *    default stream). Every call only enqueues work on it and returns; none
+ *    synchronises except mla_read_device_error.
+ *  - Errors: argument errors are detected on the host, return a status and
+ *    launch nothing. A failed launch returns MLA_ERR_CUDA. Problems only the
+ *    device can see (a block id outside the pool, a sequence longer than its
+ *    table row, a bounded wait that expired) are recorded in the error word
+ *    at the start of the workspace and read with mla_read_device_error.
+ *  - Shapes: H (query heads) in {16, 32, 64, 128}; s_q (query tokens per
+ *    sequence) in {1, 2}; one shared latent kv head (h_kv = 1).
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t mla_bf16_t;   /* IEEE bfloat16 bit pattern */
+typedef void* mla_stream_t;    /* cudaStream_t */
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or shape */
+    MLA_ERR_UNSUPPORTED = 2,  /* device is not sm_103, or shape outside the supported set */
+    MLA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a launch failed */
+    MLA_ERR_TIMEOUT = 4,      /* (device) a bounded pipeline wait expired */
+    MLA_ERR_BAD_BLOCK = 5     /* (device) block id outside [0, num_blocks) or seqlen past its table row */
+} mla_status_t;
+
+/* Fixed model geometry (DeepSeek-V3 MLA, [V3] sec. 2.3 and 3.1; page size [FM]). */
+#define MLA_PAGE_SIZE 64      /* tokens per kv page */
+#define MLA_D_LATENT 512      /* c_KV width d_c, also the latent value width */
+#define MLA_D_ROPE 64         /* decoupled rope width */
+#define MLA_D_QK 576          /* absorbed query / cached key width = 512 + 64 */
+#define MLA_D_NOPE 128        /* per-head non-rope query width d_h */
+#define MLA_D_Q 192           /* per-head query width = 128 + 64 */
+#define MLA_D_V 128           /* per-head output width after W_UV */
+#define MLA_TILE_META_INTS 8  /* int32 per schedule row */
+
+/* Schedule constants used by mla_get_metadata (see there). */
+#define MLA_SCHED_PIECE_OVERHEAD 7   /* cost of one piece, in page-equivalents */
+#define MLA_SCHED_MIN_SPLIT_PAGES 32 /* sequences shorter than this are never split */
+
+/* Human-readable name of a status code (static string). */
+const char* mla_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int mla_version(void);
+
+/* The two schedule constants compiled into this library. */
+void mla_schedule_constants(int* piece_overhead, int* min_split_pages);
+
+/*
+ * Default number of schedule parts for `device`: one part per pair of SMs
+ * for each query token, i.e. floor(SM count / (2 * s_q)). Returns a positive
+ * count, or minus a status code (e.g. -MLA_ERR_CUDA).
+ */
+int mla_default_num_parts(int device, int s_q);
+
+/*
+ * Bytes of device workspace mla_decode_paged needs for this shape: a 256-byte
+ * error-word header, then the split partials (fp32 o [P, s_q, H, 512] and fp32
+ * lse [P, s_q, H] for up to P = B + num_parts pieces). Returns 0 for bad
+ * arguments. The workspace must be zero-filled before its first use.
+ */
+size_t mla_workspace_size(int B, int s_q, int H, int num_parts);
+
+/*
+ * mla_get_metadata - tile/split schedule of one decode step.
+ * Pages: [FM] usage example (get_mla_metadata(cache_seqlens, s_q*h_q/h_kv, h_kv),
+ * called once per step and reused by every layer). The pages fix only the
+ * call shape; the schedule rule is this library's own:
+ *
+ *   nblk_b = ceil(seqlen_b / 64); cost_b = nblk_b + MLA_SCHED_PIECE_OVERHEAD
+ *   (0 if nblk_b == 0); start_b = sum of earlier costs; total = sum of costs;
+ *   quota = max(1, ceil(total / num_parts)).
+ *   Unit (b, page j) has key start_b when the batch is short
+ *   (nblk_b < MLA_SCHED_MIN_SPLIT_PAGES) or j == 0, else
+ *   start_b + MLA_SCHED_PIECE_OVERHEAD + j; it belongs to part floor(key / quota).
+ *   A piece is a maximal run of one batch's pages inside one part; pieces are
+ *   numbered in part order.
+ *
+ * cache_seqlens: device int32 [B], kv length of each sequence including its
+ *   s_q new tokens (negative values count as 0).
+ * h_kv must be 1. s_q and H are validated like mla_decode_paged's.
+ * tile_meta (out): device int32 [num_parts, 8]; row p =
+ *   {begin_b, begin_page, end_b, end_page (exclusive), first_piece, n_pieces, 0, 0},
+ *   all zeros for an empty part.
+ * num_splits (out): device int32 [B + 1]; num_splits[b] = index of batch b's
+ *   first piece, num_splits[B] = number of pieces (<= B + num_parts).
+ * One small kernel, no host synchronisation.
+ */
+int mla_get_metadata(const int32_t* cache_seqlens, int B, int s_q, int H, int h_kv, int num_parts,
+                     int32_t* tile_meta, int32_t* num_splits, mla_stream_t stream);
+
+/*
+ * mla_absorb_q - query absorption. Pages: [V3] sec. 2.4 (q' = W_UK^T q, so the
+ * score is taken against the cached latent directly), [V3] sec. 3.1 (the rope
+ * part of the query stays separate), [SC] (absorb mode for decode).
+ *
+ * q_abs[b,s,h, c]     = sum_{d<128} q[b,s,h,d] * w_uk[h,d,c]   (c < 512)
+ * q_abs[b,s,h,512+i]  = q[b,s,h,128+i]                          (i < 64)
+ * q: bf16 [B, s_q, H, 192] = [q_nope 128 | q_rope 64];  w_uk: bf16 [H, 128, 512];
+ * q_abs (out): bf16 [B, s_q, H, 576]. fp32 accumulation, bf16 round-to-nearest-even.
+ * Runs as a batched tcgen05 GEMM, one (head, 128-row tile, 256-column half) per CTA.
+ */
+int mla_absorb_q(const mla_bf16_t* q, const mla_bf16_t* w_uk, mla_bf16_t* q_abs, int B, int s_q, int H,
+                 mla_stream_t stream);
+
+/*
+ * mla_decode_paged - absorbed attention over the paged latent cache.
+ * Pages: [V3] sec. 2.4 (score = scale * q' . [c_KV | k_rope]), sec. 4.3 (only
+ * the latent is cached, in pages), [FM] (bf16 cache, 64-token blocks, returns
+ * o and lse, num_splits for long sequences), [DS1] sec. 1 (causal mask),
+ * [SC] Fig. 2 text (page loads overlap compute).
+ *
+ * For every (b, s, h):  n = causal ? seqlen_b - s_q + s + 1 : seqlen_b (clamped
+ * to [0, seqlen_b]); score_t = softmax_scale * q_abs[b,s,h,:] . kv(b,t)[0:576]
+ * for t < n; o_lat[b,s,h,:] = sum_t softmax(score)_t * kv(b,t)[0:512];
+ * lse[b,s,h] = ln sum_t exp(score_t). A row with n == 0 gets o = 0, lse = -inf.
+ * kv(b,t) is row t % 64 of block block_table[b][t / 64].
+ *
+ * q_abs:        bf16 [B, s_q, H, 576] (from mla_absorb_q, or any absorbed query).
+ * kv_cache:     bf16 [num_blocks, 64, 576]; row = [c_KV 512 | k_rope 64].
+ * block_table:  int32 [B, max_blocks_per_seq]; entries past a sequence's last
+ *               page are never read.
+ * cache_seqlens:int32 [B]; must need at most max_blocks_per_seq pages.
+ * tile_meta, num_splits, num_parts: from mla_get_metadata on the same
+ *               cache_seqlens, B, s_q, H and num_parts.
+ * softmax_scale > 0 (DeepSeek-V3: 1/sqrt(192)). causal: 0 or 1.
+ * o_lat (out):  bf16 [B, s_q, H, 512]; lse (out): fp32 [B, s_q, H].
+ * workspace:    device, >= mla_workspace_size(B, s_q, H, num_parts) bytes,
+ *               256-byte aligned, zero-filled before first use; holds the
+ *               device error word and the split partials. Calls that share a
+ *               workspace must be ordered on one stream.
+ * Launches the decode kernel (2-CTA clusters, TMA + tcgen05) and the split
+ * combine kernel.
+ */
+int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int num_blocks,
+                     const int32_t* block_table, int max_blocks_per_seq, const int32_t* cache_seqlens,
+                     int B, int s_q, int H, const int32_t* tile_meta, const int32_t* num_splits, int num_parts,
+                     float softmax_scale, int causal, mla_bf16_t* o_lat, float* lse,
+                     void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
+ * mla_out_proj - output up-projection. Pages: [V3] sec. 2.2 (v = W_UV c, applied
+ * after attention on the latent side), [SC] (output projection step).
+ * out[b,s,h,j] = sum_{c<512} o_lat[b,s,h,c] * w_uv[h,c,j]
+ * o_lat: bf16 [B, s_q, H, 512]; w_uv: bf16 [H, 512, 128]; out (out): bf16 [B, s_q, H, 128].
+ * fp32 accumulation, bf16 round-to-nearest-even. Batched tcgen05 GEMM.
+ */
+int mla_out_proj(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla_bf16_t* out, int B, int s_q, int H,
+                 mla_stream_t stream);
+
+/*
+ * Reads and clears the device error word of `workspace` (synchronises
+ * `stream`). Returns MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_BAD_BLOCK as recorded
+ * by the kernels since the last read, or MLA_ERR_CUDA if the read failed.
+ */
+int mla_read_device_error(void* workspace, mla_stream_t stream);
+
+/*
+ * Bound on every pipeline wait inside the kernels, in nanoseconds of device
+ * wall-clock time (default 4e9, i.e. 4 s). A wait that runs out records
+ * MLA_ERR_TIMEOUT in the error word (the workspace's, or the library's own
+ * word for the projections) and the kernel drains its copies and MMAs, frees
+ * its tensor memory and returns. `ns` <= 0 restores the default. Applies to
+ * launches made after the call, process-wide.
+ */
+void mla_set_wait_limit_ns(long long ns);
+
+/* ----------------------------------------------------------------------------
+ * Test hooks. They expose single building blocks of the path so tests can
+ * check them on their own; they are not part of a decode step.
+ * ------------------------------------------------------------------------- */
+
+/*
+ * Paged gather through TMA, the same way mla_decode_paged loads pages:
+ * out[b, t, :] = kv(b, t)[0:576] for t < min(seqlen_b, max_tokens); other rows
+ * of out are left untouched. out: bf16 [B, max_tokens, 576]. Bit-exact copy.
+ */
+int mla_debug_gather(const mla_bf16_t* kv_cache, int num_blocks, const int32_t* block_table,
+                     int max_blocks_per_seq, const int32_t* cache_seqlens, int B, int max_tokens,
+                     mla_bf16_t* out, mla_stream_t stream);
+
+/*
+ * One-tile tcgen05 check: D[128, N] = A[128, K] * B[K, N] in fp32, the same
+ * shared-memory layouts the decode kernel uses. A: bf16 [128, K] row-major
+ * (K-major). b_kmajor = 1: B given as bf16 [N, K] row-major (K-major, like the
+ * key tile); b_kmajor = 0: B given as bf16 [K, N] row-major (N-major, like the
+ * value tile). K in {64, 128, ..., 576}, N in {64, 128, 256}. d: fp32 [128, N].
+ */
+int mla_debug_mma(const mla_bf16_t* a, const mla_bf16_t* b, int K, int N, int b_kmajor, float* d,
+                  mla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

@@ -1,0 +1,280 @@
+"""ctypes binding of libmla (include/mla.h) over torch tensors.
+
+Argument marshalling only: every function checks dtypes, devices and
+contiguity, allocates missing outputs with torch (device memory is torch's
+job), passes raw pointers and the current CUDA stream, and raises MLAError on
+a non-zero status. All arithmetic runs in the library's CUDA kernels; there is
+no fallback: if libmla.so is missing or cannot load, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmla.so")
+
+MLA_OK = 0
+MLA_ERR_INVALID_ARG = 1
+MLA_ERR_UNSUPPORTED = 2
+MLA_ERR_CUDA = 3
+MLA_ERR_TIMEOUT = 4
+MLA_ERR_BAD_BLOCK = 5
+
+PAGE = 64
+D_QK = 576
+D_LATENT = 512
+D_Q = 192
+D_V = 128
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MLAError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        self.status = status
+        super().__init__(f"{call} failed: {status_string(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmla.so. Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libmla.so not found at {LIB_PATH}: build it with "
+                               "`python -m mla_paged_kv_absorbed_gb300._build` (nvcc, sm_103a)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, F, SZ, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_longlong
+        L.mla_status_string.argtypes = [I]
+        L.mla_status_string.restype = ctypes.c_char_p
+        L.mla_version.restype = I
+        L.mla_schedule_constants.argtypes = [ctypes.POINTER(I), ctypes.POINTER(I)]
+        L.mla_default_num_parts.argtypes = [I, I]
+        L.mla_default_num_parts.restype = I
+        L.mla_workspace_size.argtypes = [I, I, I, I]
+        L.mla_workspace_size.restype = SZ
+        L.mla_set_wait_limit_ns.argtypes = [LL]
+        L.mla_get_metadata.argtypes = [P, I, I, I, I, I, P, P, P]
+        L.mla_get_metadata.restype = I
+        L.mla_absorb_q.argtypes = [P, P, P, I, I, I, P]
+        L.mla_absorb_q.restype = I
+        L.mla_decode_paged.argtypes = [P, P, I, P, I, P, I, I, I, P, P, I, F, I, P, P, P, SZ, P]
+        L.mla_decode_paged.restype = I
+        L.mla_out_proj.argtypes = [P, P, P, I, I, I, P]
+        L.mla_out_proj.restype = I
+        L.mla_read_device_error.argtypes = [P, P]
+        L.mla_read_device_error.restype = I
+        L.mla_debug_gather.argtypes = [P, I, P, I, P, I, I, P, P]
+        L.mla_debug_gather.restype = I
+        L.mla_debug_mma.argtypes = [P, P, I, I, I, P, P]
+        L.mla_debug_mma.restype = I
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().mla_status_string(int(status)).decode()
+    except Exception:
+        return f"status {status}"
+
+
+def _check(call: str, status: int):
+    if status != MLA_OK:
+        raise MLAError(call, status)
+
+
+def _p(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: Optional[int] = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+
+
+# ------------------------------------------------------------------ queries --
+
+def mla_version() -> int:
+    return int(lib().mla_version())
+
+
+def mla_schedule_constants() -> Tuple[int, int]:
+    a, b = ctypes.c_int(), ctypes.c_int()
+    lib().mla_schedule_constants(ctypes.byref(a), ctypes.byref(b))
+    return a.value, b.value
+
+
+def mla_default_num_parts(device: Optional[int] = None, s_q: int = 1) -> int:
+    dev = torch.cuda.current_device() if device is None else int(device)
+    n = int(lib().mla_default_num_parts(dev, int(s_q)))
+    if n <= 0:
+        raise MLAError("mla_default_num_parts", -n)
+    return n
+
+
+def mla_workspace_size(B: int, s_q: int, H: int, num_parts: int) -> int:
+    return int(lib().mla_workspace_size(int(B), int(s_q), int(H), int(num_parts)))
+
+
+def mla_set_wait_limit_ns(ns: int):
+    lib().mla_set_wait_limit_ns(int(ns))
+
+
+def make_workspace(B: int, s_q: int, H: int, num_parts: int, device=None) -> torch.Tensor:
+    """Zero-filled device workspace of mla_workspace_size bytes (256-byte aligned by torch)."""
+    n = mla_workspace_size(B, s_q, H, num_parts)
+    if n == 0:
+        raise MLAError("mla_workspace_size", MLA_ERR_INVALID_ARG)
+    return torch.zeros(n, dtype=torch.uint8, device=device if device is not None else "cuda")
+
+
+# ---------------------------------------------------------------- hot path --
+
+def mla_get_metadata(cache_seqlens: torch.Tensor, s_q: int, H: int, num_parts: Optional[int] = None, h_kv: int = 1,
+                     tile_meta: Optional[torch.Tensor] = None, num_splits: Optional[torch.Tensor] = None,
+                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    _need(cache_seqlens, "cache_seqlens", torch.int32, 1)
+    B = cache_seqlens.shape[0]
+    if num_parts is None:
+        num_parts = mla_default_num_parts(cache_seqlens.device.index, s_q)
+    if tile_meta is None:
+        tile_meta = torch.empty((num_parts, 8), dtype=torch.int32, device=cache_seqlens.device)
+    if num_splits is None:
+        num_splits = torch.empty((B + 1,), dtype=torch.int32, device=cache_seqlens.device)
+    _need(tile_meta, "tile_meta", torch.int32, 2)
+    _need(num_splits, "num_splits", torch.int32, 1)
+    if tile_meta.shape != (num_parts, 8) or num_splits.shape[0] != B + 1:
+        raise ValueError("tile_meta must be [num_parts, 8] and num_splits [B + 1]")
+    _check("mla_get_metadata", lib().mla_get_metadata(_p(cache_seqlens), B, int(s_q), int(H), int(h_kv),
+                                                      int(num_parts), _p(tile_meta), _p(num_splits), _stream(stream)))
+    return tile_meta, num_splits
+
+
+def mla_absorb_q(q: torch.Tensor, w_uk: torch.Tensor, q_abs: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    _need(q, "q", torch.bfloat16, 4)
+    _need(w_uk, "w_uk", torch.bfloat16, 3)
+    B, s_q, H, dq = q.shape
+    if dq != D_Q or tuple(w_uk.shape) != (H, 128, D_LATENT):
+        raise ValueError("q must be [B, s_q, H, 192] and w_uk [H, 128, 512]")
+    if q_abs is None:
+        q_abs = torch.empty((B, s_q, H, D_QK), dtype=torch.bfloat16, device=q.device)
+    _need(q_abs, "q_abs", torch.bfloat16, 4)
+    _check("mla_absorb_q", lib().mla_absorb_q(_p(q), _p(w_uk), _p(q_abs), B, s_q, H, _stream(stream)))
+    return q_abs
+
+
+def mla_decode_paged(q_abs: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                     cache_seqlens: torch.Tensor, tile_meta: torch.Tensor, num_splits: torch.Tensor,
+                     softmax_scale: float, causal: bool = True, o_lat: Optional[torch.Tensor] = None,
+                     lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    _need(q_abs, "q_abs", torch.bfloat16, 4)
+    _need(kv_cache, "kv_cache", torch.bfloat16, 3)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(cache_seqlens, "cache_seqlens", torch.int32, 1)
+    _need(tile_meta, "tile_meta", torch.int32, 2)
+    _need(num_splits, "num_splits", torch.int32, 1)
+    B, s_q, H, d = q_abs.shape
+    if d != D_QK or kv_cache.shape[1:] != (PAGE, D_QK):
+        raise ValueError("q_abs must be [B, s_q, H, 576] and kv_cache [num_blocks, 64, 576]")
+    if block_table.shape[0] != B or cache_seqlens.shape[0] != B or num_splits.shape[0] != B + 1:
+        raise ValueError("block_table, cache_seqlens and num_splits must match the batch of q_abs")
+    num_parts = tile_meta.shape[0]
+    if o_lat is None:
+        o_lat = torch.empty((B, s_q, H, D_LATENT), dtype=torch.bfloat16, device=q_abs.device)
+    if lse is None:
+        lse = torch.empty((B, s_q, H), dtype=torch.float32, device=q_abs.device)
+    if workspace is None:
+        workspace = make_workspace(B, s_q, H, num_parts, q_abs.device)
+    _need(o_lat, "o_lat", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    _need(workspace, "workspace", torch.uint8, 1)
+    _check("mla_decode_paged", lib().mla_decode_paged(
+        _p(q_abs), _p(kv_cache), kv_cache.shape[0], _p(block_table), block_table.shape[1], _p(cache_seqlens),
+        B, s_q, H, _p(tile_meta), _p(num_splits), num_parts, float(softmax_scale), int(bool(causal)),
+        _p(o_lat), _p(lse), _p(workspace), workspace.numel(), _stream(stream)))
+    return o_lat, lse
+
+
+def mla_out_proj(o_lat: torch.Tensor, w_uv: torch.Tensor, out: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    _need(o_lat, "o_lat", torch.bfloat16, 4)
+    _need(w_uv, "w_uv", torch.bfloat16, 3)
+    B, s_q, H, d = o_lat.shape
+    if d != D_LATENT or tuple(w_uv.shape) != (H, D_LATENT, D_V):
+        raise ValueError("o_lat must be [B, s_q, H, 512] and w_uv [H, 512, 128]")
+    if out is None:
+        out = torch.empty((B, s_q, H, D_V), dtype=torch.bfloat16, device=o_lat.device)
+    _need(out, "out", torch.bfloat16, 4)
+    _check("mla_out_proj", lib().mla_out_proj(_p(o_lat), _p(w_uv), _p(out), B, s_q, H, _stream(stream)))
+    return out
+
+
+def mla_read_device_error(workspace: torch.Tensor, stream=None) -> int:
+    """Device-recorded status since the last read (synchronises the stream)."""
+    return int(lib().mla_read_device_error(_p(workspace), _stream(stream)))
+
+
+# -------------------------------------------------------------- test hooks --
+
+def mla_debug_gather(kv_cache: torch.Tensor, block_table: torch.Tensor, cache_seqlens: torch.Tensor,
+                     max_tokens: int, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    _need(kv_cache, "kv_cache", torch.bfloat16, 3)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(cache_seqlens, "cache_seqlens", torch.int32, 1)
+    B = block_table.shape[0]
+    if out is None:
+        out = torch.zeros((B, max_tokens, D_QK), dtype=torch.bfloat16, device=kv_cache.device)
+    _check("mla_debug_gather", lib().mla_debug_gather(_p(kv_cache), kv_cache.shape[0], _p(block_table),
+                                                      block_table.shape[1], _p(cache_seqlens), B, int(max_tokens),
+                                                      _p(out), _stream(stream)))
+    return out
+
+
+def mla_debug_mma(a: torch.Tensor, b: torch.Tensor, b_kmajor: bool, stream=None) -> torch.Tensor:
+    """a [128, K]; b [N, K] if b_kmajor else [K, N]; returns fp32 [128, N] = a . B."""
+    _need(a, "a", torch.bfloat16, 2)
+    _need(b, "b", torch.bfloat16, 2)
+    K = a.shape[1]
+    N = b.shape[0] if b_kmajor else b.shape[1]
+    d = torch.empty((128, N), dtype=torch.float32, device=a.device)
+    _check("mla_debug_mma", lib().mla_debug_mma(_p(a), _p(b), K, N, int(bool(b_kmajor)), _p(d), _stream(stream)))
+    return d
+
+
+# ------------------------------------------------------------- convenience --
+
+def decode_step(inputs, num_parts: Optional[int] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """One pass of the path on device-resident inputs (an inputs.MLAInputs on cuda):
+    metadata -> absorb (when q is given) -> decode (+ combine) -> out-projection.
+    Returns dict(o_lat, lse, out, q_abs, tile_meta, num_splits)."""
+    s_q, H = inputs.s_q, inputs.H
+    tm, ns = mla_get_metadata(inputs.seqlens, s_q, H, num_parts, stream=stream)
+    q_abs = inputs.q_abs if inputs.q is None else mla_absorb_q(inputs.q, inputs.w_uk, stream=stream)
+    o_lat, lse = mla_decode_paged(q_abs, inputs.kv_cache, inputs.block_table, inputs.seqlens, tm, ns, inputs.scale,
+                                  inputs.causal, workspace=workspace, stream=stream)
+    out = mla_out_proj(o_lat, inputs.w_uv, stream=stream) if inputs.w_uv is not None else None
+    return {"o_lat": o_lat, "lse": lse, "out": out, "q_abs": q_abs, "tile_meta": tm, "num_splits": ns}

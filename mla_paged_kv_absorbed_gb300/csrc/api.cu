@@ -1,0 +1,306 @@
+// api.cu - the extern "C" boundary declared in include/mla.h: argument
+// checks, TMA tensor-map construction, workspace layout and kernel launches.
+// Nothing here computes any part of the method; every step runs on the GPU.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "mla.h"
+#include "mla_internal.h"
+
+namespace mla {
+
+WorkspaceLayout workspace_layout(int B, int s_q, int H, int num_parts) {
+    WorkspaceLayout l;
+    const size_t pieces = (size_t)B + (size_t)num_parts;
+    const size_t rows = pieces * (size_t)s_q * (size_t)H;
+    l.lse_offset = kWorkspaceHeader;
+    l.o_offset = l.lse_offset + ((rows * sizeof(float) + 255) & ~size_t(255));
+    l.total = l.o_offset + rows * kDLatent * sizeof(float);
+    return l;
+}
+
+namespace {
+
+std::atomic<long long> g_wait_ns{4000000000LL};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims[0] is the contiguous one.
+bool make_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+               const uint32_t* box, CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_128B) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
+                    reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides_bytes),
+                    reinterpret_cast<const cuuint32_t*>(box), elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+    int sm_count = 0, major = 0, minor = 0, max_clusters = -1;
+};
+
+bool device_info(DeviceInfo& info) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    static bool valid[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!valid[dev]) {
+        cudaDeviceProp p;
+        if (cudaGetDeviceProperties(&p, dev) != cudaSuccess) return false;
+        cache[dev].sm_count = p.multiProcessorCount;
+        cache[dev].major = p.major;
+        cache[dev].minor = p.minor;
+        valid[dev] = true;
+    }
+    info = cache[dev];
+    return true;
+}
+
+int check_device() {
+    DeviceInfo d;
+    if (!device_info(d)) return MLA_ERR_CUDA;
+    if (!(d.major == 10 && d.minor == 3)) return MLA_ERR_UNSUPPORTED;
+    return MLA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool valid_heads(int H) { return H == 16 || H == 32 || H == 64 || H == 128; }
+bool valid_sq(int s_q) { return s_q == 1 || s_q == 2; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+int head_gemm(const void* a, int a_row_elems, const void* w, int K, int N, int n_cta, void* out, int out_row_elems,
+              const void* rope_src, int B, int s_q, int H, cudaStream_t stream) {
+    const int R = B * s_q;
+    CUtensorMap tm_a, tm_b;
+    const uint64_t a_dims[3] = {(uint64_t)a_row_elems, (uint64_t)H, (uint64_t)R};
+    const uint64_t a_strides[2] = {(uint64_t)a_row_elems * 2, (uint64_t)H * a_row_elems * 2};
+    const uint32_t a_box[3] = {64, 1, 128};
+    const uint64_t b_dims[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)H};
+    const uint64_t b_strides[2] = {(uint64_t)N * 2, (uint64_t)K * N * 2};
+    const uint32_t b_box[3] = {64, 64, 1};
+    if (!make_tmap(&tm_a, a, 3, a_dims, a_strides, a_box)) return MLA_ERR_CUDA;
+    if (!make_tmap(&tm_b, w, 3, b_dims, b_strides, b_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) return MLA_ERR_CUDA;
+    GemmArgs args;
+    args.R = R;
+    args.H = H;
+    args.K = K;
+    args.N = N;
+    args.n_cta = n_cta;
+    args.out = out;
+    args.out_row_elems = out_row_elems;
+    args.rope_src = rope_src;
+    return cuda_status(launch_head_gemm(&tm_a, &tm_b, args, g_wait_ns.load(), nullptr, stream));
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+const char* mla_status_string(int status) {
+    switch (status) {
+        case MLA_OK: return "MLA_OK";
+        case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: bad pointer, size, alignment or shape";
+        case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: device is not sm_103 or shape not supported";
+        case MLA_ERR_CUDA: return "MLA_ERR_CUDA: a CUDA call or kernel launch failed";
+        case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded pipeline wait expired on the device";
+        case MLA_ERR_BAD_BLOCK: return "MLA_ERR_BAD_BLOCK: block id outside the pool or seqlen past its table row";
+        default: return "unknown mla status";
+    }
+}
+
+int mla_version(void) { return 100; }
+
+void mla_schedule_constants(int* piece_overhead, int* min_split_pages) {
+    if (piece_overhead) *piece_overhead = kSchedOverhead;
+    if (min_split_pages) *min_split_pages = kSchedMinSplitPages;
+}
+
+int mla_default_num_parts(int device, int s_q) {
+    if (!valid_sq(s_q)) return -MLA_ERR_INVALID_ARG;
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return -MLA_ERR_CUDA;
+    if (device != prev && cudaSetDevice(device) != cudaSuccess) return -MLA_ERR_CUDA;
+    DeviceInfo d;
+    const bool ok = device_info(d);
+    int clusters = ok ? decode_max_active_clusters(device) : 0;
+    if (device != prev) cudaSetDevice(prev);
+    if (!ok) return -MLA_ERR_CUDA;
+    if (clusters <= 0) clusters = d.sm_count / 2;
+    int parts = clusters / s_q;
+    return parts > 0 ? parts : 1;
+}
+
+size_t mla_workspace_size(int B, int s_q, int H, int num_parts) {
+    if (B <= 0 || !valid_sq(s_q) || !valid_heads(H) || num_parts <= 0) return 0;
+    return workspace_layout(B, s_q, H, num_parts).total;
+}
+
+void mla_set_wait_limit_ns(long long ns) { g_wait_ns.store(ns > 0 ? ns : 4000000000LL); }
+
+int mla_get_metadata(const int32_t* cache_seqlens, int B, int s_q, int H, int h_kv, int num_parts,
+                     int32_t* tile_meta, int32_t* num_splits, mla_stream_t stream) {
+    if (!cache_seqlens || !tile_meta || !num_splits || B <= 0 || num_parts <= 0 || num_parts > 65536 || h_kv != 1 ||
+        !valid_sq(s_q) || !valid_heads(H))
+        return MLA_ERR_INVALID_ARG;
+    int dev = check_device();
+    if (dev != MLA_OK) return dev;
+    return cuda_status(launch_metadata(cache_seqlens, B, num_parts, kSchedOverhead, kSchedMinSplitPages, tile_meta,
+                                       num_splits, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_absorb_q(const mla_bf16_t* q, const mla_bf16_t* w_uk, mla_bf16_t* q_abs, int B, int s_q, int H,
+                 mla_stream_t stream) {
+    if (!q || !w_uk || !q_abs || B <= 0 || !valid_sq(s_q) || !valid_heads(H)) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(w_uk) || !aligned16(q_abs)) return MLA_ERR_INVALID_ARG;
+    int dev = check_device();
+    if (dev != MLA_OK) return dev;
+    return head_gemm(q, kDQ, w_uk, kDNope, kDLatent, 256, q_abs, kDQK, q, B, s_q, H,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int mla_out_proj(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla_bf16_t* out, int B, int s_q, int H,
+                 mla_stream_t stream) {
+    if (!o_lat || !w_uv || !out || B <= 0 || !valid_sq(s_q) || !valid_heads(H)) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+    int dev = check_device();
+    if (dev != MLA_OK) return dev;
+    return head_gemm(o_lat, kDLatent, w_uv, kDLatent, kDV, 128, out, kDV, nullptr, B, s_q, H,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int num_blocks, const int32_t* block_table,
+                     int max_blocks_per_seq, const int32_t* cache_seqlens, int B, int s_q, int H,
+                     const int32_t* tile_meta, const int32_t* num_splits, int num_parts, float softmax_scale,
+                     int causal, mla_bf16_t* o_lat, float* lse, void* workspace, size_t workspace_bytes,
+                     mla_stream_t stream) {
+    if (!q_abs || !kv_cache || !block_table || !cache_seqlens || !tile_meta || !num_splits || !o_lat || !lse ||
+        !workspace)
+        return MLA_ERR_INVALID_ARG;
+    if (B <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || num_parts <= 0 || !valid_sq(s_q) || !valid_heads(H))
+        return MLA_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || (causal != 0 && causal != 1)) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_abs) || !aligned16(kv_cache) || !aligned16(o_lat) || !aligned16(lse) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return MLA_ERR_INVALID_ARG;
+    if ((uint64_t)num_blocks * kPage > 0xFFFFFFFFull) return MLA_ERR_INVALID_ARG;
+    const WorkspaceLayout wl = workspace_layout(B, s_q, H, num_parts);
+    if (workspace_bytes < wl.total) return MLA_ERR_INVALID_ARG;
+    int dev = check_device();
+    if (dev != MLA_OK) return dev;
+
+    CUtensorMap tm_q, tm_kv;
+    const uint64_t q_dims[3] = {(uint64_t)kDQK, (uint64_t)H, (uint64_t)B * s_q};
+    const uint64_t q_strides[2] = {(uint64_t)kDQK * 2, (uint64_t)H * kDQK * 2};
+    const uint32_t q_box[3] = {64, (uint32_t)H, 1};
+    const uint64_t kv_dims[2] = {(uint64_t)kDQK, (uint64_t)num_blocks * kPage};
+    const uint64_t kv_strides[1] = {(uint64_t)kDQK * 2};
+    const uint32_t kv_box[2] = {64, (uint32_t)kPage};
+    if (!make_tmap(&tm_q, q_abs, 3, q_dims, q_strides, q_box)) return MLA_ERR_CUDA;
+    if (!make_tmap(&tm_kv, kv_cache, 2, kv_dims, kv_strides, kv_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+        return MLA_ERR_CUDA;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    DecodeArgs a;
+    a.block_table = block_table;
+    a.mbps = max_blocks_per_seq;
+    a.seqlens = cache_seqlens;
+    a.tile_meta = tile_meta;
+    a.num_splits = num_splits;
+    a.num_parts = num_parts;
+    a.B = B;
+    a.s_q = s_q;
+    a.H = H;
+    a.num_blocks = num_blocks;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.causal = causal;
+    a.o_lat = o_lat;
+    a.lse = lse;
+    a.lse_part = reinterpret_cast<float*>(ws + wl.lse_offset);
+    a.o_part = reinterpret_cast<float*>(ws + wl.o_offset);
+    a.err = reinterpret_cast<int*>(ws);
+    a.wait_ns = g_wait_ns.load();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_decode(&tm_q, &tm_kv, a, st);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    e = launch_combine(num_splits, B, s_q, H, a.o_part, a.lse_part, o_lat, lse, st);
+    return cuda_status(e);
+}
+
+int mla_read_device_error(void* workspace, mla_stream_t stream) {
+    if (!workspace) return MLA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int ws_err = 0, gemm_err = 0;
+    if (cudaMemcpyAsync(&ws_err, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (gemm_error_fetch(&gemm_err, st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+    return ws_err != 0 ? ws_err : gemm_err;
+}
+
+int mla_debug_gather(const mla_bf16_t* kv_cache, int num_blocks, const int32_t* block_table, int max_blocks_per_seq,
+                     const int32_t* cache_seqlens, int B, int max_tokens, mla_bf16_t* out, mla_stream_t stream) {
+    if (!kv_cache || !block_table || !cache_seqlens || !out || num_blocks <= 0 || max_blocks_per_seq <= 0 || B <= 0 ||
+        max_tokens <= 0 || !aligned16(kv_cache) || !aligned16(out))
+        return MLA_ERR_INVALID_ARG;
+    int dev = check_device();
+    if (dev != MLA_OK) return dev;
+    CUtensorMap tm_kv;
+    const uint64_t kv_dims[2] = {(uint64_t)kDQK, (uint64_t)num_blocks * kPage};
+    const uint64_t kv_strides[1] = {(uint64_t)kDQK * 2};
+    const uint32_t kv_box[2] = {64, (uint32_t)kPage};
+    if (!make_tmap(&tm_kv, kv_cache, 2, kv_dims, kv_strides, kv_box)) return MLA_ERR_CUDA;
+    return cuda_status(launch_debug_gather(&tm_kv, block_table, max_blocks_per_seq, cache_seqlens, B, max_tokens,
+                                           num_blocks, out, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_debug_mma(const mla_bf16_t* a, const mla_bf16_t* b, int K, int N, int b_kmajor, float* d,
+                  mla_stream_t stream) {
+    if (!a || !b || !d || K <= 0 || K % 64 != 0 || K > 576 || !(N == 64 || N == 128 || N == 256) ||
+        (b_kmajor != 0 && b_kmajor != 1) || !aligned16(a) || !aligned16(b))
+        return MLA_ERR_INVALID_ARG;
+    int dev = check_device();
+    if (dev != MLA_OK) return dev;
+    CUtensorMap tm_a, tm_b;
+    const uint64_t a_dims[2] = {(uint64_t)K, 128};
+    const uint64_t a_strides[1] = {(uint64_t)K * 2};
+    const uint32_t a_box[2] = {64, 128};
+    if (!make_tmap(&tm_a, a, 2, a_dims, a_strides, a_box)) return MLA_ERR_CUDA;
+    if (b_kmajor) {
+        const uint64_t b_dims[2] = {(uint64_t)K, (uint64_t)N};
+        const uint64_t b_strides[1] = {(uint64_t)K * 2};
+        const uint32_t b_box[2] = {64, (uint32_t)N};
+        if (!make_tmap(&tm_b, b, 2, b_dims, b_strides, b_box)) return MLA_ERR_CUDA;
+    } else {
+        const uint64_t b_dims[2] = {(uint64_t)N, (uint64_t)K};
+        const uint64_t b_strides[1] = {(uint64_t)N * 2};
+        const uint32_t b_box[2] = {64, 64};
+        if (!make_tmap(&tm_b, b, 2, b_dims, b_strides, b_box)) return MLA_ERR_CUDA;
+    }
+    return cuda_status(launch_debug_mma(&tm_a, &tm_b, K, N, b_kmajor, d, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

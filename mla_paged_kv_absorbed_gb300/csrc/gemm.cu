@@ -1,0 +1,184 @@
+// gemm.cu - per-head batched bf16 GEMM on tcgen05, used by both projections
+// around the attention:
+//   absorb   q_abs[r,h,0:512] = q[r,h,0:128] . W_UK[h]   (K = 128, N = 512)
+//            q_abs[r,h,512:576] = q[r,h,128:192]          (rope part, copied)
+//   out-proj out[r,h,:]       = o_lat[r,h,:] . W_UV[h]    (K = 512, N = 128)
+// ("DeepSeek-V3 MLA deep engineering", sec. 2.2 and sec. 2.4.)
+//
+// One CTA computes a [128 rows x n_cta] tile of one head: rows are the
+// B * s_q query tokens (TMA zero-fills rows past the end), the accumulator
+// lives in TMEM (n_cta fp32 columns), A (activations, K-major) and B (the
+// head's weight, N-major) stream through a TMA ring of 64-wide K chunks in
+// 128-byte-swizzled shared memory. Warp 0 produces, one thread of warp 1
+// issues the MMAs, and all four warps run the epilogue (TMEM -> bf16 -> HBM).
+#include <cuda_bf16.h>
+
+#include "mla_internal.h"
+#include "ptx.cuh"
+
+namespace mla {
+
+__device__ int g_gemm_error = 0;
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+
+template <int NCTA, int STAGES>
+struct GemmSmem {
+    static constexpr int kABytes = kBM * kBK * 2;          // 16 KB
+    static constexpr int kBBytes = kBK * NCTA * 2;         // NCTA/64 atoms of 8 KB
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kBarOffset = STAGES * kStageBytes;
+    static constexpr int kBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
+};
+
+template <int NCTA, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                     GemmArgs args, long long wait_ns) {
+    using L = GemmSmem<NCTA, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
+    uint64_t* empty = full + STAGES;
+    uint64_t* done = empty + STAGES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * NCTA;
+    const int m0 = blockIdx.y * kBM;
+    const int h = blockIdx.z;
+    const int num_k = args.K / kBK;
+    int* err = &g_gemm_error;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        *abort = 0;
+        fence_mbarrier_init_cluster();
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, NCTA);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // producer
+        int issued = 0;
+        for (int kc = 0; kc < num_k; ++kc) {
+            const int s = kc % STAGES;
+            if (kc >= STAGES && !mbar_wait(&empty[s], ((kc / STAGES) - 1) & 1, abort, err, wait_ns)) break;
+            uint8_t* a_dst = smem + s * L::kStageBytes;
+            uint8_t* b_dst = a_dst + L::kABytes;
+            mbar_arrive_expect_tx(&full[s], L::kStageBytes);
+            tma_load_3d(a_dst, &tm_a, &full[s], kc * kBK, h, m0);
+#pragma unroll
+            for (int j = 0; j < NCTA / 64; ++j) tma_load_3d(b_dst + j * 8192, &tm_b, &full[s], n0 + 64 * j, kc * kBK, h);
+            issued = kc + 1;
+        }
+        // never leave with a copy in flight: wait for the last load of every stage
+        for (int kc = issued - STAGES > 0 ? issued - STAGES : 0; kc < issued; ++kc)
+            mbar_wait(&full[kc % STAGES], (kc / STAGES) & 1, nullptr, err, kDrainNs);
+    } else if (warp == 1) {
+        // MMA issuer
+        constexpr uint32_t idesc = idesc_bf16_f32(kBM, NCTA, false, true);
+        bool ok = true;
+        for (int kc = 0; kc < num_k && ok; ++kc) {
+            const int s = kc % STAGES;
+            ok = warp_wait(&full[s], (kc / STAGES) & 1, abort, err, wait_ns);
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t a_base = smem_u32(smem + s * L::kStageBytes);
+                const uint32_t b_base = a_base + L::kABytes;
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    const uint64_t ad = desc_sw128(a_base + kk * 32, 0, 1024);
+                    const uint64_t bd = desc_sw128(b_base + kk * 2048, 8192, 1024);
+                    mma_bf16_ss(tmem, ad, bd, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&empty[s]);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) mma_commit(done);  // also covers the partial run on abort
+        __syncwarp();
+    }
+
+    // epilogue: thread t owns output row m0 + t
+    const bool ok = mbar_wait(done, 0, nullptr, err, kDrainNs);
+    tc_fence_after();
+    const int row = m0 + threadIdx.x;
+    const bool row_ok = ok && row < args.R && !*abort;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + ((size_t)row * args.H + h) * args.out_row_elems + n0;
+#pragma unroll 1
+    for (int c = 0; c < NCTA / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), v);
+        tmem_wait_ld();
+        if (row_ok) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+    }
+    if (args.rope_src != nullptr && blockIdx.x == 0 && row < args.R) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.rope_src) +
+                                                          ((size_t)row * args.H + h) * kDQ + kDNope);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) +
+                                              ((size_t)row * args.H + h) * args.out_row_elems + kDLatent);
+#pragma unroll
+        for (int i = 0; i < kDRope * 2 / 16; ++i) dst[i] = src[i];
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, NCTA);
+}
+
+template <int NCTA, int STAGES>
+cudaError_t launch_variant(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const GemmArgs& args, long long wait_ns,
+                           cudaStream_t stream) {
+    using L = GemmSmem<NCTA, STAGES>;
+    auto kern = head_gemm_kernel<NCTA, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(args.N / NCTA, (args.R + kBM - 1) / kBM, args.H);
+    kern<<<grid, kThreads, L::kBytes, stream>>>(*tm_a, *tm_b, args, wait_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Reads the projection kernels' error word into *out and clears it, in stream order
+// (the caller synchronises).
+cudaError_t gemm_error_fetch(int* out, cudaStream_t stream) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_gemm_error, sizeof(int), 0, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    static const int zero = 0;
+    return cudaMemcpyToSymbolAsync(g_gemm_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, stream);
+}
+
+cudaError_t launch_head_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const GemmArgs& args, long long wait_ns,
+                             int* /*err*/, cudaStream_t stream) {
+    if (args.n_cta == 256) return launch_variant<256, 2>(tm_a, tm_b, args, wait_ns, stream);
+    if (args.n_cta == 128) return launch_variant<128, 4>(tm_a, tm_b, args, wait_ns, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace mla

@@ -1,0 +1,78 @@
+// mla_internal.h - launchers shared between the C-ABI layer (api.cu) and the
+// kernel translation units. Not installed; the public interface is include/mla.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+constexpr int kPage = 64;
+constexpr int kDLatent = 512;
+constexpr int kDRope = 64;
+constexpr int kDQK = 576;
+constexpr int kDNope = 128;
+constexpr int kDQ = 192;
+constexpr int kDV = 128;
+constexpr int kSchedOverhead = 7;
+constexpr int kSchedMinSplitPages = 32;
+constexpr size_t kWorkspaceHeader = 256;
+
+// Workspace layout: [error word | pad to 256] [lse_part fp32 P*s_q*H, padded to
+// 256 B] [o_part fp32 P*s_q*H*512], with P = B + num_parts.
+struct WorkspaceLayout {
+    size_t lse_offset, o_offset, total;
+};
+WorkspaceLayout workspace_layout(int B, int s_q, int H, int num_parts);
+
+cudaError_t launch_metadata(const int32_t* seqlens, int B, int num_parts, int ovh, int min_split,
+                            int32_t* tile_meta, int32_t* num_splits, cudaStream_t stream);
+
+struct GemmArgs {
+    int R;            // rows = B * s_q
+    int H;            // heads
+    int K;            // contraction length (128 absorb, 512 out-proj)
+    int N;            // output columns per head (512 absorb, 128 out-proj)
+    int n_cta;        // output columns per CTA
+    void* out;        // bf16 [R, H, out_row_elems]
+    int out_row_elems;
+    const void* rope_src;  // absorb only: q [R, H, 192]; rope part copied to out columns 512..575
+};
+cudaError_t launch_head_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const GemmArgs& args,
+                             long long wait_ns, int* err, cudaStream_t stream);
+
+struct DecodeArgs {
+    const int32_t* block_table;
+    int mbps;
+    const int32_t* seqlens;
+    const int32_t* tile_meta;
+    const int32_t* num_splits;
+    int num_parts;
+    int B, s_q, H, num_blocks;
+    float scale_log2;  // softmax_scale * log2(e)
+    int causal;
+    void* o_lat;       // bf16 [B, s_q, H, 512]
+    float* lse;        // [B, s_q, H]
+    float* o_part;     // [P, s_q, H, 512]
+    float* lse_part;   // [P, s_q, H]
+    int* err;
+    long long wait_ns;
+};
+cudaError_t gemm_error_fetch(int* out, cudaStream_t stream);
+int decode_max_active_clusters(int device);
+
+cudaError_t launch_decode(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, const DecodeArgs& args,
+                          cudaStream_t stream);
+
+cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, const float* o_part,
+                           const float* lse_part, void* o_lat, float* lse, cudaStream_t stream);
+
+cudaError_t launch_debug_gather(const CUtensorMap* tm_kv, const int32_t* block_table, int mbps,
+                                const int32_t* seqlens, int B, int max_tokens, int num_blocks, void* out,
+                                cudaStream_t stream);
+
+cudaError_t launch_debug_mma(const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, int N, int b_kmajor,
+                             float* d, cudaStream_t stream);
+
+}  // namespace mla

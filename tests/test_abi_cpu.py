@@ -1,0 +1,91 @@
+"""The C-ABI library builds, loads and exports every symbol include/mla.h
+declares; host-side argument checks reject bad calls before touching a GPU.
+No compute call is made here (no GPU in this environment)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mla_paged_kv_absorbed_gb300 import _build
+    _build.build()
+    from mla_paged_kv_absorbed_gb300 import api
+    return api.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", text)))
+
+
+def header_define(name):
+    m = re.search(rf"#define\s+{name}\s+(\d+)", open(HEADER).read())
+    return int(m.group(1))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for n in ("mla_get_metadata", "mla_absorb_q", "mla_decode_paged", "mla_out_proj", "mla_read_device_error",
+              "mla_workspace_size", "mla_default_num_parts"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in mla.h but not exported by libmla.so"
+
+
+def test_library_is_built_for_sm_103a(L):
+    from mla_paged_kv_absorbed_gb300 import _build
+    assert "arch=compute_103a,code=sm_103a" in " ".join(_build.ARCH)
+
+
+def test_schedule_constants_match_header_and_oracle_tests(L):
+    from mla_paged_kv_absorbed_gb300 import api
+    ovh, min_split = api.mla_schedule_constants()
+    assert ovh == header_define("MLA_SCHED_PIECE_OVERHEAD")
+    assert min_split == header_define("MLA_SCHED_MIN_SPLIT_PAGES")
+
+
+def test_status_strings(L):
+    from mla_paged_kv_absorbed_gb300 import api
+    for code in range(6):
+        assert api.status_string(code).startswith("MLA_")
+    assert "unknown" in api.status_string(99)
+
+
+def test_workspace_size_formula(L):
+    from mla_paged_kv_absorbed_gb300 import api
+    for B, s_q, H, parts in ((128, 1, 128, 76), (132, 2, 128, 38), (2, 1, 16, 5)):
+        rows = (B + parts) * s_q * H
+        lse = (rows * 4 + 255) // 256 * 256
+        assert api.mla_workspace_size(B, s_q, H, parts) == 256 + lse + rows * 512 * 4
+    assert api.mla_workspace_size(0, 1, 128, 76) == 0
+    assert api.mla_workspace_size(4, 3, 128, 76) == 0
+    assert api.mla_workspace_size(4, 1, 100, 76) == 0
+
+
+def test_bad_arguments_are_rejected_on_the_host(L):
+    null = ctypes.c_void_p(0)
+    assert L.mla_get_metadata(null, 4, 1, 128, 1, 8, null, null, null) == 1
+    assert L.mla_absorb_q(null, null, null, 4, 1, 128, null) == 1
+    assert L.mla_out_proj(null, null, null, 4, 1, 128, null) == 1
+    assert L.mla_decode_paged(null, null, 1, null, 1, null, 1, 1, 128, null, null, 1, ctypes.c_float(0.1), 1,
+                              null, null, null, 0, null) == 1
+    assert L.mla_debug_mma(null, null, 64, 64, 1, null, null) == 1
+    assert L.mla_read_device_error(null, null) == 1
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from mla_paged_kv_absorbed_gb300 import api
+    monkeypatch.setattr(api, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(api, "_lib", None)
+    with pytest.raises(RuntimeError, match="libmla.so not found"):
+        api.lib()

@@ -1,0 +1,191 @@
+"""GPU parity of the decode path through the C ABI against the CPU oracle.
+
+Small cases run the oracle on every output; the five named workloads run at
+full size in the launch configuration the benchmark times (default number of
+schedule parts) and compare sampled sequences, which the oracle evaluates one
+by one at their full length."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_paged_kv_absorbed_gb300 import inputs as gen
+from parity_util import assert_lse_close, assert_o_close, f32, oracle_decode, oracle_end_to_end
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    from mla_paged_kv_absorbed_gb300 import _build
+    _build.build()
+    from mla_paged_kv_absorbed_gb300 import api as a
+    return a
+
+
+def run(api, inp, num_parts=None):
+    d = inp.to("cuda")
+    tm, ns = api.mla_get_metadata(d.seqlens, d.s_q, d.H, num_parts)
+    q_abs = d.q_abs if d.q is None else api.mla_absorb_q(d.q, d.w_uk)
+    ws = api.make_workspace(d.B, d.s_q, d.H, tm.shape[0])
+    o, lse = api.mla_decode_paged(q_abs, d.kv_cache, d.block_table, d.seqlens, tm, ns, d.scale, d.causal,
+                                  workspace=ws)
+    out = api.mla_out_proj(o, d.w_uv) if d.w_uv is not None else None
+    status = api.mla_read_device_error(ws)
+    return {"q_abs": q_abs.cpu(), "o": o.cpu(), "lse": lse.cpu(), "out": None if out is None else out.cpu(),
+            "status": status, "tm": tm.cpu(), "ns": ns.cpu()}
+
+
+def check_decode(inp, r):
+    assert r["status"] == 0, f"device status {r['status']}"
+    o_ref, lse_ref = oracle_decode(inp, r["q_abs"])
+    assert_o_close(r["o"], o_ref, "o_lat")
+    assert_lse_close(r["lse"], lse_ref)
+
+
+# -------------------------------------------------------------- small, full --
+
+SMALL = [
+    (3, 1, 128, [1, 64, 65]),
+    (4, 2, 128, [2, 63, 64, 129]),
+    (2, 1, 16, [37, 100]),
+    (3, 2, 64, [1, 5, 300]),
+    (5, 1, 32, [200, 1, 77, 128, 513]),
+    (2, 2, 16, [64, 65]),
+]
+
+
+@pytest.mark.parametrize("B,s_q,H,seqlens", SMALL)
+@pytest.mark.parametrize("num_parts", [None, 1, 7])
+def test_small_full_parity(api, B, s_q, H, seqlens, num_parts):
+    inp = gen.make_inputs(B, s_q, H, seqlens, seed=B * 31 + s_q * 7 + H, q_mode="q_abs")
+    check_decode(inp, run(api, inp, num_parts))
+
+
+@pytest.mark.parametrize("s_q", [1, 2])
+@pytest.mark.parametrize("num_parts", [1, 5, 13, 40])
+def test_split_kv_and_combine(api, s_q, num_parts):
+    inp = gen.make_inputs(3, s_q, 128, [2100, 3000, 4095], seed=77 + s_q, q_mode="q_abs")
+    r = run(api, inp, num_parts)
+    if num_parts >= 5:
+        assert int(r["ns"][-1]) > 3  # the schedule really split something
+    check_decode(inp, r)
+
+
+def test_tiny_end_to_end(api):
+    inp = gen.make_workload("tiny")
+    r = run(api, inp)
+    check_decode(inp, r)
+    qa, o, lse, out = oracle_end_to_end(inp)
+    assert_o_close(r["q_abs"], qa, "q_abs")
+    assert_o_close(r["out"], out, "out")
+    assert_lse_close(r["lse"], lse, "lse (end to end)")
+
+
+def test_empty_and_fully_masked_rows(api):
+    inp = gen.make_inputs(4, 2, 128, [0, 1, 64, 65], seed=5, q_mode="q_abs")
+    r = run(api, inp, 3)
+    check_decode(inp, r)
+    assert torch.all(r["o"][0] == 0) and torch.all(r["lse"][0] == -np.inf)
+    assert torch.all(r["o"][1, 0] == 0) and torch.all(r["lse"][1, 0] == -np.inf)
+
+
+def test_nan_and_inf_in_tail_rows_do_not_leak(api):
+    inp = gen.make_inputs(3, 1, 128, [3, 70, 200], seed=9, q_mode="q_abs", tail_fill=float("nan"))
+    check_decode(inp, run(api, inp))
+    inp = gen.make_inputs(3, 2, 128, [3, 70, 200], seed=10, q_mode="q_abs", tail_fill=float("inf"))
+    check_decode(inp, run(api, inp))
+
+
+def test_page_permutation_bit_identical(api):
+    inp = gen.make_inputs(4, 2, 128, [100, 640, 64, 3000], seed=12, q_mode="q_abs")
+    r1 = run(api, inp, 9)
+    g = torch.Generator().manual_seed(1)
+    perm = torch.randperm(inp.num_blocks, generator=g)
+    kv2 = torch.empty_like(inp.kv_cache)
+    kv2[perm] = inp.kv_cache
+    table = inp.block_table.clone()
+    valid = table >= 0
+    table[valid] = perm[table[valid].long()].to(torch.int32)
+    inp2 = gen.MLAInputs(inp.B, inp.s_q, inp.H, inp.scale, inp.causal, inp.seqlens, table, kv2, None, inp.q_abs,
+                         None, None)
+    r2 = run(api, inp2, 9)
+    assert torch.equal(r1["o"].view(torch.int16), r2["o"].view(torch.int16))
+    assert torch.equal(r1["lse"], r2["lse"])
+
+
+def test_non_causal_multi_token(api):
+    inp = gen.make_inputs(3, 2, 128, [65, 129, 1], seed=14, q_mode="q_abs", causal=False)
+    check_decode(inp, run(api, inp))
+
+
+# -------------------------------------------------- named workloads, sampled --
+
+def sampled_check(api, name, batches, heads=None, end_to_end=False):
+    inp = gen.make_workload(name)
+    r = run(api, inp)
+    assert r["status"] == 0
+    sub = gen.sample_batches(inp, batches)
+    idx = torch.tensor(batches)
+    q_abs = r["q_abs"][idx]
+    o_gpu, lse_gpu = r["o"][idx], r["lse"][idx]
+    if heads is not None:
+        q_abs, o_gpu, lse_gpu = q_abs[:, :, heads], o_gpu[:, :, heads], lse_gpu[:, :, heads]
+    o_ref, lse_ref = oracle.attend_absorbed(f32(q_abs), f32(sub.kv_cache), sub.block_table, sub.seqlens, sub.scale,
+                                            sub.causal)
+    assert_o_close(o_gpu, o_ref, f"{name} o_lat")
+    assert_lse_close(lse_gpu, lse_ref, f"{name} lse")
+    if end_to_end:
+        qa = oracle.absorb_q(f32(sub.q), f32(sub.w_uk))
+        o64, _ = oracle.attend_absorbed(qa, f32(sub.kv_cache), sub.block_table, sub.seqlens, sub.scale, sub.causal)
+        out_ref = oracle.out_proj(o64, f32(sub.w_uv))
+        assert_o_close(r["out"][idx], out_ref, f"{name} out")
+    return r
+
+
+def test_workload_dsv3(api):
+    sampled_check(api, "dsv3", [0, 1, 37, 64, 100, 127], end_to_end=True)
+
+
+def test_workload_varlen(api):
+    sampled_check(api, "varlen", [0, 13, 31, 50, 63])
+
+
+def test_workload_long(api):
+    sampled_check(api, "long", [0, 7, 15], heads=list(range(0, 128, 8)))
+
+
+def test_workload_spec(api):
+    sampled_check(api, "spec", [0, 65, 131], end_to_end=True)
+
+
+# ------------------------------------------------------------------ errors --
+
+def test_bad_block_is_reported(api):
+    inp = gen.make_inputs(2, 1, 128, [100, 100], seed=21, q_mode="q_abs")
+    inp.block_table[1, 1] = inp.num_blocks + 5
+    r = run(api, inp)
+    assert r["status"] == api.MLA_ERR_BAD_BLOCK
+    # the healthy sequence is still right
+    o_ref, lse_ref = oracle.attend_absorbed(f32(r["q_abs"][:1]), f32(inp.kv_cache), inp.block_table[:1],
+                                            inp.seqlens[:1], inp.scale, True)
+    assert_o_close(r["o"][:1], o_ref)
+
+
+def test_host_rejects_bad_shapes(api):
+    d = gen.make_inputs(2, 1, 128, [10, 10], seed=1, q_mode="q_abs").to("cuda")
+    tm, ns = api.mla_get_metadata(d.seqlens, 1, 128, 4)
+    with pytest.raises(api.MLAError) as e:
+        api.mla_get_metadata(d.seqlens, 3, 128, 4)
+    assert e.value.status == api.MLA_ERR_INVALID_ARG
+    ws = api.make_workspace(2, 1, 128, 4)
+    small_ws = ws[: ws.numel() // 2]
+    with pytest.raises(api.MLAError) as e:
+        api.mla_decode_paged(d.q_abs, d.kv_cache, d.block_table, d.seqlens, tm, ns, d.scale, True, workspace=small_ws)
+    assert e.value.status == api.MLA_ERR_INVALID_ARG
+    # a misaligned q_abs view
+    flat = torch.zeros(d.q_abs.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    mis = flat[1:1 + d.q_abs.numel()].view_as(d.q_abs)
+    with pytest.raises(api.MLAError) as e:
+        api.mla_decode_paged(mis, d.kv_cache, d.block_table, d.seqlens, tm, ns, d.scale, True, workspace=ws)
+    assert e.value.status == api.MLA_ERR_INVALID_ARG
