@@ -209,6 +209,41 @@ int mla_read_device_error(void* workspace, mla_stream_t stream);
  */
 void mla_set_wait_limit_ns(long long ns);
 
+/*
+ * mla_decode_paged_noalloc - mla_decode_paged for callers that may not
+ * allocate device memory. (No counterpart on the pages: this is a packaging
+ * variant of the same decode, not part of the method.)
+ *
+ * Who needs it: code that is handed only its input and output buffers and must
+ * not call cudaMalloc itself - e.g. a plugin inside a host inference engine that
+ * owns the device memory pool, or a serving loop where an allocation could
+ * synchronise the device. It computes exactly what mla_decode_paged computes,
+ * with the same arguments and errors, except that the workspace (split
+ * partials and device error word) lives in a fixed scratch array compiled into
+ * the library, MLA_NOALLOC_SCRATCH_BYTES (about 64 MiB) per GPU that uses it,
+ * held until the process exits. Limit: (B + num_parts) * s_q * H must not
+ * exceed MLA_NOALLOC_MAX_ROWS (32768; e.g. B = 128, num_parts = 76, s_q = 1,
+ * H = 128 uses 26112); larger shapes return MLA_ERR_INVALID_ARG and launch
+ * nothing. The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ * device_status (optional, may be NULL): caller-owned device int32 that
+ * receives, in stream order after the kernels, the device status of this call
+ * (MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_BAD_BLOCK); the scratch error word is
+ * cleared at the start of every call.
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress, with that device current), so make that first call
+ * before any stream capture. All calls share the one array and it keeps the
+ * last call's contents: calls that overlap on the GPU (on unordered streams)
+ * race on it and must be serialised by the caller.
+ */
+#define MLA_NOALLOC_MAX_ROWS 32768
+#define MLA_NOALLOC_SCRATCH_BYTES (256 + MLA_NOALLOC_MAX_ROWS * (4 + 4 * MLA_D_LATENT))
+int mla_decode_paged_noalloc(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int num_blocks,
+                             const int32_t* block_table, int max_blocks_per_seq, const int32_t* cache_seqlens,
+                             int B, int s_q, int H, const int32_t* tile_meta, const int32_t* num_splits,
+                             int num_parts, float softmax_scale, int causal, mla_bf16_t* o_lat, float* lse,
+                             int32_t* device_status, mla_stream_t stream);
+
 /* ----------------------------------------------------------------------------
  * Test hooks. They expose single building blocks of the path so tests can
  * check them on their own; they are not part of a decode step.

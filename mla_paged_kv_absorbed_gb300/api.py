@@ -278,3 +278,33 @@ def decode_step(inputs, num_parts: Optional[int] = None, workspace: Optional[tor
                                   inputs.causal, workspace=workspace, stream=stream)
     out = mla_out_proj(o_lat, inputs.w_uv, stream=stream) if inputs.w_uv is not None else None
     return {"o_lat": o_lat, "lse": lse, "out": out, "q_abs": q_abs, "tile_meta": tm, "num_splits": ns}
+
+
+# ------------------------------------------------------- no-allocation entry --
+
+def mla_decode_paged_noalloc(q_abs: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                             cache_seqlens: torch.Tensor, tile_meta: torch.Tensor, num_splits: torch.Tensor,
+                             softmax_scale: float, causal: bool, o_lat: torch.Tensor, lse: torch.Tensor,
+                             device_status: Optional[torch.Tensor] = None, stream=None):
+    """mla_decode_paged for callers that must not allocate device memory: the
+    scratch comes from an array inside the library, the caller passes every
+    input and output (this wrapper allocates nothing either). See include/mla.h."""
+    L = lib()
+    fn = L.mla_decode_paged_noalloc
+    if fn.restype is not ctypes.c_int or fn.argtypes is None:
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fn.argtypes = [P, P, I, P, I, P, I, I, I, P, P, I, F, I, P, P, P, P]
+        fn.restype = I
+    for t, name, dt in ((q_abs, "q_abs", torch.bfloat16), (kv_cache, "kv_cache", torch.bfloat16),
+                        (block_table, "block_table", torch.int32), (cache_seqlens, "cache_seqlens", torch.int32),
+                        (tile_meta, "tile_meta", torch.int32), (num_splits, "num_splits", torch.int32),
+                        (o_lat, "o_lat", torch.bfloat16), (lse, "lse", torch.float32)):
+        _need(t, name, dt)
+    if device_status is not None:
+        _need(device_status, "device_status", torch.int32)
+    B, s_q, H, _ = q_abs.shape
+    _check("mla_decode_paged_noalloc", fn(
+        _p(q_abs), _p(kv_cache), kv_cache.shape[0], _p(block_table), block_table.shape[1], _p(cache_seqlens),
+        B, s_q, H, _p(tile_meta), _p(num_splits), tile_meta.shape[0], float(softmax_scale), int(bool(causal)),
+        _p(o_lat), _p(lse), _p(device_status), _stream(stream)))
+    return o_lat, lse
