@@ -260,12 +260,15 @@ int mla_debug_gather(const mla_bf16_t* kv_cache, int num_blocks, const int32_t* 
 
 /*
  * One-tile tcgen05 check: D[128, N] = A[128, K] * B[K, N] in fp32, the same
- * shared-memory layouts the decode kernel uses. A: bf16 [128, K] row-major
- * (K-major). b_kmajor = 1: B given as bf16 [N, K] row-major (K-major, like the
- * key tile); b_kmajor = 0: B given as bf16 [K, N] row-major (N-major, like the
- * value tile). K in {64, 128, ..., 576}, N in {64, 128, 256}. d: fp32 [128, N].
+ * operand layouts the decode kernel uses. A: bf16 [128, K] row-major
+ * (K-major); a_tmem = 0 reads it from 128-byte-swizzled shared memory, a_tmem = 1
+ * from tensor memory (row m in lane m, bf16 pairs per 32-bit column, as the
+ * decode kernel holds the absorbed query and P). b_kmajor = 1: B given as bf16
+ * [N, K] row-major (K-major, like the key tile); b_kmajor = 0: B given as bf16
+ * [K, N] row-major (N-major, like the value tile). K in {64, 128, ..., 576},
+ * N in {64, 128, 256}. d: fp32 [128, N].
  */
-int mla_debug_mma(const mla_bf16_t* a, const mla_bf16_t* b, int K, int N, int b_kmajor, float* d,
+int mla_debug_mma(const mla_bf16_t* a, const mla_bf16_t* b, int K, int N, int b_kmajor, int a_tmem, float* d,
                   mla_stream_t stream);
 
 #ifdef __cplusplus

@@ -73,7 +73,7 @@ def lib() -> ctypes.CDLL:
         L.mla_read_device_error.restype = I
         L.mla_debug_gather.argtypes = [P, I, P, I, P, I, I, P, P]
         L.mla_debug_gather.restype = I
-        L.mla_debug_mma.argtypes = [P, P, I, I, I, P, P]
+        L.mla_debug_mma.argtypes = [P, P, I, I, I, I, P, P]
         L.mla_debug_mma.restype = I
         _lib = L
         return L
@@ -254,14 +254,17 @@ def mla_debug_gather(kv_cache: torch.Tensor, block_table: torch.Tensor, cache_se
     return out
 
 
-def mla_debug_mma(a: torch.Tensor, b: torch.Tensor, b_kmajor: bool, stream=None) -> torch.Tensor:
-    """a [128, K]; b [N, K] if b_kmajor else [K, N]; returns fp32 [128, N] = a . B."""
+def mla_debug_mma(a: torch.Tensor, b: torch.Tensor, b_kmajor: bool, a_tmem: bool = False,
+                  stream=None) -> torch.Tensor:
+    """a [128, K]; b [N, K] if b_kmajor else [K, N]; returns fp32 [128, N] = a . B
+    (A read from tensor memory when a_tmem)."""
     _need(a, "a", torch.bfloat16, 2)
     _need(b, "b", torch.bfloat16, 2)
     K = a.shape[1]
     N = b.shape[0] if b_kmajor else b.shape[1]
     d = torch.empty((128, N), dtype=torch.float32, device=a.device)
-    _check("mla_debug_mma", lib().mla_debug_mma(_p(a), _p(b), K, N, int(bool(b_kmajor)), _p(d), _stream(stream)))
+    _check("mla_debug_mma", lib().mla_debug_mma(_p(a), _p(b), K, N, int(bool(b_kmajor)), int(bool(a_tmem)), _p(d),
+                                                _stream(stream)))
     return d
 
 

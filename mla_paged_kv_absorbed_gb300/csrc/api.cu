@@ -98,8 +98,12 @@ int head_gemm(const void* a, int a_row_elems, const void* w, int K, int N, int n
     const uint64_t b_dims[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)H};
     const uint64_t b_strides[2] = {(uint64_t)N * 2, (uint64_t)K * N * 2};
     const uint32_t b_box[3] = {64, 64, 1};
+    CUtensorMap tm_out;
+    const uint64_t o_dims[3] = {(uint64_t)out_row_elems, (uint64_t)H, (uint64_t)R};
+    const uint64_t o_strides[2] = {(uint64_t)out_row_elems * 2, (uint64_t)H * out_row_elems * 2};
     if (!make_tmap(&tm_a, a, 3, a_dims, a_strides, a_box)) return MLA_ERR_CUDA;
     if (!make_tmap(&tm_b, w, 3, b_dims, b_strides, b_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) return MLA_ERR_CUDA;
+    if (!make_tmap(&tm_out, out, 3, o_dims, o_strides, a_box)) return MLA_ERR_CUDA;
     GemmArgs args;
     args.R = R;
     args.H = H;
@@ -109,7 +113,7 @@ int head_gemm(const void* a, int a_row_elems, const void* w, int K, int N, int n
     args.out = out;
     args.out_row_elems = out_row_elems;
     args.rope_src = rope_src;
-    return cuda_status(launch_head_gemm(&tm_a, &tm_b, args, g_wait_ns.load(), nullptr, stream));
+    return cuda_status(launch_head_gemm(&tm_a, &tm_b, &tm_out, args, g_wait_ns.load(), stream));
 }
 
 }  // namespace
@@ -211,19 +215,16 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
     int dev = check_device();
     if (dev != MLA_OK) return dev;
 
-    CUtensorMap tm_q, tm_kv;
-    const uint64_t q_dims[3] = {(uint64_t)kDQK, (uint64_t)H, (uint64_t)B * s_q};
-    const uint64_t q_strides[2] = {(uint64_t)kDQK * 2, (uint64_t)H * kDQK * 2};
-    const uint32_t q_box[3] = {64, (uint32_t)H, 1};
+    CUtensorMap tm_kv;
     const uint64_t kv_dims[2] = {(uint64_t)kDQK, (uint64_t)num_blocks * kPage};
     const uint64_t kv_strides[1] = {(uint64_t)kDQK * 2};
     const uint32_t kv_box[2] = {64, (uint32_t)kPage};
-    if (!make_tmap(&tm_q, q_abs, 3, q_dims, q_strides, q_box)) return MLA_ERR_CUDA;
     if (!make_tmap(&tm_kv, kv_cache, 2, kv_dims, kv_strides, kv_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
         return MLA_ERR_CUDA;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     DecodeArgs a;
+    a.q_abs = q_abs;
     a.block_table = block_table;
     a.mbps = max_blocks_per_seq;
     a.seqlens = cache_seqlens;
@@ -243,7 +244,7 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
     a.err = reinterpret_cast<int*>(ws);
     a.wait_ns = g_wait_ns.load();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_decode(&tm_q, &tm_kv, a, st);
+    cudaError_t e = launch_decode(&tm_kv, a, st);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     e = launch_combine(num_splits, B, s_q, H, a.o_part, a.lse_part, o_lat, lse, st);
     return cuda_status(e);
@@ -277,10 +278,10 @@ int mla_debug_gather(const mla_bf16_t* kv_cache, int num_blocks, const int32_t* 
                                            num_blocks, out, static_cast<cudaStream_t>(stream)));
 }
 
-int mla_debug_mma(const mla_bf16_t* a, const mla_bf16_t* b, int K, int N, int b_kmajor, float* d,
+int mla_debug_mma(const mla_bf16_t* a, const mla_bf16_t* b, int K, int N, int b_kmajor, int a_tmem, float* d,
                   mla_stream_t stream) {
     if (!a || !b || !d || K <= 0 || K % 64 != 0 || K > 576 || !(N == 64 || N == 128 || N == 256) ||
-        (b_kmajor != 0 && b_kmajor != 1) || !aligned16(a) || !aligned16(b))
+        (b_kmajor != 0 && b_kmajor != 1) || (a_tmem != 0 && a_tmem != 1) || !aligned16(a) || !aligned16(b))
         return MLA_ERR_INVALID_ARG;
     int dev = check_device();
     if (dev != MLA_OK) return dev;
@@ -300,7 +301,7 @@ int mla_debug_mma(const mla_bf16_t* a, const mla_bf16_t* b, int K, int N, int b_
         const uint32_t b_box[2] = {64, 64};
         if (!make_tmap(&tm_b, b, 2, b_dims, b_strides, b_box)) return MLA_ERR_CUDA;
     }
-    return cuda_status(launch_debug_mma(&tm_a, &tm_b, K, N, b_kmajor, d, static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_debug_mma(&tm_a, &tm_b, K, N, b_kmajor, a_tmem, a, d, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

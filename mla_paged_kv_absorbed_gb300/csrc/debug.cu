@@ -60,7 +60,7 @@ constexpr int kMmaSmem = 16384 + 32768 + 64 + 1024;
 
 __global__ void __launch_bounds__(kMmaThreads, 1)
     mma_tile_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, int K, int N,
-                    int b_kmajor, float* __restrict__ d) {
+                    int b_kmajor, int a_tmem, const __nv_bfloat16* __restrict__ a_glob, float* __restrict__ d) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;              // [128 rows x 64] K-major, 16 KB
@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         fence_mbarrier_init_cluster();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 256);
+        tmem_alloc(tmem_slot, 512);  // D in columns [0, N), A (when in TMEM) in [256, 288)
         tmem_relinquish();
     }
     tc_fence_before();
@@ -97,15 +97,29 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 for (int j = 0; j < N / 64; ++j) tma_load_2d(sB + j * 8192, &tm_b, full, 64 * j, 64 * kc);
             }
         }
+        if (a_tmem) {
+            // row t of this K chunk -> TMEM lane t, 32 columns of bf16 pairs
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(a_glob + (size_t)threadIdx.x * K + 64 * kc);
+            uint32_t v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = src[i];
+            tmem_st32(tmem + ((uint32_t)(warp * 32) << 16) + 256u, v);
+            tmem_wait_st();
+            tc_fence_before();
+        }
         ok = __syncthreads_and(mbar_wait(full, kc & 1, nullptr, nullptr, 2000000000LL));
         tc_fence_after();
         if (ok && threadIdx.x == 0) {
             const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
             for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = desc_sw128(a_base + kk * 32, 0, 1024);
                 const uint64_t bd = b_kmajor ? desc_sw128(b_base + kk * 32, 0, 1024)
                                              : desc_sw128(b_base + kk * 2048, 8192, 1024);
-                mma_bf16_ss(tmem, ad, bd, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+                if (a_tmem) {
+                    mma_bf16_ts(tmem, tmem + 256u + 8u * kk, bd, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+                } else {
+                    const uint64_t ad = desc_sw128(a_base + kk * 32, 0, 1024);
+                    mma_bf16_ss(tmem, ad, bd, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+                }
             }
             mma_commit(done);
         }
@@ -123,7 +137,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
@@ -138,11 +152,12 @@ cudaError_t launch_debug_gather(const CUtensorMap* tm_kv, const int32_t* block_t
     return cudaGetLastError();
 }
 
-cudaError_t launch_debug_mma(const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, int N, int b_kmajor, float* d,
-                             cudaStream_t stream) {
+cudaError_t launch_debug_mma(const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, int N, int b_kmajor, int a_tmem,
+                             const void* a, float* d, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(mma_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
     if (e != cudaSuccess) return e;
-    mma_tile_kernel<<<1, kMmaThreads, kMmaSmem, stream>>>(*tm_a, *tm_b, K, N, b_kmajor, d);
+    mma_tile_kernel<<<1, kMmaThreads, kMmaSmem, stream>>>(*tm_a, *tm_b, K, N, b_kmajor, a_tmem,
+                                                         static_cast<const __nv_bfloat16*>(a), d);
     return cudaGetLastError();
 }
 

@@ -16,18 +16,28 @@
 // softmax is bit-identical on both sides).
 //
 // Each CTA therefore needs 5 of the 9 64-column chunks of every page
-// (r = 0: chunks 0-4, r = 1: chunks 4-8; chunk 4 is shared) and of the query.
+// (r = 0: chunks 0-4, r = 1: chunks 4-8; chunk 4 is shared).
+// Tensor memory of a CTA (512 columns): O_r [0, 256), its 288 query dims as
+// the A operand [256, 400), S_r [416, 480), P in bf16 [480, 512).
 // Per page (64 tokens):
-//   TMA      5 x [64 x 64] bf16 boxes of the page into a 2-stage ring
+//   TMA      5 x [64 x 64] bf16 boxes of the page into a 4-stage ring
 //            (128-byte swizzle), addressed through the block table;
-//   tcgen05  S_r[128 x 64]   = Q'_r . K_r^T       (18 K-steps, fp32 in TMEM);
-//   exchange S = S_0 + S_1 via DSMEM (32 KB each way);
+//   tcgen05  S_r[128 x 64] = Q'_r . K_r^T (18 K-steps, A from TMEM);
+//   exchange the fp32 partial, scaled to log2 units, is staged in shared
+//            memory and sent to the peer with one 32 KB bulk DSMEM copy that
+//            completes on the peer's mbarrier; both CTAs then add the same two
+//            values in the same order (x_0 + x_1), so the softmax is
+//            bit-identical on both sides (fp16 partials were tried: their
+//            rounding moves lse by up to 1.3e-3 on N(0,1) absorbed queries);
 //   softmax  one thread per row: mask, row max, lazy rescale (only when the
-//            max grows by more than 2^8), p = exp2(x - m), P bf16 to smem;
-//   tcgen05  O_r[128 x 256] += P . V_r            (V_r = chunks 0-3 of the stage,
-//            read as an MN-major operand).
-// Roles (8 warps): warp 0 TMA producer, warp 1 MMA issuer (and TMEM owner),
-// warps 4-7 softmax + epilogue; warps 2-3 only join the final barriers.
+//            max grows by more than 2^8), p = exp2(x - m), P bf16 to TMEM;
+//   tcgen05  O_r[128 x 256] += P . V_r (A = P from TMEM; V_r = chunks 0-3 of
+//            the stage, read as an MN-major operand).
+// Roles (10 warps): warps 0-3 exchange (S from TMEM -> staged -> bulk copy;
+// page g+1 goes out while the softmax of page g runs), warps 4-7 query load, softmax and
+// epilogue, warp 8 TMA producer, warp 9 MMA issuer and TMEM owner. The MMA
+// issuer polls its inputs and issues whichever of the next score product and
+// the oldest pending P.V product is ready, so score products run ahead.
 // Every wait is bounded; on expiry the kernel records MLA_ERR_TIMEOUT, drains
 // its copies and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -39,27 +49,28 @@
 namespace mla {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 320;
 constexpr int kRows = 128;
 constexpr int kChunks = 5;
-constexpr int kStages = 2;
+constexpr int kStages = 4;
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
 
-constexpr int kQChunkBytes = kRows * 128;   // 16 KB: 128 rows x 64 bf16
 constexpr int kKVChunkBytes = kPage * 128;  // 8 KB: 64 tokens x 64 bf16
-constexpr int kQBytes = kChunks * kQChunkBytes;
 constexpr int kStageBytes = kChunks * kKVChunkBytes;
-constexpr int kPBytes = kRows * 128;         // P: 128 rows x 64 bf16
-constexpr int kXBytes = kRows * kPage * 4;   // partial scores: 128 x 64 fp32
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffP = kOffKV + kStages * kStageBytes;
-constexpr int kOffX = kOffP + kPBytes;
-constexpr int kOffBar = kOffX + kXBytes;
+constexpr int kXBytes = kRows * kPage * 4;   // one page of partial scores: 128 x 64 fp32
+constexpr int kOffKV = 0;
+constexpr int kOffSend = kOffKV + kStages * kStageBytes;  // this CTA's partial
+constexpr int kOffRecv = kOffSend + kXBytes;               // the peer's partial
+constexpr int kOffBar = kOffRecv + kXBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;
 
 constexpr uint32_t kTmemO = 0;     // 256 columns
-constexpr uint32_t kTmemS = 256;   // 64 columns
+constexpr uint32_t kTmemQ = 256;   // 144 columns: 288 bf16 query dims per row
+constexpr uint32_t kTmemS = 416;   // 64 columns
+constexpr uint32_t kTmemP = 480;   // 32 columns: 64 bf16 probabilities per row
 constexpr uint32_t kTmemCols = 512;
+constexpr int kQWords = 144;       // 32-bit words of one row's query slice
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: tolerate growth up to 2^8 before rescaling O
 
@@ -70,7 +81,10 @@ struct Bars {
     uint64_t s_full, s_free;
     uint64_t p_full, pv_done;
     uint64_t o_free;
-    uint64_t x_full, peer_free;
+    uint64_t x_full;     // own expect_tx arrival + the peer's copy bytes
+    uint64_t sx_ready;   // one arrival per exchange warp: own partial staged
+    uint64_t c_done;     // one arrival per softmax warp: both partials read
+    uint64_t send_free;  // local softmax done + peer softmax done with the buffer pair
     uint64_t drain;
     uint32_t tmem_slot;
     int abort;
@@ -115,19 +129,80 @@ struct ItemIter {
     }
 };
 
+// Walks the pages of a part in order, with their item context.
+struct PageIter {
+    ItemIter items;
+    Item it;
+    int j, g, n_items;  // page within the batch, page counter, items started
+    bool valid;
+    __device__ void init(const DecodeArgs& args, int part) {
+        items.init(args, part);
+        g = 0;
+        n_items = 0;
+        valid = items.next(it);
+        j = valid ? it.lo : 0;
+        if (valid) n_items = 1;
+    }
+    __device__ bool first_of_item() const { return j == it.lo; }
+    __device__ bool last_of_item() const { return j == it.hi - 1; }
+    __device__ void advance() {
+        ++g;
+        if (++j >= it.hi) {
+            valid = items.next(it);
+            if (valid) {
+                j = it.lo;
+                ++n_items;
+            }
+        }
+    }
+};
+
 __device__ __forceinline__ int visible_keys(int seqlen, int s_q, int s, int causal) {
     int n = causal ? seqlen - s_q + s + 1 : seqlen;
     return n < 0 ? 0 : (n > seqlen ? seqlen : n);
 }
 
+__device__ __forceinline__ const uint4* query_row(const DecodeArgs& args, int b, int s, int row, uint32_t rank) {
+    return reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.q_abs) +
+                                          (((size_t)b * args.s_q + s) * args.H + row) * kDQK + 288 * rank);
+}
+
+// Query slice of one row into TMEM (the A operand of the score MMA): this CTA's
+// 288 dims as 144 words of bf16 pairs; rows >= H get zeros. All 36 loads are
+// in flight together (one memory latency, not nine).
+__device__ __forceinline__ void load_query(const DecodeArgs& args, const Item& it, int s, int row, uint32_t rank,
+                                           uint32_t taddr) {
+    const bool live = row < args.H;
+    const uint4* src = query_row(args, it.b, s, live ? row : 0, rank);
+    uint32_t v[kQWords];
+#pragma unroll
+    for (int i = 0; i < kQWords / 4; ++i) {
+        const uint4 w = live ? src[i] : make_uint4(0, 0, 0, 0);
+        v[4 * i] = w.x;
+        v[4 * i + 1] = w.y;
+        v[4 * i + 2] = w.z;
+        v[4 * i + 3] = w.w;
+    }
+#pragma unroll
+    for (int c = 0; c < kQWords; c += 16) tmem_st16(taddr + (uint32_t)c, v + c);
+    tmem_wait_st();
+}
+
+// Warm L2 with the query slice of a row that will be loaded one item later.
+__device__ __forceinline__ void prefetch_query(const DecodeArgs& args, int b, int s, int row, uint32_t rank) {
+    if (row >= args.H) return;
+    const char* p = reinterpret_cast<const char*>(query_row(args, b, s, row, rank));
+#pragma unroll
+    for (int i = 0; i < 576; i += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + i));
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv, DecodeArgs args) {
+    decode_kernel(const __grid_constant__ CUtensorMap tm_kv, DecodeArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem + kOffQ;
     uint8_t* sKV = smem + kOffKV;
-    uint8_t* sP = smem + kOffP;
-    float4* sX = reinterpret_cast<float4*>(smem + kOffX);
+    float4* sSend = reinterpret_cast<float4*>(smem + kOffSend);  // [16][128] float4
+    float4* sRecv = reinterpret_cast<float4*>(smem + kOffRecv);  // [16][128] float4
     Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
     volatile int* abort = &bars->abort;
 
@@ -145,241 +220,265 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->kv_full[i], 1);
             mbar_init(&bars->kv_empty[i], 1);
         }
-        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_full, kRows);
         mbar_init(&bars->q_empty, 1);
         mbar_init(&bars->s_full, 1);
         mbar_init(&bars->s_free, kRows);
         mbar_init(&bars->p_full, kRows);
         mbar_init(&bars->pv_done, 1);
         mbar_init(&bars->o_free, kRows);
-        mbar_init(&bars->x_full, kRows);     // arrivals come from the peer CTA
-        mbar_init(&bars->peer_free, kRows);  // arrivals come from the peer CTA
+        mbar_init(&bars->x_full, 1);
+        mbar_init(&bars->sx_ready, 4);
+        mbar_init(&bars->c_done, 4);
+        mbar_init(&bars->send_free, 2);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_mbarrier_init_cluster();
-        tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_kv);
     }
-    if (args.H < kRows) {
-        // query rows >= H are never loaded: keep them zero for every item
-        for (int i = threadIdx.x; i < kChunks * (kRows - args.H) * 8; i += kThreads) {
-            const int c = i / ((kRows - args.H) * 8);
-            const int rem = i % ((kRows - args.H) * 8);
-            const int r = args.H + rem / 8;
-            reinterpret_cast<uint4*>(sQ + c * kQChunkBytes + r * 128)[rem % 8] = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-    }
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         tmem_alloc(&bars->tmem_slot, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync_all();  // the peer's barriers are initialised before any remote arrive
+    cluster_sync_all();  // the peer's barriers are initialised before any remote arrive or copy
     tc_fence_after();
     const uint32_t tmem = bars->tmem_slot;
 
-    if (warp == 0) {
+    if (warp == kWarpProducer) {
         // ------------------------------------------------------- producer --
         if (lane == 0) {
-            ItemIter iter;
-            iter.init(args, part);
-            Item it;
-            int g = 0, n_items = 0;
+            PageIter pg;
+            pg.init(args, part);
             bool ok = true;
-            const uint32_t q_bytes = (uint32_t)(kChunks * args.H * 128);
-            while (ok && iter.next(it)) {
-                if (n_items > 0) ok = mbar_wait(&bars->q_empty, (n_items - 1) & 1, abort, err, wait_ns);
+            for (; pg.valid; pg.advance()) {
+                const int g = pg.g, st = g % kStages;
+                if (g >= kStages) ok = mbar_wait(&bars->kv_empty[st], ((g / kStages) - 1) & 1, abort, err, wait_ns);
                 if (!ok) break;
-                mbar_arrive_expect_tx(&bars->q_full, q_bytes);
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(sQ + c * kQChunkBytes, &tm_q, &bars->q_full, 64 * (4 * (int)rank + c), 0,
-                                it.b * args.s_q + s);
-                ++n_items;
-                for (int j = it.lo; j < it.hi; ++j, ++g) {
-                    const int st = g % kStages;
-                    if (g >= kStages) ok = mbar_wait(&bars->kv_empty[st], ((g / kStages) - 1) & 1, abort, err, wait_ns);
-                    if (!ok) break;
-                    int blk = j < args.mbps ? args.block_table[(size_t)it.b * args.mbps + j] : -1;
-                    if (blk < 0 || blk >= args.num_blocks) {
-                        record_error(err, kErrBadBlock);
-                        blk = 0;
-                    }
-                    mbar_arrive_expect_tx(&bars->kv_full[st], (uint32_t)kStageBytes);
-                    uint8_t* dst = sKV + st * kStageBytes;
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_load_2d(dst + c * kKVChunkBytes, &tm_kv, &bars->kv_full[st], 64 * (4 * (int)rank + c),
-                                    blk * kPage);
+                const int j = pg.j;
+                int blk = j < args.mbps ? args.block_table[(size_t)pg.it.b * args.mbps + j] : -1;
+                if (blk < 0 || blk >= args.num_blocks) {
+                    record_error(err, kErrBadBlock);
+                    blk = 0;
                 }
+                mbar_arrive_expect_tx(&bars->kv_full[st], (uint32_t)kStageBytes);
+                uint8_t* dst = sKV + st * kStageBytes;
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_2d(dst + c * kKVChunkBytes, &tm_kv, &bars->kv_full[st], 64 * (4 * (int)rank + c),
+                                blk * kPage);
             }
+            const int g = pg.g;
             // drain: wait for the last load issued into each buffer
             for (int gg = g - kStages > 0 ? g - kStages : 0; gg < g; ++gg)
                 mbar_wait(&bars->kv_full[gg % kStages], (gg / kStages) & 1, nullptr, err, kDrainNs);
-            if (n_items > 0) mbar_wait(&bars->q_full, (n_items - 1) & 1, nullptr, err, kDrainNs);
         }
-    } else if (warp == 1) {
+    } else if (warp == kWarpMma) {
         // ----------------------------------------------------- MMA issuer --
         constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kPage, false, false);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, 256, false, true);
-        ItemIter iter;
-        iter.init(args, part);
-        Item it;
-        int g = 0, n_items = 0;
-        bool ok = true;
-        bool issued_any = false;
-        // the page whose P.V product is still to be issued
-        bool pend = false;
-        int pend_st = 0, pend_g = 0, pend_item = 0;
-        bool pend_first = false;
-
-        auto issue_pv = [&]() -> bool {
-            if (!warp_wait(&bars->p_full, pend_g & 1, abort, err, wait_ns)) return false;
-            if (pend_first && pend_item >= 1 &&
-                !warp_wait(&bars->o_free, (pend_item - 1) & 1, abort, err, wait_ns))
-                return false;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t p_base = smem_u32(sP);
-                const uint32_t v_base = smem_u32(sKV + pend_st * kStageBytes);
-#pragma unroll
-                for (int kk = 0; kk < kPage / 16; ++kk) {
-                    const uint64_t ad = desc_sw128(p_base + kk * 32, 0, 1024);
-                    const uint64_t bd = desc_sw128(v_base + kk * 2048, kKVChunkBytes, 1024);
-                    mma_bf16_ss(tmem + kTmemO, ad, bd, idesc_pv, (!pend_first || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(&bars->pv_done);
-                mma_commit(&bars->kv_empty[pend_st]);
-            }
-            __syncwarp();
-            pend = false;
-            return true;
-        };
-
-        while (ok && iter.next(it)) {
-            ok = warp_wait(&bars->q_full, n_items & 1, abort, err, wait_ns);
-            if (!ok) break;
-            for (int j = it.lo; j < it.hi && ok; ++j, ++g) {
-                const int st = g % kStages;
-                ok = warp_wait(&bars->kv_full[st], (g / kStages) & 1, abort, err, wait_ns);
-                if (!ok) break;
-                uint8_t* stage = sKV + st * kStageBytes;
-                const int tail_rows = (j == it.nblk - 1) ? it.seqlen - j * kPage : kPage;
-                if (tail_rows < kPage) {
-                    // rows past seqlen hold arbitrary bytes: zero them so that
-                    // 0-probability columns cannot inject NaN/Inf into P.V
-                    const int per_chunk = (kPage - tail_rows) * 8;  // 16-byte words
-                    for (int i = lane; i < kChunks * per_chunk; i += 32) {
-                        const int c = i / per_chunk, w = i % per_chunk;
-                        reinterpret_cast<uint4*>(stage + c * kKVChunkBytes + tail_rows * 128)[w] = make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                }
-                if (g >= 1) ok = warp_wait(&bars->s_free, (g - 1) & 1, abort, err, wait_ns);
-                if (!ok) break;
-                tc_fence_after();
+        PageIter ps, pp;  // next score product, next P.V product
+        ps.init(args, part);
+        pp.init(args, part);
+        bool ok = true, issued_any = false, q_ready = false;
+        uint64_t t_last = globaltimer_ns();
+        while (ok && pp.valid) {
+            bool progressed = false;
+            // --- score product of page ps.g
+            if (ps.valid) {
+                const int g = ps.g, st = g % kStages;
+                bool ready = true;
                 if (lane == 0) {
-                    const uint32_t q_base = smem_u32(sQ);
-                    const uint32_t k_base = smem_u32(stage);
-                    // partial score over 18 K-steps of 16 dims: [288 r, 288 r + 288)
-                    const int step0 = rank == 0 ? 0 : 2;  // first K-step inside local chunk 0
-#pragma unroll
-                    for (int t = 0; t < 18; ++t) {
-                        const int ls = step0 + t;  // local K-step index
-                        const int c = ls >> 2, kk = ls & 3;
-                        const uint64_t ad = desc_sw128(q_base + c * kQChunkBytes + kk * 32, 0, 1024);
-                        const uint64_t bd = desc_sw128(k_base + c * kKVChunkBytes + kk * 32, 0, 1024);
-                        mma_bf16_ss(tmem + kTmemS, ad, bd, idesc_s, t > 0 ? 1u : 0u);
-                    }
-                    mma_commit(&bars->s_full);
-                    if (j == it.hi - 1) mma_commit(&bars->q_empty);
+                    if (!q_ready && ps.first_of_item()) q_ready = mbar_test(smem_u32(&bars->q_full), (ps.n_items - 1) & 1);
+                    ready = (q_ready || !ps.first_of_item()) && mbar_test(smem_u32(&bars->kv_full[st]), (g / kStages) & 1) &&
+                            (g == 0 || mbar_test(smem_u32(&bars->s_free), (g - 1) & 1));
                 }
-                __syncwarp();
-                issued_any = true;
-                if (pend) ok = issue_pv();
-                if (!ok) break;
-                pend = true;
-                pend_st = st;
-                pend_g = g;
-                pend_item = n_items;
-                pend_first = (j == it.lo);
+                ready = __shfl_sync(0xffffffffu, ready, 0);
+                if (ready) {
+                    uint8_t* stage = sKV + st * kStageBytes;
+                    const int tail_rows = (ps.j == ps.it.nblk - 1) ? ps.it.seqlen - ps.j * kPage : kPage;
+                    if (tail_rows < kPage) {
+                        // rows past seqlen hold arbitrary bytes: zero them so that
+                        // 0-probability columns cannot inject NaN/Inf into P.V
+                        const int per_chunk = (kPage - tail_rows) * 8;  // 16-byte words
+                        for (int i = lane; i < kChunks * per_chunk; i += 32) {
+                            const int c = i / per_chunk, w = i % per_chunk;
+                            reinterpret_cast<uint4*>(stage + c * kKVChunkBytes + tail_rows * 128)[w] = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t k_base = smem_u32(stage);
+                        // partial score over 18 K-steps of 16 dims: [288 r, 288 r + 288);
+                        // the query slice in TMEM holds exactly those dims
+                        const int step0 = rank == 0 ? 0 : 2;  // first K-step inside local chunk 0
+#pragma unroll
+                        for (int t = 0; t < 18; ++t) {
+                            const int ls = step0 + t;
+                            const int c = ls >> 2, kk = ls & 3;
+                            const uint64_t bd = desc_sw128(k_base + c * kKVChunkBytes + kk * 32, 0, 1024);
+                            mma_bf16_ts(tmem + kTmemS, tmem + kTmemQ + 8u * t, bd, idesc_s, t > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&bars->s_full);
+                        if (ps.last_of_item()) mma_commit(&bars->q_empty);
+                    }
+                    __syncwarp();
+                    issued_any = true;
+                    if (ps.last_of_item()) q_ready = false;
+                    ps.advance();
+                    progressed = true;
+                }
             }
-            ++n_items;
+            // --- P.V product of page pp.g (its score product was issued earlier)
+            if (pp.g < ps.g || !ps.valid) {
+                const int g = pp.g, st = g % kStages;
+                const bool first = pp.first_of_item();
+                bool ready = true;
+                if (lane == 0)
+                    ready = mbar_test(smem_u32(&bars->p_full), g & 1) &&
+                            (!first || pp.n_items == 1 || mbar_test(smem_u32(&bars->o_free), (pp.n_items - 2) & 1));
+                ready = __shfl_sync(0xffffffffu, ready, 0);
+                if (ready) {
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t v_base = smem_u32(sKV + st * kStageBytes);
+#pragma unroll
+                        for (int kk = 0; kk < kPage / 16; ++kk) {
+                            const uint64_t bd = desc_sw128(v_base + kk * 2048, kKVChunkBytes, 1024);
+                            mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 8u * kk, bd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&bars->pv_done);
+                        mma_commit(&bars->kv_empty[st]);
+                    }
+                    __syncwarp();
+                    pp.advance();
+                    progressed = true;
+                }
+            }
+            if (progressed) {
+                t_last = globaltimer_ns();
+            } else {
+                if (*abort) ok = false;
+                else if ((long long)(globaltimer_ns() - t_last) > wait_ns) {
+                    record_error(err, kErrTimeout);
+                    *abort = 1;
+                    ok = false;
+                }
+                ok = __all_sync(0xffffffffu, ok);
+            }
         }
-        if (ok && pend) ok = issue_pv();
         // drain: every MMA this thread issued has completed before TMEM is freed
         if (issued_any) {
             if (lane == 0) mma_commit(&bars->drain);
             __syncwarp();
             warp_wait(&bars->drain, 0, nullptr, err, kDrainNs);
         }
-    } else if (warp >= 4) {
-        // ---------------------------------------------- softmax + epilogue --
+    } else if (warp < 4) {
+        // ------------------------------------------------------- exchange --
+        const int row = threadIdx.x;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        PageIter pg;
+        pg.init(args, part);
+        bool ok = true;
+        for (; ok && pg.valid; pg.advance()) {
+            const int g = pg.g;
+            ok = warp_wait(&bars->s_full, g & 1, abort, err, wait_ns);
+            if (!ok) break;
+            tc_fence_after();
+            float x[kPage];
+            {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + kTmemS, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]) * args.scale_log2;
+                tmem_ld32(tmem + lane_base + kTmemS + 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) x[32 + c] = __uint_as_float(v[c]) * args.scale_log2;
+            }
+            tc_fence_before();
+            mbar_arrive(&bars->s_free);
+            // the buffer pair was last used by page g - 1: both softmax sides must have read it
+            if (g >= 1) ok = warp_wait(&bars->send_free, (g - 1) & 1, abort, err, wait_ns);
+            if (!ok) break;
+#pragma unroll
+            for (int q = 0; q < kPage / 4; ++q) sSend[q * kRows + row] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->sx_ready);
+            if (row == 0 && mbar_wait(&bars->sx_ready, g & 1, abort, err, wait_ns)) {
+                mbar_arrive_expect_tx(&bars->x_full, (uint32_t)kXBytes);
+                bulk_copy_to_peer(mapa_shared(smem_u32(sRecv), peer), sSend, (uint32_t)kXBytes,
+                                  mapa_shared(smem_u32(&bars->x_full), peer));
+            }
+        }
+    } else if (warp < 8) {
+        // ------------------------------------ query load, softmax, epilogue --
         const int row = threadIdx.x - 128;
         const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
-        const uint32_t x_remote = mapa_shared(smem_u32(sX), peer);
-        const uint32_t xfull_remote = mapa_shared(smem_u32(&bars->x_full), peer);
-        const uint32_t pfree_remote = mapa_shared(smem_u32(&bars->peer_free), peer);
         ItemIter iter;
         iter.init(args, part);
-        Item it;
+        Item it, nxt;
         int g = 0, n_items = 0;
         bool ok = true;
-        while (ok && iter.next(it)) {
+        bool have = iter.next(it);
+        if (have) {
+            load_query(args, it, s, row, rank, tmem + lane_base + kTmemQ);
+            tc_fence_before();
+            mbar_arrive(&bars->q_full);
+        }
+        ItemIter ahead = iter;  // one item ahead of `it`, for L2 prefetch of its query rows
+        while (ok && have) {
+            {
+                Item pf;
+                ItemIter probe = ahead;
+                if (probe.next(pf)) prefetch_query(args, pf.b, s, row, rank);
+            }
             const int n_valid = visible_keys(it.seqlen, args.s_q, s, args.causal);
             float m = -INFINITY, l = 0.f;
             for (int j = it.lo; j < it.hi && ok; ++j, ++g) {
-                ok = warp_wait(&bars->s_full, g & 1, abort, err, wait_ns);
-                if (!ok) break;
-                tc_fence_after();
-                float x[kPage];
-                {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + kTmemS, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]);
-                    tmem_ld32(tmem + lane_base + kTmemS + 32, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) x[32 + c] = __uint_as_float(v[c]);
-                }
-                tc_fence_before();
-                mbar_arrive(&bars->s_free);
-                // swap partial scores with the peer
-                if (g >= 1) ok = warp_wait<true>(&bars->peer_free, (g - 1) & 1, abort, err, wait_ns);
-                if (!ok) break;
-#pragma unroll
-                for (int q = 0; q < kPage / 4; ++q)
-                    st_cluster_v4(x_remote + (uint32_t)((q * kRows + row) * 16), x[4 * q], x[4 * q + 1], x[4 * q + 2],
-                                  x[4 * q + 3]);
-                mbar_arrive_remote(xfull_remote);
-                ok = warp_wait<true>(&bars->x_full, g & 1, abort, err, wait_ns);
+                ok = warp_wait(&bars->sx_ready, g & 1, abort, err, wait_ns);
+                if (ok) ok = warp_wait(&bars->x_full, g & 1, abort, err, wait_ns);
                 if (!ok) break;
                 const int vcount = min(max(n_valid - j * kPage, 0), kPage);
+                float x[kPage];
                 float mx = -INFINITY;
 #pragma unroll
                 for (int q = 0; q < kPage / 4; ++q) {
-                    const float4 w = sX[q * kRows + row];
-                    const float wv[4] = {w.x, w.y, w.z, w.w};
+                    const float4 a = sSend[q * kRows + row];
+                    const float4 b = sRecv[q * kRows + row];
+                    const float av[4] = {a.x, a.y, a.z, a.w};
+                    const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int c = 4 * q + e;
-                        // S_0 + S_1 in this order on both CTAs
-                        const float sc = rank == 0 ? x[c] + wv[e] : wv[e] + x[c];
-                        x[c] = c < vcount ? sc * args.scale_log2 : -INFINITY;
+                        // x_0 + x_1 in this order on both CTAs
+                        const float sc = rank == 0 ? av[e] + bv[e] : bv[e] + av[e];
+                        x[c] = c < vcount ? sc : -INFINITY;
                         mx = fmaxf(mx, x[c]);
                     }
                 }
-                mbar_arrive_remote(pfree_remote);
+                // both partials of this page are read: hand the buffer pair back.
+                // The remote arrival only reports that our reads are complete (they
+                // are ordered before it through c_done); the peer's next write into
+                // our receive buffer is its bulk copy, so no cluster-scope release.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->c_done);
+                if (row == 0 && mbar_wait(&bars->c_done, g & 1, abort, err, wait_ns)) {
+                    mbar_arrive(&bars->send_free);
+                    fence_proxy_async_smem();
+                    mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&bars->send_free), peer));
+                }
                 bool pv_waited = false;
                 // lazy rescale: a row moves its reference max only when the new
                 // max exceeds it by more than 2^8. The TMEM read-modify-write of O
                 // is warp-collective, so the whole warp takes it when any of its
                 // rows needs it; rows that do not scale by 1.
                 const bool need = mx > m + kRescaleThreshold;
-                const float alpha = need ? exp2f(m - mx) : 1.f;  // 0 when m = -inf
+                const float alpha = need ? fast_exp2(m - mx) : 1.f;  // 0 when m = -inf
                 if (j > it.lo && __any_sync(0xffffffffu, need)) {
                     ok = warp_wait(&bars->pv_done, (g - 1) & 1, abort, err, wait_ns);
                     if (!ok) break;
@@ -405,22 +504,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < kPage / 2; ++c) {
                     // the row sum takes the fp32 probabilities; only the P.V operand is bf16
-                    const float p0 = exp2f(x[2 * c] - m_use), p1 = exp2f(x[2 * c + 1] - m_use);
+                    const float p0 = fast_exp2(x[2 * c] - m_use), p1 = fast_exp2(x[2 * c + 1] - m_use);
                     l += p0 + p1;
                     pk[c] = pack_bf16x2(p0, p1);
                 }
                 if (g >= 1 && !pv_waited) ok = warp_wait(&bars->pv_done, (g - 1) & 1, abort, err, wait_ns);
                 if (!ok) break;
-                uint8_t* prow = sP + row * 128;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) * 16)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                fence_proxy_async_smem();
+                tmem_st32(tmem + lane_base + kTmemP, pk);
+                tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&bars->p_full);
             }
             if (!ok) break;
+            // the next item's query slice goes in as soon as this item's last score
+            // MMA is done: this item's last P.V product may be issued after the
+            // next item's first score product
+            const bool have_next = iter.next(nxt);
+            ahead = iter;
+            if (have_next) {
+                ok = warp_wait(&bars->q_empty, n_items & 1, abort, err, wait_ns);
+                if (!ok) break;
+                tc_fence_after();
+                load_query(args, nxt, s, row, rank, tmem + lane_base + kTmemQ);
+                tc_fence_before();
+                mbar_arrive(&bars->q_full);
+            }
             // epilogue of the item
             ok = warp_wait(&bars->pv_done, (g - 1) & 1, abort, err, wait_ns);
             if (!ok) break;
@@ -455,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&bars->o_free);
             if (rank == 0 && row_ok) {
+                // lse in natural log: x is in log2 units of the scaled score
                 const float lse_v = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
                 if (it.split)
                     args.lse_part[prow_idx] = lse_v;
@@ -462,15 +571,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     args.lse[orow] = lse_v;
             }
             ++n_items;
+            it = nxt;
+            have = have_next;
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    // the peer may still arrive on our barriers / write our buffers until it
+    // the peer may still arrive on our barriers / copy into our buffers until it
     // has finished its last page: leave together
     cluster_sync_all();
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -504,13 +615,13 @@ cudaLaunchConfig_t make_config(int clusters, cudaStream_t stream, cudaLaunchAttr
 
 }  // namespace
 
-cudaError_t launch_decode(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, const DecodeArgs& args,
+cudaError_t launch_decode(const CUtensorMap* tm_kv, const DecodeArgs& args,
                           cudaStream_t stream) {
     cudaError_t e = prepare_kernel();
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = make_config(args.num_parts * args.s_q, stream, attr);
-    return cudaLaunchKernelEx(&cfg, decode_kernel, *tm_q, *tm_kv, args);
+    return cudaLaunchKernelEx(&cfg, decode_kernel, *tm_kv, args);
 }
 
 // Clusters of the decode kernel that can be resident at once on the current device.

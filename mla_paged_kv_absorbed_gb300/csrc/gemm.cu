@@ -10,7 +10,8 @@
 // lives in TMEM (n_cta fp32 columns), A (activations, K-major) and B (the
 // head's weight, N-major) stream through a TMA ring of 64-wide K chunks in
 // 128-byte-swizzled shared memory. Warp 0 produces, one thread of warp 1
-// issues the MMAs, and all four warps run the epilogue (TMEM -> bf16 -> HBM).
+// issues the MMAs, and all four warps run the epilogue: TMEM -> bf16 -> the
+// (now idle) stage buffers in the same swizzled layout -> TMA tensor stores.
 #include <cuda_bf16.h>
 
 #include "mla_internal.h"
@@ -38,7 +39,7 @@ struct GemmSmem {
 template <int NCTA, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                     GemmArgs args, long long wait_ns) {
+                     const __grid_constant__ CUtensorMap tm_out, GemmArgs args, long long wait_ns) {
     using L = GemmSmem<NCTA, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbarrier_init_cluster();
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
+        tma_prefetch_desc(&tm_out);
     }
     if (warp == 0) {
         tmem_alloc(tmem_slot, NCTA);
@@ -118,25 +120,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     }
 
-    // epilogue: thread t owns output row m0 + t
-    const bool ok = mbar_wait(done, 0, nullptr, err, kDrainNs);
+    // epilogue: thread t owns tile row t (output row m0 + t). Every load and MMA
+    // is complete once `done` fires, so the stage buffers hold the bf16 tile in
+    // 64-column swizzled boxes, which TMA stores (rows past R are clipped).
+    const bool ok = mbar_wait(done, 0, nullptr, err, kDrainNs) && !*abort;
     tc_fence_after();
-    const int row = m0 + threadIdx.x;
-    const bool row_ok = ok && row < args.R && !*abort;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) + ((size_t)row * args.H + h) * args.out_row_elems + n0;
+    const int t = threadIdx.x;
+    const int row = m0 + t;
 #pragma unroll 1
     for (int c = 0; c < NCTA / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), v);
         tmem_wait_ld();
-        if (row_ok) {
-            uint32_t pk[16];
+        uint8_t* box = smem + (c / 2) * (kBM * 128) + t * 128;  // box of 64 columns, row t
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-            uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        for (int i = 0; i < 4; ++i) {
+            const int gidx = (c & 1) * 4 + i;  // 16-byte granule inside the 128-byte row
+            *reinterpret_cast<uint4*>(box + ((gidx ^ (t & 7)) * 16)) =
+                make_uint4(pack_bf16x2(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1])),
+                           pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                           pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                           pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
         }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (t == 0 && ok) {
+        for (int c = 0; c < NCTA / 64; ++c) tma_store_3d(&tm_out, smem + c * (kBM * 128), n0 + 64 * c, h, m0);
+        bulk_commit_group();
+        bulk_wait_group_read0();
     }
     if (args.rope_src != nullptr && blockIdx.x == 0 && row < args.R) {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.rope_src) +
@@ -152,14 +164,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int NCTA, int STAGES>
-cudaError_t launch_variant(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const GemmArgs& args, long long wait_ns,
-                           cudaStream_t stream) {
+cudaError_t launch_variant(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const CUtensorMap* tm_out,
+                           const GemmArgs& args, long long wait_ns, cudaStream_t stream) {
     using L = GemmSmem<NCTA, STAGES>;
     auto kern = head_gemm_kernel<NCTA, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(args.N / NCTA, (args.R + kBM - 1) / kBM, args.H);
-    kern<<<grid, kThreads, L::kBytes, stream>>>(*tm_a, *tm_b, args, wait_ns);
+    kern<<<grid, kThreads, L::kBytes, stream>>>(*tm_a, *tm_b, *tm_out, args, wait_ns);
     return cudaGetLastError();
 }
 
@@ -174,10 +186,10 @@ cudaError_t gemm_error_fetch(int* out, cudaStream_t stream) {
     return cudaMemcpyToSymbolAsync(g_gemm_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, stream);
 }
 
-cudaError_t launch_head_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const GemmArgs& args, long long wait_ns,
-                             int* /*err*/, cudaStream_t stream) {
-    if (args.n_cta == 256) return launch_variant<256, 2>(tm_a, tm_b, args, wait_ns, stream);
-    if (args.n_cta == 128) return launch_variant<128, 4>(tm_a, tm_b, args, wait_ns, stream);
+cudaError_t launch_head_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const CUtensorMap* tm_out,
+                             const GemmArgs& args, long long wait_ns, cudaStream_t stream) {
+    if (args.n_cta == 256) return launch_variant<256, 2>(tm_a, tm_b, tm_out, args, wait_ns, stream);
+    if (args.n_cta == 128) return launch_variant<128, 4>(tm_a, tm_b, tm_out, args, wait_ns, stream);
     return cudaErrorInvalidValue;
 }
 

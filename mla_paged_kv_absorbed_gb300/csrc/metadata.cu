@@ -6,13 +6,13 @@
 // pages form contiguous runs of parts), and the part rows are filled by the
 // batches that open and close them. Chunked block scans give the running
 // batch starts, the previous batch's last key and the piece numbering, so any
-// B fits one 1024-thread block and nothing is stored per batch.
+// B fits one 256-thread block and nothing is stored per batch.
 #include "mla_internal.h"
 
 namespace mla {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
 template <typename T, typename Op>

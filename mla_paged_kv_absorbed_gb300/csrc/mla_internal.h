@@ -39,10 +39,11 @@ struct GemmArgs {
     int out_row_elems;
     const void* rope_src;  // absorb only: q [R, H, 192]; rope part copied to out columns 512..575
 };
-cudaError_t launch_head_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const GemmArgs& args,
-                             long long wait_ns, int* err, cudaStream_t stream);
+cudaError_t launch_head_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const CUtensorMap* tm_out,
+                             const GemmArgs& args, long long wait_ns, cudaStream_t stream);
 
 struct DecodeArgs {
+    const void* q_abs;  // bf16 [B, s_q, H, 576]
     const int32_t* block_table;
     int mbps;
     const int32_t* seqlens;
@@ -62,8 +63,7 @@ struct DecodeArgs {
 cudaError_t gemm_error_fetch(int* out, cudaStream_t stream);
 int decode_max_active_clusters(int device);
 
-cudaError_t launch_decode(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, const DecodeArgs& args,
-                          cudaStream_t stream);
+cudaError_t launch_decode(const CUtensorMap* tm_kv, const DecodeArgs& args, cudaStream_t stream);
 
 cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, const float* o_part,
                            const float* lse_part, void* o_lat, float* lse, cudaStream_t stream);
@@ -73,6 +73,6 @@ cudaError_t launch_debug_gather(const CUtensorMap* tm_kv, const int32_t* block_t
                                 cudaStream_t stream);
 
 cudaError_t launch_debug_mma(const CUtensorMap* tm_a, const CUtensorMap* tm_b, int K, int N, int b_kmajor,
-                             float* d, cudaStream_t stream);
+                             int a_tmem, const void* a, float* d, cudaStream_t stream);
 
 }  // namespace mla

@@ -79,7 +79,7 @@ def test_bad_arguments_are_rejected_on_the_host(L):
     assert L.mla_out_proj(null, null, null, 4, 1, 128, null) == 1
     assert L.mla_decode_paged(null, null, 1, null, 1, null, 1, 1, 128, null, null, 1, ctypes.c_float(0.1), 1,
                               null, null, null, 0, null) == 1
-    assert L.mla_debug_mma(null, null, 64, 64, 1, null, null) == 1
+    assert L.mla_debug_mma(null, null, 64, 64, 1, 0, null, null) == 1
     assert L.mla_read_device_error(null, null) == 1
 
 

@@ -68,13 +68,14 @@ def test_paged_gather_bit_exact(api):
 
 # ------------------------------------------------------------- tcgen05 tile --
 
+@pytest.mark.parametrize("a_tmem", [False, True])
 @pytest.mark.parametrize("K,N,kmajor", [(64, 64, True), (576, 64, True), (320, 64, True), (64, 256, False),
                                         (128, 128, False), (576, 256, True), (192, 64, False)])
-def test_mma_tile(api, K, N, kmajor):
+def test_mma_tile(api, K, N, kmajor, a_tmem):
     g = torch.Generator().manual_seed(K * 1000 + N)
     a = torch.randn(128, K, generator=g).to(torch.bfloat16)
     b = torch.randn((N, K) if kmajor else (K, N), generator=g).to(torch.bfloat16)
-    d = api.mla_debug_mma(a.cuda(), b.cuda(), kmajor).cpu().double()
+    d = api.mla_debug_mma(a.cuda(), b.cuda(), kmajor, a_tmem).cpu().double()
     bm = b.double().T if kmajor else b.double()
     ref = a.double() @ bm
     err = (d - ref).abs().max().item()
