@@ -15,6 +15,7 @@
 #include <math.h>
 
 #include "mla_internal.h"
+#include "ptx.cuh"
 
 namespace mla {
 namespace {
@@ -26,6 +27,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __rest
                                                            const float* __restrict__ lse_part,
                                                            __nv_bfloat16* __restrict__ o_lat,
                                                            float* __restrict__ lse) {
+    // launched as a programmatic dependent of the decode kernel: wait for it
+    griddep_wait();
+    griddep_launch_dependents();
     const int b = blockIdx.x / s_q;
     const int s = blockIdx.x % s_q;
     const int first = num_splits[b];
@@ -78,9 +82,17 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __rest
 
 cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, const float* o_part,
                            const float* lse_part, void* o_lat, float* lse, cudaStream_t stream) {
-    combine_kernel<<<B * s_q, kThreads, 0, stream>>>(num_splits, s_q, H, o_part, lse_part,
-                                                     static_cast<__nv_bfloat16*>(o_lat), lse);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(B * s_q, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, num_splits, s_q, H, o_part, lse_part,
+                              static_cast<__nv_bfloat16*>(o_lat), lse);
 }
 
 }  // namespace mla

@@ -76,6 +76,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // launched as a programmatic dependent: the set-up above overlaps the
+    // previous kernel; no global memory is touched before it has completed
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp == 0 && lane == 0) {
         // producer
@@ -170,9 +174,17 @@ cudaError_t launch_variant(const CUtensorMap* tm_a, const CUtensorMap* tm_b, con
     auto kern = head_gemm_kernel<NCTA, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(args.N / NCTA, (args.R + kBM - 1) / kBM, args.H);
-    kern<<<grid, kThreads, L::kBytes, stream>>>(*tm_a, *tm_b, *tm_out, args, wait_ns);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(args.N / NCTA, (args.R + kBM - 1) / kBM, args.H);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::kBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, *tm_a, *tm_b, *tm_out, args, wait_ns);
 }
 
 }  // namespace

@@ -76,6 +76,20 @@ __device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe of a phase (mbarrier.test_wait never suspends the thread,
+// unlike try_wait): for a thread that polls several barriers in turn.
+__device__ __forceinline__ bool mbar_probe(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_test_cluster(uint32_t addr, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -250,6 +264,47 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+    uint32_t v;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr));
+    return v;
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// Barrier `id` over `count` threads that also ANDs a predicate across them:
+// every participant gets the same answer, so a flag that went false in one
+// warp (a timed-out wait) makes all of them leave together.
+__device__ __forceinline__ bool barrier_and(int id, int count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // 2^x on the SFU (ex2.approx, flush-to-zero); exp2(-inf) = +0.
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -315,6 +370,16 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                  : "memory");
 }
 
+// Asynchronous 16-byte store into another CTA's shared memory (addresses from
+// mapa); its bytes complete on that CTA's mbarrier `mbar_cluster`.
+__device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, float a, float b, float c, float d,
+                                            uint32_t mbar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     dst_cluster),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(mbar_cluster)
+                 : "memory");
+}
+
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to the
 // shared memory of another CTA of the cluster; completes `bytes` of transaction
 // count on the destination CTA's mbarrier (addresses from mapa).
@@ -325,6 +390,23 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const vo
             dst_cluster),
         "r"(smem_u32(src)), "r"(bytes), "r"(mbar_cluster)
         : "memory");
+}
+
+// ------------------------------------------------------- dependent launch --
+// With programmatic dependent launch a kernel may start while the previous
+// kernel on the stream is still running; griddep_wait() blocks until that
+// kernel has completed and its memory is visible. griddep_launch_dependents()
+// lets the next kernel start its own launch early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 32-byte global stores (one full sector per thread).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+                 "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
 }
 
 // ------------------------------------------------------------------ misc --
