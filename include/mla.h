@@ -262,8 +262,10 @@ int mla_debug_gather(const mla_bf16_t* kv_cache, int num_blocks, const int32_t* 
  * One-tile tcgen05 check: D[128, N] = A[128, K] * B[K, N] in fp32, the same
  * operand layouts the decode kernel uses. A: bf16 [128, K] row-major
  * (K-major); a_tmem = 0 reads it from 128-byte-swizzled shared memory, a_tmem = 1
- * from tensor memory (row m in lane m, bf16 pairs per 32-bit column, as the
- * decode kernel holds the absorbed query and P). b_kmajor = 1: B given as bf16
+ * from tensor memory written by thread stores, a_tmem = 2 from tensor memory
+ * filled by tcgen05.cp from the swizzled shared tile (row m in lane m, bf16
+ * pairs per 32-bit column, as the decode kernel holds the absorbed query).
+ * b_kmajor = 1: B given as bf16
  * [N, K] row-major (K-major, like the key tile); b_kmajor = 0: B given as bf16
  * [K, N] row-major (N-major, like the value tile). K in {64, 128, ..., 576},
  * N in {64, 128, 256}. d: fp32 [128, N].

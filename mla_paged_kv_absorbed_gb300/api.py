@@ -254,16 +254,17 @@ def mla_debug_gather(kv_cache: torch.Tensor, block_table: torch.Tensor, cache_se
     return out
 
 
-def mla_debug_mma(a: torch.Tensor, b: torch.Tensor, b_kmajor: bool, a_tmem: bool = False,
+def mla_debug_mma(a: torch.Tensor, b: torch.Tensor, b_kmajor: bool, a_tmem: int = 0,
                   stream=None) -> torch.Tensor:
     """a [128, K]; b [N, K] if b_kmajor else [K, N]; returns fp32 [128, N] = a . B
-    (A read from tensor memory when a_tmem)."""
+    (A from shared memory for a_tmem = 0, from tensor memory written by thread
+    stores for 1, or copied in by tcgen05.cp for 2)."""
     _need(a, "a", torch.bfloat16, 2)
     _need(b, "b", torch.bfloat16, 2)
     K = a.shape[1]
     N = b.shape[0] if b_kmajor else b.shape[1]
     d = torch.empty((128, N), dtype=torch.float32, device=a.device)
-    _check("mla_debug_mma", lib().mla_debug_mma(_p(a), _p(b), K, N, int(bool(b_kmajor)), int(bool(a_tmem)), _p(d),
+    _check("mla_debug_mma", lib().mla_debug_mma(_p(a), _p(b), K, N, int(bool(b_kmajor)), int(a_tmem), _p(d),
                                                 _stream(stream)))
     return d
 

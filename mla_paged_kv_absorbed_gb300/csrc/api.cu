@@ -39,13 +39,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// bf16 tensor map with 128-byte swizzle; dims[0] is the contiguous one.
+// Tensor map with 128-byte swizzle (bf16 unless stated); dims[0] is the contiguous one.
 bool make_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-               const uint32_t* box, CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_128B) {
+               const uint32_t* box, CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
+    CUresult r = fn(map, dtype, (cuuint32_t)rank, const_cast<void*>(base),
                     reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides_bytes),
                     reinterpret_cast<const cuuint32_t*>(box), elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -215,14 +216,41 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
     int dev = check_device();
     if (dev != MLA_OK) return dev;
 
-    CUtensorMap tm_kv;
-    const uint64_t kv_dims[2] = {(uint64_t)kDQK, (uint64_t)num_blocks * kPage};
-    const uint64_t kv_strides[1] = {(uint64_t)kDQK * 2};
-    const uint32_t kv_box[2] = {64, (uint32_t)kPage};
-    if (!make_tmap(&tm_kv, kv_cache, 2, kv_dims, kv_strides, kv_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    DecodeMaps maps;
+    // row-group views: 8 rows x 64 dims per 1 KB swizzle atom, chunks of 64 dims 128 B apart
+    const uint64_t kg_dims[4] = {64, 8, (uint64_t)kDQK / 64, (uint64_t)num_blocks * (kPage / 8)};
+    const uint64_t kg_strides[3] = {(uint64_t)kDQK * 2, 128, (uint64_t)kDQK * 2 * 8};
+    const uint32_t kg_box[4] = {64, 8, 3, (uint32_t)(kPage / 8)};
+    if (!make_tmap(&maps.kg, kv_cache, 4, kg_dims, kg_strides, kg_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+        return MLA_ERR_CUDA;
+    const uint64_t v_dims[3] = {64, (uint64_t)num_blocks * kPage, (uint64_t)kDQK / 64};
+    const uint64_t v_strides[2] = {(uint64_t)kDQK * 2, 128};
+    const uint32_t v_box[3] = {64, (uint32_t)kPage, 4};
+    if (!make_tmap(&maps.v, kv_cache, 3, v_dims, v_strides, v_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+        return MLA_ERR_CUDA;
+    const uint64_t rows = (uint64_t)B * s_q;
+    const uint32_t h_box = (uint32_t)(H < 128 ? H : 128), h_store = (uint32_t)(H < 32 ? H : 32);
+    const uint64_t qg_dims[4] = {64, 8, (uint64_t)kDQK / 64, rows * (uint64_t)H / 8};
+    const uint64_t qg_strides[3] = {(uint64_t)kDQK * 2, 128, (uint64_t)kDQK * 2 * 8};
+    const uint32_t qg_box[4] = {64, 8, 3, h_box / 8};
+    if (!make_tmap(&maps.qg, q_abs, 4, qg_dims, qg_strides, qg_box)) return MLA_ERR_CUDA;
+    const uint64_t q_dims[3] = {(uint64_t)kDQK, (uint64_t)H, rows};
+    const uint64_t q_strides[2] = {(uint64_t)kDQK * 2, (uint64_t)H * kDQK * 2};
+    const uint32_t q_box[3] = {64, h_box, 1};
+    if (!make_tmap(&maps.q, q_abs, 3, q_dims, q_strides, q_box)) return MLA_ERR_CUDA;
+    const uint64_t o_dims[3] = {(uint64_t)kDLatent, (uint64_t)H, rows};
+    const uint64_t o_strides[2] = {(uint64_t)kDLatent * 2, (uint64_t)H * kDLatent * 2};
+    const uint32_t o_box[3] = {64, h_store, 1};
+    if (!make_tmap(&maps.o, o_lat, 3, o_dims, o_strides, o_box)) return MLA_ERR_CUDA;
+    const uint64_t pieces = ((uint64_t)B + (uint64_t)num_parts) * s_q;
+    const uint64_t op_dims[3] = {(uint64_t)kDLatent, (uint64_t)H, pieces};
+    const uint64_t op_strides[2] = {(uint64_t)kDLatent * 4, (uint64_t)H * kDLatent * 4};
+    const uint32_t op_box[3] = {32, h_store, 1};
+    if (!make_tmap(&maps.op, ws + wl.o_offset, 3, op_dims, op_strides, op_box, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
         return MLA_ERR_CUDA;
 
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
     DecodeArgs a;
     a.q_abs = q_abs;
     a.block_table = block_table;
@@ -244,7 +272,7 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
     a.err = reinterpret_cast<int*>(ws);
     a.wait_ns = g_wait_ns.load();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_decode(&tm_kv, a, st);
+    cudaError_t e = launch_decode(maps, a, st);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     e = launch_combine(num_splits, B, s_q, H, a.o_part, a.lse_part, o_lat, lse, st);
     return cuda_status(e);
@@ -281,7 +309,7 @@ int mla_debug_gather(const mla_bf16_t* kv_cache, int num_blocks, const int32_t* 
 int mla_debug_mma(const mla_bf16_t* a, const mla_bf16_t* b, int K, int N, int b_kmajor, int a_tmem, float* d,
                   mla_stream_t stream) {
     if (!a || !b || !d || K <= 0 || K % 64 != 0 || K > 576 || !(N == 64 || N == 128 || N == 256) ||
-        (b_kmajor != 0 && b_kmajor != 1) || (a_tmem != 0 && a_tmem != 1) || !aligned16(a) || !aligned16(b))
+        (b_kmajor != 0 && b_kmajor != 1) || (a_tmem < 0 || a_tmem > 2) || !aligned16(a) || !aligned16(b))
         return MLA_ERR_INVALID_ARG;
     int dev = check_device();
     if (dev != MLA_OK) return dev;

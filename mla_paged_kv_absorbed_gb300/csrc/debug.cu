@@ -3,7 +3,9 @@
 //    128-byte swizzle as the decode kernel, then un-swizzles them to HBM;
 //  * a one-tile tcgen05 product D[128 x N] = A[128 x K] . B with the same
 //    shared-memory layouts and descriptors as the decode kernel (K-major B
-//    like the key tile, MN-major B like the value tile).
+//    like the key tile, MN-major B like the value tile); A is read from
+//    shared memory, or from tensor memory filled by tcgen05.st (a_tmem = 1)
+//    or by tcgen05.cp from the swizzled shared tile (a_tmem = 2).
 #include <cuda_bf16.h>
 
 #include "mla_internal.h"
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 for (int j = 0; j < N / 64; ++j) tma_load_2d(sB + j * 8192, &tm_b, full, 64 * j, 64 * kc);
             }
         }
-        if (a_tmem) {
+        if (a_tmem == 1) {
             // row t of this K chunk -> TMEM lane t, 32 columns of bf16 pairs
             const uint32_t* src = reinterpret_cast<const uint32_t*>(a_glob + (size_t)threadIdx.x * K + 64 * kc);
             uint32_t v[32];
@@ -111,6 +113,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         tc_fence_after();
         if (ok && threadIdx.x == 0) {
             const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+            if (a_tmem == 2) {
+                // the A tile goes from shared to tensor memory on the tensor pipe
+                // (tcgen05.cp), ahead of the MMAs that read it
+                for (int kk = 0; kk < 4; ++kk)
+                    tmem_cp_128x256b(tmem + 256u + 8u * kk, desc_sw128(a_base + kk * 32, 0, 1024));
+            }
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t bd = b_kmajor ? desc_sw128(b_base + kk * 32, 0, 1024)
                                              : desc_sw128(b_base + kk * 2048, 8192, 1024);

@@ -7,42 +7,40 @@
 // visible keys, o = sum_t p_t kv_t[0:512] and lse = ln sum_t exp(score_t).
 //
 // Work decomposition. One 2-CTA cluster owns one schedule part for one query
-// token s (all H heads = the 128 rows of every MMA). The fp32 latent output of
-// 128 rows x 512 columns is exactly one SM's tensor memory, so the pair splits
-// it: CTA r keeps O[:, 256r : 256r+256] in TMEM. Both need the full score tile,
-// so the score contraction (576 deep) is split in K instead: CTA r computes
-// the partial S_r over dims [288r, 288r+288) and the two partials are swapped
-// through distributed shared memory and added (S_0 + S_1 in both CTAs, so the
-// softmax is bit-identical on both sides).
+// token s; all H heads are the 128 rows of every MMA. The two CTAs split the
+// work by role:
+//  * the score CTA (rank 0) holds the whole absorbed query of the part's
+//    current batch - dims [0, 512) in TMEM as the A operand, the 64 rope dims
+//    in shared memory - and computes S = Q' K^T for two pages at a time
+//    (N = 128 keys) into one of two TMEM buffers. Its softmax threads (one
+//    per row and page) mask, take the row max, rescale lazily, exponentiate
+//    and ship P (bf16, 128-byte-swizzled like an MMA operand) together with
+//    the per-row rescale factor straight into the value CTA's shared memory
+//    (st.async, counted on the value CTA's mbarrier);
+//  * the value CTA (rank 1) keeps the fp32 output O [128 x 512] in its TMEM
+//    (all 512 columns), loads its own copy of the value rows of each page
+//    (mostly L2 hits: the score CTA has just read the same page), accumulates
+//    O += P . V, rescales O rows when the score CTA moved their reference
+//    max, and writes the normalised rows through shared memory with TMA
+//    stores.
+// Only P crosses between the CTAs (16 KB per page plus 1 KB of factors per
+// pair); no score or exponential is computed twice.
 //
-// Each CTA therefore needs 5 of the 9 64-column chunks of every page
-// (r = 0: chunks 0-4, r = 1: chunks 4-8; chunk 4 is shared).
-// Tensor memory of a CTA (512 columns): O_r [0, 256), its 288 query dims as
-// the A operand [256, 400), S_r [416, 480), P in bf16 [480, 512).
-// Per page (64 tokens):
-//   TMA      5 x [64 x 64] bf16 boxes of the page into a 4-stage ring
-//            (128-byte swizzle), addressed through the block table;
-//   tcgen05  S_r[128 x 64] = Q'_r . K_r^T (18 K-steps, A from TMEM);
-//   exchange each thread scales its row of S_r to log2 units (fp32) and
-//            st.async's it into the peer's receive buffer (double-buffered);
-//            the bytes complete on the peer's mbarrier, so no fence or flag
-//            write is needed. Both CTAs add the same two values in the same
-//            order (x_0 + x_1): the softmax is bit-identical on both sides;
-//   softmax  one thread per row: mask, row max, lazy rescale (only when the
-//            max grows by more than 2^8), p = exp2(x - m), P bf16 to TMEM;
-//   tcgen05  O_r[128 x 256] += P . V_r (A = P from TMEM; V_r = chunks 0-3 of
-//            the stage, read as an MN-major operand).
-// The softmax threads run one page ahead on the exchange: while page g is
-// being normalised, the partial scores of page g+1 are already in flight.
-// Roles (10 warps): warps 0-7 query load, exchange, softmax and epilogue -
-// two warps per TMEM lane quadrant, each owning 32 of a page's 64 columns (and
-// half of the query words and of O); the pair combines its row maxima and row
-// sums through two TMEM columns around a pair barrier - warp 8 TMA producer,
-// warp 9 MMA issuer and TMEM owner. The MMA issuer polls its inputs and issues
-// whichever of the next score product and the oldest pending P.V product is
-// ready.
-// Every wait is bounded; on expiry the kernel records MLA_ERR_TIMEOUT, drains
-// its copies and MMAs, frees TMEM and returns.
+// Loads are few and large: the TMA engine streams whole 24-32 KB boxes at
+// close to HBM speed but only about half of that as 8 KB boxes. Key tiles use
+// a 4-D view of the cache, [8-key group][64-dim chunk][8 keys][64 dims], so
+// one 24 KB box brings three chunks of a page; the two pages of a pair go
+// back to back into one 48 KB ring slot, which is then a valid 128-key MMA
+// operand (8-key groups 3 KB apart). A batch's query comes through the same
+// ring (three 48 KB boxes of 128 rows) and tcgen05.cp moves it into TMEM.
+// Value CTA per page: two 32 KB boxes of [64 keys x 256 value columns], read
+// as an MN-major operand.
+// Roles (10 warps per CTA): warps 0-7 softmax (score CTA) or O rescale and
+// epilogue (value CTA), two warps per TMEM lane quadrant - on the score CTA
+// warp half h owns page h of a pair, on the value CTA O columns
+// [256 h, 256 h + 256); warp 8 TMA producer; warp 9 MMA issuer and TMEM owner.
+// Every wait is bounded; on expiry the kernel records MLA_ERR_TIMEOUT, tells
+// the peer CTA, drains its copies and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -54,45 +52,60 @@ namespace {
 
 constexpr int kThreads = 320;
 constexpr int kRows = 128;
-constexpr int kSoftmaxThreads = 256;  // warps 0-7
-constexpr int kChunks = 5;
-constexpr int kStages = 4;
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 
-constexpr int kKVChunkBytes = kPage * 128;  // 8 KB: 64 tokens x 64 bf16
-constexpr int kStageBytes = kChunks * kKVChunkBytes;
-constexpr int kXBytes = kRows * kPage * 4;   // one page of partial scores: 128 x 64 fp32
-constexpr int kOffKV = 0;
-constexpr int kOffRecv = kOffKV + kStages * kStageBytes;  // 2 buffers: the peer's partials
-constexpr int kOffBar = kOffRecv + 2 * kXBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;
+// ---- shared memory (offsets from a 1024-byte-aligned base) ----
+constexpr int kChunkBytes = kPage * 128;         // [64 rows x 64 bf16], 128-byte swizzle
+constexpr int kGroupChunks = 3;                  // 64-dim chunks per key box
+constexpr int kBoxBytes = kGroupChunks * kChunkBytes;  // one page, three chunks: [8 groups][3 chunks][8 x 128 B]
+constexpr int kSlotBytes = 2 * kBoxBytes;        // two pages (or 128 query rows), three chunks
+constexpr int kGroupStride = kGroupChunks * 1024;      // bytes between 8-row groups inside a slot
+constexpr int kQRopeBytes = kRows * 128;         // [128 rows x 64 rope dims]
+constexpr int kOffBars = 0;
+constexpr int kOffX = 1024;                      // score: row-stat exchange; value: rescale factors and 1/l
+constexpr int kOffRole = 3072;
+// score CTA
+constexpr int kRing = 4;
+constexpr int kOffQRope = kOffRole;              // 2 buffers (batch parity) of the 64 rope query dims
+constexpr int kOffRing = kOffQRope + 2 * kQRopeBytes;
+constexpr int kSmemScore = kOffRing + kRing * kSlotBytes;
+// value CTA
+constexpr int kPSlotBytes = 2 * kRows * 128;     // P of a page pair: two K-chunks [128 rows x 64 keys] bf16
+constexpr int kVRing = 4;
+constexpr int kVSlotBytes = 4 * kChunkBytes;     // [64 keys x 256 value columns]
+constexpr int kOffP = kOffRole;
+constexpr int kOffV = kOffP + 2 * kPSlotBytes;
+constexpr int kSmemValue = kOffV + kVRing * kVSlotBytes;
+constexpr int kSmemBytes = kSmemScore > kSmemValue ? kSmemScore : kSmemValue;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+// one P message: P (32 KB) + rescale factor and 1/l per row (fp32)
+constexpr uint32_t kPMsgBytes = kPSlotBytes + 2 * kRows * 4;
 
-constexpr uint32_t kTmemO = 0;     // 256 columns
-constexpr uint32_t kTmemQ = 256;   // 144 columns: 288 bf16 query dims per row
-constexpr uint32_t kTmemX = 400;   // 4 columns: the warp pair's row max (400, 401) and row sum (402, 403)
-constexpr uint32_t kTmemS = 416;   // 64 columns
-constexpr uint32_t kTmemP = 480;   // 32 columns: 64 bf16 probabilities per row
-constexpr uint32_t kTmemCols = 512;
-constexpr int kQWords = 144;       // 32-bit words of one row's query slice
+// ---- tensor memory ----
+constexpr uint32_t kTmemQ = 0;      // score CTA: query dims [0, 512) as bf16 pairs (256 columns)
+constexpr uint32_t kTmemS0 = 256;   // score CTA: S buffers, 128 columns each
+constexpr uint32_t kTmemS1 = 384;
+constexpr uint32_t kTmemCols = 512; // value CTA: O, all columns
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: tolerate growth up to 2^8 before rescaling O
 
 struct Bars {
-    uint64_t kv_full[kStages];
-    uint64_t kv_empty[kStages];
-    uint64_t q_full, q_empty;
-    uint64_t s_full, s_free;
-    uint64_t p_full, pv_done;
-    uint64_t o_free;
-    uint64_t x_full[2];     // own expect_tx arrival + the peer's st.async bytes
-    uint64_t c_done[2];     // one arrival per softmax warp (8): receive buffer read
-    uint64_t peer_free[2];  // the peer has read its receive buffer: we may write it again
+    // score CTA
+    uint64_t ring_full[kRing], ring_empty[kRing];
+    uint64_t qr_full[2], qr_empty[2];
+    uint64_t q_drained;
+    uint64_t s_full[2], s_free[2];
+    uint64_t p_free[2];  // score CTA; arrivals come from the value CTA
+    // value CTA
+    uint64_t p_full[2];  // own arrive + expect_tx, bytes from the score CTA
+    uint64_t v_full[kVRing], v_empty[kVRing];
+    uint64_t pv_done, o_full, o_ack, o_free[2], stage_done;
     uint64_t drain;
     uint32_t tmem_slot;
     int abort;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= kOffX, "barrier block");
 
 // One work item: the pages [lo, hi) of batch b inside this part.
 struct Item {
@@ -132,31 +145,36 @@ struct ItemIter {
     }
 };
 
-// Walks the pages of a part in order, with their item context.
-struct PageIter {
+// Walks the page pairs of a part in order: pages [j, j + np) of item `it`,
+// np in {1, 2}; pairs never straddle two items.
+struct PairIter {
     ItemIter items;
     Item it;
-    int j, g, n_items;  // page within the batch, page counter, items started
+    int j, np, n, n_items;  // first page, pages in the pair, pair counter, items started
     bool valid;
     __device__ void init(const DecodeArgs& args, int part) {
         items.init(args, part);
-        g = 0;
+        n = 0;
         n_items = 0;
         valid = items.next(it);
-        j = valid ? it.lo : 0;
-        if (valid) n_items = 1;
+        if (valid) {
+            n_items = 1;
+            j = it.lo;
+            np = min(2, it.hi - j);
+        }
     }
     __device__ bool first_of_item() const { return j == it.lo; }
-    __device__ bool last_of_item() const { return j == it.hi - 1; }
+    __device__ bool last_of_item() const { return j + np >= it.hi; }
     __device__ void advance() {
-        ++g;
-        if (++j >= it.hi) {
+        ++n;
+        j += np;
+        if (j >= it.hi) {
             valid = items.next(it);
-            if (valid) {
-                j = it.lo;
-                ++n_items;
-            }
+            if (!valid) return;
+            j = it.lo;
+            ++n_items;
         }
+        np = min(2, it.hi - j);
     }
 };
 
@@ -165,89 +183,578 @@ __device__ __forceinline__ int visible_keys(int seqlen, int s_q, int s, int caus
     return n < 0 ? 0 : (n > seqlen ? seqlen : n);
 }
 
-__device__ __forceinline__ const uint4* query_row(const DecodeArgs& args, int b, int s, int row, uint32_t rank) {
-    return reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.q_abs) +
-                                          (((size_t)b * args.s_q + s) * args.H + row) * kDQK + 288 * rank);
-}
-
-// Half `half` of one row's query slice into TMEM (the A operand of the score
-// MMA): of this CTA's 288 dims (144 words of bf16 pairs), words
-// [72 half, 72 half + 72); rows >= H get zeros. All 18 loads are in flight
-// together.
-__device__ __forceinline__ void load_query(const DecodeArgs& args, const Item& it, int s, int row, uint32_t rank,
-                                           int half, uint32_t taddr) {
-    constexpr int kHalfWords = kQWords / 2;
-    const bool live = row < args.H;
-    const uint4* src = query_row(args, it.b, s, live ? row : 0, rank) + half * (kHalfWords / 4);
-    uint32_t v[kHalfWords];
-#pragma unroll
-    for (int i = 0; i < kHalfWords / 4; ++i) {
-        const uint4 w = live ? src[i] : make_uint4(0, 0, 0, 0);
-        v[4 * i] = w.x;
-        v[4 * i + 1] = w.y;
-        v[4 * i + 2] = w.z;
-        v[4 * i + 3] = w.w;
+__device__ __forceinline__ int checked_block(const DecodeArgs& args, int b, int j, int* err) {
+    int blk = j < args.mbps ? args.block_table[(size_t)b * args.mbps + j] : -1;
+    if (blk < 0 || blk >= args.num_blocks) {
+        record_error(err, kErrBadBlock);
+        blk = 0;
     }
-    const uint32_t dst = taddr + (uint32_t)(half * kHalfWords);
-    tmem_st16(dst, v);
-    tmem_st16(dst + 16, v + 16);
-    tmem_st16(dst + 32, v + 32);
-    tmem_st16(dst + 48, v + 48);
-    tmem_st8(dst + 64, v + 64);
-    tmem_wait_st();
+    return blk;
 }
 
-// Warm L2 with the query slice of a row that will be loaded one item later.
-__device__ __forceinline__ void prefetch_query(const DecodeArgs& args, int b, int s, int row, uint32_t rank) {
-    if (row >= args.H) return;
-    const char* p = reinterpret_cast<const char*>(query_row(args, b, s, row, rank));
+// Waits for the last TMA load issued into each of the `slots` buffers of a
+// ring that has seen `issued` loads, so that no copy is in flight at exit.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int slots, int issued, int* err) {
+    for (int r = issued - slots > 0 ? issued - slots : 0; r < issued; ++r)
+        mbar_wait(&full[r % slots], (r / slots) & 1, nullptr, err, kDrainNs);
+}
+
+// ============================================================== score CTA ==
+__device__ void score_producer(const DecodeMaps& maps, const DecodeArgs& args, Bars* bars, uint8_t* smem, int part,
+                               int s, volatile int* abort) {
+    int* err = args.err;
+    const long long wait_ns = args.wait_ns;
+    uint8_t* ring = smem + kOffRing;
+    const int hq = min(args.H, kRows);
+    const uint32_t qbytes = (uint32_t)hq * 128;                    // rope box
+    const uint32_t qgbytes = (uint32_t)hq * 128 * kGroupChunks;   // query chunk-group box
+    PairIter pi;
+    pi.init(args, part);
+    bool ok = true;
+    int r = 0, nq = 0;  // ring loads issued, rope query loads issued
+    for (; ok && pi.valid; pi.advance()) {
+        const int bs = pi.it.b * args.s_q + s;
+        if (pi.first_of_item()) {
+            // the batch's query: dims [0, 576) through the ring, three chunks per
+            // slot (the MMA warp moves dims [0, 512) into TMEM), and the rope dims
+            // into the rope buffer of its parity
+            for (int g = 0; g < 3; ++g, ++r) {
+                if (r >= kRing) ok = mbar_wait(&bars->ring_empty[r % kRing], ((r / kRing) - 1) & 1, abort, err, wait_ns);
+                if (!ok) break;
+                uint64_t* bar = &bars->ring_full[r % kRing];
+                mbar_arrive_expect_tx(bar, qgbytes);
+                tma_load_4d(ring + (r % kRing) * kSlotBytes, &maps.qg, bar, 0, 0, kGroupChunks * g, bs * args.H / 8);
+            }
+            if (!ok) break;
+            const int qi = pi.n_items - 1;
+            if (qi >= 2) ok = mbar_wait(&bars->qr_empty[qi & 1], ((qi >> 1) - 1) & 1, abort, err, wait_ns);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bars->qr_full[qi & 1], qbytes);
+            tma_load_3d(smem + kOffQRope + (qi & 1) * kQRopeBytes, &maps.q, &bars->qr_full[qi & 1], 512, 0, bs);
+            ++nq;
+        }
+        const int blk0 = checked_block(args, pi.it.b, pi.j, err);
+        const int blk1 = pi.np == 2 ? checked_block(args, pi.it.b, pi.j + 1, err) : 0;
+        for (int g = 0; g < 3; ++g, ++r) {
+            if (r >= kRing) ok = mbar_wait(&bars->ring_empty[r % kRing], ((r / kRing) - 1) & 1, abort, err, wait_ns);
+            if (!ok) break;
+            uint8_t* dst = ring + (r % kRing) * kSlotBytes;
+            uint64_t* bar = &bars->ring_full[r % kRing];
+            mbar_arrive_expect_tx(bar, (uint32_t)pi.np * kBoxBytes);
+            tma_load_4d(dst, &maps.kg, bar, 0, 0, kGroupChunks * g, blk0 * (kPage / 8));
+            if (pi.np == 2) tma_load_4d(dst + kBoxBytes, &maps.kg, bar, 0, 0, kGroupChunks * g, blk1 * (kPage / 8));
+        }
+    }
+    drain_ring(bars->ring_full, kRing, r, err);
+    drain_ring(bars->qr_full, 2, nq, err);
+}
+
+// Returns false when it gave up (timeout or abort).
+__device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uint32_t tmem, int part,
+                          volatile int* abort) {
+    int* err = args.err;
+    const long long wait_ns = args.wait_ns;
+    const int lane = threadIdx.x & 31;
+    uint8_t* ring = smem + kOffRing;
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, 2 * kPage, false, false);
+    PairIter pi;
+    pi.init(args, part);
+    bool ok = true, issued = false;
+    int r = 0;
+    for (; ok && pi.valid; pi.advance()) {
+        const int n = pi.n, buf = n & 1, qi = pi.n_items - 1;
+        if (pi.first_of_item()) {
+            // the previous batch's last score product has finished reading the query
+            if (qi > 0) ok = warp_wait(&bars->q_drained, (qi - 1) & 1, abort, err, wait_ns);
+            for (int g = 0; ok && g < 3; ++g, ++r) {
+                ok = warp_wait(&bars->ring_full[r % kRing], (r / kRing) & 1, abort, err, wait_ns);
+                if (!ok) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t base = smem_u32(ring + (r % kRing) * kSlotBytes);
+                    // chunks 3g .. 3g + 2 of the query; chunk 8 (rope) stays in shared memory
+                    for (int cc = 0; cc < kGroupChunks; ++cc) {
+                        const int c = kGroupChunks * g + cc;
+                        if (c >= 8) break;
 #pragma unroll
-    for (int i = 0; i < 576; i += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + i));
+                        for (int kk = 0; kk < 4; ++kk)
+                            tmem_cp_128x256b(tmem + kTmemQ + 32u * c + 8u * kk,
+                                             desc_sw128(base + cc * 1024 + 32 * kk, 0, kGroupStride));
+                    }
+                    mma_commit(&bars->ring_empty[r % kRing]);
+                }
+                __syncwarp();
+                issued = true;
+            }
+            if (ok) ok = warp_wait(&bars->qr_full[qi & 1], (qi >> 1) & 1, abort, err, wait_ns);
+            if (!ok) break;
+        }
+        // S buffer `buf` was read by the softmax of pair n - 2
+        if (n >= 2) ok = warp_wait(&bars->s_free[buf], ((n >> 1) - 1) & 1, abort, err, wait_ns);
+        if (!ok) break;
+        const uint32_t d = tmem + (buf ? kTmemS1 : kTmemS0);
+        const uint32_t rope = smem_u32(smem + kOffQRope + (qi & 1) * kQRopeBytes);
+        for (int g = 0; g < 3; ++g, ++r) {
+            ok = warp_wait(&bars->ring_full[r % kRing], (r / kRing) & 1, abort, err, wait_ns);
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t base = smem_u32(ring + (r % kRing) * kSlotBytes);
+#pragma unroll
+                for (int cc = 0; cc < kGroupChunks; ++cc) {
+                    const int c = kGroupChunks * g + cc;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        // keys 0-63 from the first page, 64-127 from the second (8-key groups 3 KB apart)
+                        const uint64_t bd = desc_sw128(base + cc * 1024 + 32 * kk, 0, kGroupStride);
+                        const uint32_t acc = (c | kk) != 0 ? 1u : 0u;
+                        if (c < 8)
+                            mma_bf16_ts(d, tmem + kTmemQ + 32u * c + 8u * kk, bd, idesc_s, acc);
+                        else
+                            mma_bf16_ss(d, desc_sw128(rope + 32 * kk, 0, 1024), bd, idesc_s, acc);
+                    }
+                }
+                mma_commit(&bars->ring_empty[r % kRing]);
+            }
+            __syncwarp();
+            issued = true;
+        }
+        if (!ok) break;
+        if (lane == 0) {
+            mma_commit(&bars->s_full[buf]);
+            if (pi.last_of_item()) {
+                mma_commit(&bars->q_drained);
+                mma_commit(&bars->qr_empty[qi & 1]);
+            }
+        }
+        __syncwarp();
+    }
+    // every MMA and copy this warp issued has completed before TMEM is freed
+    if (issued) {
+        if (lane == 0) mma_commit(&bars->drain);
+        __syncwarp();
+        warp_wait(&bars->drain, 0, nullptr, err, kDrainNs);
+    }
+    return ok;
+}
+
+__device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem, uint32_t tmem, int part, int s,
+                              uint32_t peer, volatile int* abort) {
+    int* err = args.err;
+    const long long wait_ns = args.wait_ns;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;
+    const int pair_bar = 1 + quad;  // named barrier of the two warps sharing these rows
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    // the value CTA's P slots, factor arrays and P barriers (same offsets there)
+    const uint32_t p_remote = mapa_shared(smem_u32(smem + kOffP), peer);
+    const uint32_t x_remote = mapa_shared(smem_u32(smem + kOffX), peer);
+    const uint32_t pfull_remote = mapa_shared(smem_u32(&bars->p_full[0]), peer);
+    float* xch = reinterpret_cast<float*>(smem + kOffX);  // [2 episodes][2 halves][128 rows]
+    PairIter pi;
+    pi.init(args, part);
+    float m = -INFINITY, l = 0.f;
+    int n_valid = 0, xe = 0;
+    bool ok = true;
+    for (; pi.valid; pi.advance()) {
+        // every exit goes through a pair barrier, so both warps of a pair leave together
+        const int n = pi.n, buf = n & 1, k = n & 1;
+        const bool first = pi.first_of_item(), last = pi.last_of_item();
+        if (first) {
+            m = -INFINITY;
+            l = 0.f;
+            n_valid = visible_keys(pi.it.seqlen, args.s_q, s, args.causal);
+        }
+        float x[64];
+        if (ok) ok = warp_wait(&bars->s_full[buf], (n >> 1) & 1, abort, err, wait_ns);
+        if (ok) {
+            tc_fence_after();
+            const uint32_t col = tmem + lane_base + (buf ? kTmemS1 : kTmemS0) + 64u * half;
+            uint32_t v[32];
+            tmem_ld32(col, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]) * args.scale_log2;
+            tmem_ld32(col + 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) x[32 + c] = __uint_as_float(v[c]) * args.scale_log2;
+            tc_fence_before();
+            mbar_arrive(&bars->s_free[buf]);
+        }
+        // keys of this half: page j + half; columns past the visible keys (or of a
+        // missing second page) are masked by selection, so garbage never leaks
+        const int vcount = half < pi.np ? min(max(n_valid - (pi.j + half) * kPage, 0), kPage) : 0;
+        float mh = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+            x[c] = c < vcount ? x[c] : -INFINITY;
+            mh = fmaxf(mh, x[c]);
+        }
+        float* xb = xch + (xe & 1) * (2 * kRows);
+        ++xe;
+        xb[half * kRows + row] = mh;
+        ok = barrier_and(pair_bar, 64, ok);
+        if (!ok) break;
+        const float mx = fmaxf(mh, xb[(half ^ 1) * kRows + row]);
+        // lazy rescale: the reference max moves only when the row max exceeds it
+        // by more than 2^8; both warps of a pair take the same decision
+        const bool need = mx > m + kRescaleThreshold;
+        const float alpha = need ? fast_exp2(m - mx) : 1.f;  // 0 when m = -inf
+        if (need) {
+            l *= alpha;
+            m = mx;
+        }
+        const float m_use = m == -INFINITY ? 0.f : m;
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            // the row sum takes the fp32 probabilities; only the P.V operand is bf16
+            const float p0 = fast_exp2(x[2 * c] - m_use), p1 = fast_exp2(x[2 * c + 1] - m_use);
+            l += p0 + p1;
+            pk[c] = pack_bf16x2(p0, p1);
+        }
+        // slot k held pair n - 2 until the value CTA released it
+        if (ok && n >= 2) ok = warp_wait(&bars->p_free[k], ((n >> 1) - 1) & 1, abort, err, wait_ns);
+        const uint32_t mbar = pfull_remote + (uint32_t)k * 8u;
+        if (ok) {
+            // row `row` of K-chunk `half`: 16-byte word q at position q ^ (row % 8)
+            const uint32_t dst = p_remote + (uint32_t)(k * kPSlotBytes + half * kRows * 128 + row * 128);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                st_async_u4(dst + (uint32_t)((q ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                            pk[4 * q + 3], mbar);
+            if (half == 0)
+                st_async_b32(x_remote + (uint32_t)(k * 1024 + row * 4), __float_as_uint(row < args.H ? alpha : 1.f),
+                             mbar);
+        }
+        if (last) {
+            // the pair adds its two half sums (half 0 + half 1) for 1/l and lse
+            xb = xch + (xe & 1) * (2 * kRows);
+            ++xe;
+            xb[half * kRows + row] = l;
+            ok = barrier_and(pair_bar, 64, ok);
+            if (!ok) break;
+            const float lo = xb[(half ^ 1) * kRows + row];
+            const float l_row = half == 0 ? l + lo : lo + l;
+            if (half == 0) {
+                const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
+                st_async_b32(x_remote + (uint32_t)(k * 1024 + 512 + row * 4), __float_as_uint(inv_l), mbar);
+                if (row < args.H) {
+                    // lse in natural log: x is in log2 units of the scaled score
+                    const float lse_v = l_row > 0.f ? (m + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
+                    if (pi.it.split)
+                        args.lse_part[((size_t)pi.it.piece * args.s_q + s) * args.H + row] = lse_v;
+                    else
+                        args.lse[((size_t)pi.it.b * args.s_q + s) * args.H + row] = lse_v;
+                }
+            }
+        } else if (ok && half == 0) {
+            st_async_b32(x_remote + (uint32_t)(k * 1024 + 512 + row * 4), 0u, mbar);
+        }
+    }
+    return ok;
+}
+
+// ============================================================== value CTA ==
+__device__ void value_producer(const DecodeMaps& maps, const DecodeArgs& args, Bars* bars, uint8_t* smem, int part,
+                               volatile int* abort) {
+    int* err = args.err;
+    const long long wait_ns = args.wait_ns;
+    uint8_t* vring = smem + kOffV;
+    PairIter pi;
+    pi.init(args, part);
+    bool ok = true;
+    int v = 0;
+    for (; ok && pi.valid; pi.advance()) {
+        for (int p = 0; ok && p < pi.np; ++p) {
+            const int blk = checked_block(args, pi.it.b, pi.j + p, err);
+            for (int h = 0; h < 2; ++h, ++v) {
+                if (v >= kVRing) ok = mbar_wait(&bars->v_empty[v % kVRing], ((v / kVRing) - 1) & 1, abort, err, wait_ns);
+                if (!ok) break;
+                uint8_t* dst = vring + (v % kVRing) * kVSlotBytes;
+                uint64_t* bar = &bars->v_full[v % kVRing];
+                mbar_arrive_expect_tx(bar, (uint32_t)kVSlotBytes);
+                tma_load_3d(dst, &maps.v, bar, 0, blk * kPage, 4 * h);
+            }
+        }
+    }
+    drain_ring(bars->v_full, kVRing, v, err);
+}
+
+__device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uint32_t tmem, int part,
+                          volatile int* abort) {
+    int* err = args.err;
+    const long long wait_ns = args.wait_ns;
+    const int lane = threadIdx.x & 31;
+    uint8_t* vring = smem + kOffV;
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, 256, false, true);
+    PairIter pi;
+    pi.init(args, part);
+    bool ok = true, issued = false;
+    int v = 0;
+    for (; ok && pi.valid; pi.advance()) {
+        const int n = pi.n, k = n & 1, qi = pi.n_items - 1;
+        const bool first = pi.first_of_item(), last = pi.last_of_item();
+        ok = warp_wait<true>(&bars->p_full[k], (n >> 1) & 1, abort, err, wait_ns);
+        if (!ok) break;
+        if (lane == 0) {
+            // P was written by the peer's generic stores: make it visible to the
+            // tensor pipe, then arm the slot for pair n + 2 (its bytes can only
+            // come after this pair has released the slot)
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars->p_full[k], kPMsgBytes);
+        }
+        __syncwarp();
+        // the O warps have read this message's factors (and rescaled O if asked)
+        ok = warp_wait(&bars->o_ack, n & 1, abort, err, wait_ns);
+        if (!ok) break;
+        for (int p = 0; ok && p < pi.np; ++p) {
+            const int page = pi.j + p;
+            const int tail = page == pi.it.nblk - 1 ? pi.it.seqlen - page * kPage : kPage;
+            for (int h = 0; h < 2; ++h, ++v) {
+                // a batch's first product overwrites O: its previous epilogue must have read it
+                if (first && p == 0 && qi > 0) ok = warp_wait(&bars->o_free[h], (qi - 1) & 1, abort, err, wait_ns);
+                if (ok) ok = warp_wait(&bars->v_full[v % kVRing], (v / kVRing) & 1, abort, err, wait_ns);
+                if (!ok) break;
+                uint8_t* vs = vring + (v % kVRing) * kVSlotBytes;
+                if (tail < kPage) {
+                    // rows past seqlen hold arbitrary bytes: zero them so that
+                    // 0-probability keys cannot inject NaN/Inf into P.V
+                    const int per_chunk = (kPage - tail) * 8;  // 16-byte words
+                    for (int i = lane; i < 4 * per_chunk; i += 32) {
+                        const int c = i / per_chunk, w = i % per_chunk;
+                        reinterpret_cast<uint4*>(vs + c * kChunkBytes + tail * 128)[w] = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t a_base = smem_u32(smem + kOffP + k * kPSlotBytes + p * kRows * 128);
+                    const uint32_t v_base = smem_u32(vs);
+#pragma unroll
+                    for (int kk = 0; kk < kPage / 16; ++kk)
+                        mma_bf16_ss(tmem + 256u * h, desc_sw128(a_base + 32 * kk, 0, 1024),
+                                    desc_sw128(v_base + 2048 * kk, kChunkBytes, 1024), idesc_pv,
+                                    (first && p == 0 && kk == 0) ? 0u : 1u);
+                    mma_commit(&bars->v_empty[v % kVRing]);
+                }
+                __syncwarp();
+                issued = true;
+            }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+            mma_commit(&bars->pv_done);
+            if (last)
+                mma_commit(&bars->o_full);  // the epilogue hands the slot back after staging in it
+            else
+                mma_commit_multicast(&bars->p_free[k], (uint16_t)1u);  // arrives on the score CTA (rank 0)
+        }
+        __syncwarp();
+    }
+    if (issued) {
+        if (lane == 0) mma_commit(&bars->drain);
+        __syncwarp();
+        warp_wait(&bars->drain, 0, nullptr, err, kDrainNs);
+    }
+    return ok;
+}
+
+__device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bars* bars, uint8_t* smem,
+                             uint32_t tmem, int part, int s, uint32_t peer, volatile int* abort) {
+    int* err = args.err;
+    const long long wait_ns = args.wait_ns;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const float* xv = reinterpret_cast<const float*>(smem + kOffX);  // [slot][factor 128 | 1/l 128]
+    const uint32_t ocol = tmem + lane_base + 256u * (uint32_t)half;
+    PairIter pi;
+    pi.init(args, part);
+    bool ok = true;
+    bool stored = false;
+    for (; ok && pi.valid; pi.advance()) {
+        const int n = pi.n, k = n & 1, qi = pi.n_items - 1;
+        const bool first = pi.first_of_item(), last = pi.last_of_item();
+        ok = warp_wait<true>(&bars->p_full[k], (n >> 1) & 1, abort, err, wait_ns);
+        if (!ok) break;
+        const float inv_l = xv[k * 256 + 128 + row];
+        if (!first) {
+            const float alpha = xv[k * 256 + row];
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                // O rows of this warp move to the new reference max (after the
+                // previous P.V product has landed)
+                ok = warp_wait(&bars->pv_done, (n - 1) & 1, abort, err, wait_ns);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < 256; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(ocol + c, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                    tmem_st32(ocol + c, v);
+                }
+                tmem_wait_st();
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->o_ack);
+        if (!last) continue;
+
+        // ---- epilogue of the item: O * (1/l) -> staging (the pair's P slot) -> TMA store
+        ok = warp_wait(&bars->o_full, qi & 1, abort, err, wait_ns);
+        if (!ok) break;
+        tc_fence_after();
+        const Item& it = pi.it;
+        const bool store = quad * 32 < args.H;
+        uint8_t* stage = smem + kOffP + k * kPSlotBytes + warp * 4096;  // [32 rows x 128 B], 128-byte swizzle
+        uint8_t* srow = stage + lane * 128;
+        if (!it.split) {
+            const int z = it.b * args.s_q + s;
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+                const int col = 64 * i;
+                uint32_t v0[32], v1[32];
+                tmem_ld32(ocol + col, v0);
+                tmem_ld32(ocol + col + 32, v1);
+                tmem_wait_ld();
+                if (!store) continue;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 w0, w1;
+                    w0.x = pack_bf16x2(__uint_as_float(v0[8 * q + 0]) * inv_l, __uint_as_float(v0[8 * q + 1]) * inv_l);
+                    w0.y = pack_bf16x2(__uint_as_float(v0[8 * q + 2]) * inv_l, __uint_as_float(v0[8 * q + 3]) * inv_l);
+                    w0.z = pack_bf16x2(__uint_as_float(v0[8 * q + 4]) * inv_l, __uint_as_float(v0[8 * q + 5]) * inv_l);
+                    w0.w = pack_bf16x2(__uint_as_float(v0[8 * q + 6]) * inv_l, __uint_as_float(v0[8 * q + 7]) * inv_l);
+                    w1.x = pack_bf16x2(__uint_as_float(v1[8 * q + 0]) * inv_l, __uint_as_float(v1[8 * q + 1]) * inv_l);
+                    w1.y = pack_bf16x2(__uint_as_float(v1[8 * q + 2]) * inv_l, __uint_as_float(v1[8 * q + 3]) * inv_l);
+                    w1.z = pack_bf16x2(__uint_as_float(v1[8 * q + 4]) * inv_l, __uint_as_float(v1[8 * q + 5]) * inv_l);
+                    w1.w = pack_bf16x2(__uint_as_float(v1[8 * q + 6]) * inv_l, __uint_as_float(v1[8 * q + 7]) * inv_l);
+                    *reinterpret_cast<uint4*>(srow + ((q ^ (lane & 7)) << 4)) = w0;
+                    *reinterpret_cast<uint4*>(srow + (((q + 4) ^ (lane & 7)) << 4)) = w1;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&maps.o, stage, 256 * half + col, quad * 32, z);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();
+                }
+                __syncwarp();
+                stored = true;
+            }
+        } else {
+            const int z = it.piece * args.s_q + s;
+#pragma unroll 1
+            for (int i = 0; i < 8; ++i) {
+                const int col = 32 * i;
+                uint32_t v0[32];
+                tmem_ld32(ocol + col, v0);
+                tmem_wait_ld();
+                if (!store) continue;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float4 w;
+                    w.x = __uint_as_float(v0[4 * q + 0]) * inv_l;
+                    w.y = __uint_as_float(v0[4 * q + 1]) * inv_l;
+                    w.z = __uint_as_float(v0[4 * q + 2]) * inv_l;
+                    w.w = __uint_as_float(v0[4 * q + 3]) * inv_l;
+                    *reinterpret_cast<float4*>(srow + ((q ^ (lane & 7)) << 4)) = w;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&maps.op, stage, 256 * half + col, quad * 32, z);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();
+                }
+                __syncwarp();
+                stored = true;
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&bars->o_free[half]);
+            mbar_arrive(&bars->stage_done);
+        }
+        if (warp == 0) {
+            // all eight warps are done with the staging area: give the P slot back
+            ok = warp_wait(&bars->stage_done, qi & 1, abort, err, wait_ns);
+            if (ok && lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&bars->p_free[k]), peer));
+            __syncwarp();
+        }
+    }
+    if (stored && lane == 0) bulk_wait_group0();
+    return ok;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tm_kv, DecodeArgs args) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sKV = smem + kOffKV;
-    float4* sRecv = reinterpret_cast<float4*>(smem + kOffRecv);  // [2][16][128] float4
-    Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+    decode_kernel(const __grid_constant__ DecodeMaps maps, DecodeArgs args) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
     volatile int* abort = &bars->abort;
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
     const int cluster_id = blockIdx.x >> 1;
     const int part = cluster_id / args.s_q;
     const int s = cluster_id % args.s_q;
-    int* err = args.err;
-    const long long wait_ns = args.wait_ns;
+
+    // the layout needs 1024-byte-aligned swizzle atoms and leaves no room to
+    // realign; both CTAs see the same base and leave together
+    if ((smem_u32(smem) & 1023u) != 0) {
+        if (threadIdx.x == 0) record_error(args.err, kErrUnsupported);
+        cluster_sync_all();
+        return;
+    }
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&bars->kv_full[i], 1);
-            mbar_init(&bars->kv_empty[i], 1);
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(&bars->ring_full[i], 1);
+            mbar_init(&bars->ring_empty[i], 1);
         }
-        mbar_init(&bars->q_full, kSoftmaxThreads);
-        mbar_init(&bars->q_empty, 1);
-        mbar_init(&bars->s_full, 1);
-        mbar_init(&bars->s_free, kSoftmaxThreads);
-        mbar_init(&bars->p_full, kSoftmaxThreads);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->qr_full[i], 1);
+            mbar_init(&bars->qr_empty[i], 1);
+            mbar_init(&bars->s_full[i], 1);
+            mbar_init(&bars->s_free[i], 256);
+            mbar_init(&bars->p_free[i], 1);
+            mbar_init(&bars->p_full[i], 1);
+            mbar_init(&bars->o_free[i], 4);
+        }
+        mbar_init(&bars->q_drained, 1);
+        for (int i = 0; i < kVRing; ++i) {
+            mbar_init(&bars->v_full[i], 1);
+            mbar_init(&bars->v_empty[i], 1);
+        }
         mbar_init(&bars->pv_done, 1);
-        mbar_init(&bars->o_free, kSoftmaxThreads);
-        for (int k = 0; k < 2; ++k) {
-            mbar_init(&bars->x_full[k], 1);
-            mbar_init(&bars->c_done[k], kSoftmaxThreads / 32);
-            mbar_init(&bars->peer_free[k], 1);
-        }
+        mbar_init(&bars->o_full, 1);
+        mbar_init(&bars->o_ack, 8);
+        mbar_init(&bars->stage_done, 8);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_mbarrier_init_cluster();
-        tma_prefetch_desc(&tm_kv);
-        // receive slots of pages 0 and 1 are armed up front; later ones are armed
-        // when the slot has been read
-        mbar_arrive_expect_tx(&bars->x_full[0], (uint32_t)kXBytes);
-        mbar_arrive_expect_tx(&bars->x_full[1], (uint32_t)kXBytes);
+        if (rank == 0) {
+            tma_prefetch_desc(&maps.kg);
+            tma_prefetch_desc(&maps.qg);
+            tma_prefetch_desc(&maps.q);
+        } else {
+            tma_prefetch_desc(&maps.v);
+            tma_prefetch_desc(&maps.o);
+            tma_prefetch_desc(&maps.op);
+            // the first two P messages may arrive as soon as the cluster is up
+            mbar_arrive_expect_tx(&bars->p_full[0], kPMsgBytes);
+            mbar_arrive_expect_tx(&bars->p_full[1], kPMsgBytes);
+        }
     }
     if (warp == kWarpMma) {
         tmem_alloc(&bars->tmem_slot, kTmemCols);
@@ -263,377 +770,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     griddep_wait();
     griddep_launch_dependents();
 
-    if (warp == kWarpProducer) {
-        // ------------------------------------------------------- producer --
-        if (lane == 0) {
-            PageIter pg;
-            pg.init(args, part);
-            bool ok = true;
-            for (; pg.valid; pg.advance()) {
-                const int g = pg.g, st = g % kStages;
-                if (g >= kStages) ok = mbar_wait(&bars->kv_empty[st], ((g / kStages) - 1) & 1, abort, err, wait_ns);
-                if (!ok) break;
-                const int j = pg.j;
-                int blk = j < args.mbps ? args.block_table[(size_t)pg.it.b * args.mbps + j] : -1;
-                if (blk < 0 || blk >= args.num_blocks) {
-                    record_error(err, kErrBadBlock);
-                    blk = 0;
-                }
-                mbar_arrive_expect_tx(&bars->kv_full[st], (uint32_t)kStageBytes);
-                uint8_t* dst = sKV + st * kStageBytes;
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_2d(dst + c * kKVChunkBytes, &tm_kv, &bars->kv_full[st], 64 * (4 * (int)rank + c),
-                                blk * kPage);
-            }
-            const int g = pg.g;
-            // drain: wait for the last load issued into each buffer
-            for (int gg = g - kStages > 0 ? g - kStages : 0; gg < g; ++gg)
-                mbar_wait(&bars->kv_full[gg % kStages], (gg / kStages) & 1, nullptr, err, kDrainNs);
-        }
-    } else if (warp == kWarpMma) {
-        // ----------------------------------------------------- MMA issuer --
-        constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kPage, false, false);
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, 256, false, true);
-        PageIter ps, pp;  // next score product, next P.V product
-        ps.init(args, part);
-        pp.init(args, part);
-        bool ok = true, issued_any = false, q_ready = false;
-        uint64_t t_last = globaltimer_ns();
-        while (ok && pp.valid) {
-            bool progressed = false;
-            // --- score product of page ps.g
-            if (ps.valid) {
-                const int g = ps.g, st = g % kStages;
-                bool ready = true;
-                // non-blocking probes: a suspended try_wait on one barrier would hold
-                // back a product whose inputs became ready on another
-                if (lane == 0) {
-                    if (!q_ready && ps.first_of_item()) q_ready = mbar_probe(smem_u32(&bars->q_full), (ps.n_items - 1) & 1);
-                    ready = (q_ready || !ps.first_of_item()) && mbar_probe(smem_u32(&bars->kv_full[st]), (g / kStages) & 1) &&
-                            (g == 0 || mbar_probe(smem_u32(&bars->s_free), (g - 1) & 1));
-                }
-                ready = __shfl_sync(0xffffffffu, ready, 0);
-                if (ready) {
-                    uint8_t* stage = sKV + st * kStageBytes;
-                    const int tail_rows = (ps.j == ps.it.nblk - 1) ? ps.it.seqlen - ps.j * kPage : kPage;
-                    if (tail_rows < kPage) {
-                        // rows past seqlen hold arbitrary bytes: zero them so that
-                        // 0-probability columns cannot inject NaN/Inf into P.V
-                        const int per_chunk = (kPage - tail_rows) * 8;  // 16-byte words
-                        for (int i = lane; i < kChunks * per_chunk; i += 32) {
-                            const int c = i / per_chunk, w = i % per_chunk;
-                            reinterpret_cast<uint4*>(stage + c * kKVChunkBytes + tail_rows * 128)[w] = make_uint4(0, 0, 0, 0);
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                    }
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t k_base = smem_u32(stage);
-                        // partial score over 18 K-steps of 16 dims: [288 r, 288 r + 288);
-                        // the query slice in TMEM holds exactly those dims
-                        const int step0 = rank == 0 ? 0 : 2;  // first K-step inside local chunk 0
-#pragma unroll
-                        for (int t = 0; t < 18; ++t) {
-                            const int ls = step0 + t;
-                            const int c = ls >> 2, kk = ls & 3;
-                            const uint64_t bd = desc_sw128(k_base + c * kKVChunkBytes + kk * 32, 0, 1024);
-                            mma_bf16_ts(tmem + kTmemS, tmem + kTmemQ + 8u * t, bd, idesc_s, t > 0 ? 1u : 0u);
-                        }
-                        mma_commit(&bars->s_full);
-                        if (ps.last_of_item()) mma_commit(&bars->q_empty);
-                    }
-                    __syncwarp();
-                    issued_any = true;
-                    if (ps.last_of_item()) q_ready = false;
-                    ps.advance();
-                    progressed = true;
-                }
-            }
-            // --- P.V product of page pp.g (its score product was issued earlier)
-            if (pp.g < ps.g || !ps.valid) {
-                const int g = pp.g, st = g % kStages;
-                const bool first = pp.first_of_item();
-                bool ready = true;
-                if (lane == 0)
-                    ready = mbar_probe(smem_u32(&bars->p_full), g & 1) &&
-                            (!first || pp.n_items == 1 || mbar_probe(smem_u32(&bars->o_free), (pp.n_items - 2) & 1));
-                ready = __shfl_sync(0xffffffffu, ready, 0);
-                if (ready) {
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t v_base = smem_u32(sKV + st * kStageBytes);
-#pragma unroll
-                        for (int kk = 0; kk < kPage / 16; ++kk) {
-                            const uint64_t bd = desc_sw128(v_base + kk * 2048, kKVChunkBytes, 1024);
-                            mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 8u * kk, bd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
-                        }
-                        mma_commit(&bars->pv_done);
-                        mma_commit(&bars->kv_empty[st]);
-                    }
-                    __syncwarp();
-                    pp.advance();
-                    progressed = true;
-                }
-            }
-            if (progressed) {
-                t_last = globaltimer_ns();
-            } else {
-                if (*abort) ok = false;
-                else if ((long long)(globaltimer_ns() - t_last) > wait_ns) {
-                    record_error(err, kErrTimeout);
-                    *abort = 1;
-                    ok = false;
-                }
-                ok = __all_sync(0xffffffffu, ok);
-            }
-        }
-        // drain: every MMA this thread issued has completed before TMEM is freed
-        if (issued_any) {
-            if (lane == 0) mma_commit(&bars->drain);
-            __syncwarp();
-            warp_wait(&bars->drain, 0, nullptr, err, kDrainNs);
+    bool ok = true;
+    if (rank == 0) {
+        if (warp == kWarpProducer) {
+            if ((threadIdx.x & 31) == 0) score_producer(maps, args, bars, smem, part, s, abort);
+        } else if (warp == kWarpMma) {
+            ok = score_mma(args, bars, smem, tmem, part, abort);
+        } else {
+            ok = score_softmax(args, bars, smem, tmem, part, s, peer, abort);
         }
     } else {
-        // ------------------------- query load, exchange, softmax, epilogue --
-        const int quad = warp & 3, half = warp >> 2;
-        const int row = quad * 32 + lane;
-        const int pair_bar = 1 + quad;  // named barrier of the two warps sharing these rows
-        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        // peer addresses of slot 0; slot 1 is a fixed offset away
-        const uint32_t recv_remote0 = mapa_shared(smem_u32(sRecv + row), peer);
-        const uint32_t xfull_remote0 = mapa_shared(smem_u32(&bars->x_full[0]), peer);
-        const uint32_t pfree_remote0 = mapa_shared(smem_u32(&bars->peer_free[0]), peer);
-        constexpr uint32_t kSlotBytes = 16 * kRows * 16;
-        PageIter ps, pc;  // page whose partial is sent next, page processed next
-        ps.init(args, part);
-        pc.init(args, part);
-        bool ok = true;
-        float xs[32];  // own partial (log2 units) of this warp's 32 columns of the page sent last
-
-        // reads this warp's half of S of page ps.g, frees S for the next score
-        // product and sends the half to the peer
-        auto send_page = [&]() -> bool {
-            const int g = ps.g, k = g & 1;
-            if (!warp_wait(&bars->s_full, g & 1, abort, err, wait_ns)) return false;
-            tc_fence_after();
-            {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_base + kTmemS + 32u * half, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) xs[c] = __uint_as_float(v[c]) * args.scale_log2;
-            }
-            tc_fence_before();
-            mbar_arrive(&bars->s_free);
-            // the peer's slot k held page g - 2: it must have read it
-            if (g >= 2 && !warp_wait(&bars->peer_free[k], ((g - 2) >> 1) & 1, abort, err, wait_ns)) return false;
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                st_async_v4(recv_remote0 + k * kSlotBytes + (uint32_t)((8 * half + q) * kRows * 16), xs[4 * q],
-                            xs[4 * q + 1], xs[4 * q + 2], xs[4 * q + 3], xfull_remote0 + k * (uint32_t)sizeof(uint64_t));
-            ps.advance();
-            return true;
-        };
-
-        ItemIter ahead;  // the item after the one being loaded, for an L2 prefetch of its query rows
-        if (pc.valid) {
-            load_query(args, pc.it, s, row, rank, half, tmem + lane_base + kTmemQ);
-            tc_fence_before();
-            mbar_arrive(&bars->q_full);
-            ahead = pc.items;
-            ok = send_page();
-        }
-        float m = -INFINITY, l = 0.f;  // l: this warp's half of the row sum
-        int n_valid = 0;
-        while (pc.valid) {
-            // every exit goes through a pair barrier, so both warps of a pair leave together
-            const int g = pc.g, k = g & 1;
-            const Item it = pc.it;
-            const int j = pc.j;
-            const bool first = pc.first_of_item(), last = pc.last_of_item();
-            if (first) {
-                m = -INFINITY;
-                l = 0.f;
-                n_valid = visible_keys(it.seqlen, args.s_q, s, args.causal);
-                Item pf;
-                ItemIter probe = ahead;
-                if (half == 0 && probe.next(pf)) prefetch_query(args, pf.b, s, row, rank);
-            }
-            float x[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) x[c] = xs[c];
-            // (A) the next page's partial goes out before this page is normalised
-            if (ok && ps.valid) {
-                if (ps.first_of_item()) {
-                    // a new item starts there: its query slice replaces this one as
-                    // soon as this item's last score product is done
-                    ok = warp_wait(&bars->q_empty, (ps.n_items - 2) & 1, abort, err, wait_ns);
-                    if (ok) {
-                        tc_fence_after();
-                        load_query(args, ps.it, s, row, rank, half, tmem + lane_base + kTmemQ);
-                        tc_fence_before();
-                        mbar_arrive(&bars->q_full);
-                        ahead = ps.items;
-                    }
-                }
-                if (ok) ok = send_page();
-            }
-            // (B) page g: own partial + the peer's, for this warp's 32 columns
-            if (ok) ok = warp_wait(&bars->x_full[k], (g >> 1) & 1, abort, err, wait_ns);
-            float mh = -INFINITY;
-            if (ok) {
-                const float4* rv = sRecv + k * (16 * kRows) + 8 * half * kRows;
-                const int vcount = min(max(n_valid - j * kPage - 32 * half, 0), 32);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 w = rv[q * kRows + row];
-                    const float wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = 4 * q + e;
-                        // x_0 + x_1 in this order on both CTAs
-                        x[c] = rank == 0 ? x[c] + wv[e] : wv[e] + x[c];
-                    }
-                }
-                if (vcount < 32) {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) x[c] = c < vcount ? x[c] : -INFINITY;
-                }
-#pragma unroll
-                for (int c = 0; c < 32; ++c) mh = fmaxf(mh, x[c]);
-                // slot k is read: re-arm it for page g + 2 and tell the peer it may write it
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->c_done[k]);
-                if (warp == 0 && lane == 0 && mbar_wait(&bars->c_done[k], (g >> 1) & 1, abort, err, wait_ns)) {
-                    mbar_arrive_expect_tx(&bars->x_full[k], (uint32_t)kXBytes);
-                    fence_proxy_async_smem();
-                    mbar_arrive_remote_relaxed(pfree_remote0 + k * (uint32_t)sizeof(uint64_t));
-                }
-                tmem_st1(tmem + lane_base + kTmemX + half, __float_as_uint(mh));
-                tmem_wait_st();
-            }
-            tc_fence_before();
-            ok = barrier_and(pair_bar, 64, ok);
-            if (!ok) break;
-            tc_fence_after();
-            const float mx = fmaxf(mh, __uint_as_float(tmem_ld1(tmem + lane_base + kTmemX + (half ^ 1))));
-            tmem_wait_ld();
-            bool pv_waited = false;
-            // lazy rescale: a row moves its reference max only when the new max
-            // exceeds it by more than 2^8. Both warps of the pair see the same
-            // mx and m, so they take the same decisions; the TMEM read-modify-
-            // write of O is warp-collective, so a warp takes it when any of its
-            // rows needs it (rows that do not scale by 1), each warp over its
-            // half of O's columns.
-            const bool need = mx > m + kRescaleThreshold;
-            const float alpha = need ? fast_exp2(m - mx) : 1.f;  // 0 when m = -inf
-            if (!first && __any_sync(0xffffffffu, need)) {
-                ok = warp_wait(&bars->pv_done, (g - 1) & 1, abort, err, wait_ns);
-                pv_waited = true;
-                if (ok) {
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int c = 0; c < 128; c += 32) {
-                        uint32_t v[32];
-                        const uint32_t col = tmem + lane_base + kTmemO + 128u * half + c;
-                        tmem_ld32(col, v);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                        tmem_st32(col, v);
-                    }
-                    tmem_wait_st();
-                }
-            }
-            if (need) {
-                l *= alpha;
-                m = mx;
-            }
-            const float m_use = m == -INFINITY ? 0.f : m;
-            uint32_t pk[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                // the row sum takes the fp32 probabilities; only the P.V operand is bf16
-                const float p0 = fast_exp2(x[2 * c] - m_use), p1 = fast_exp2(x[2 * c + 1] - m_use);
-                l += p0 + p1;
-                pk[c] = pack_bf16x2(p0, p1);
-            }
-            if (ok && g >= 1 && !pv_waited) ok = warp_wait(&bars->pv_done, (g - 1) & 1, abort, err, wait_ns);
-            if (ok) {
-                tmem_st16(tmem + lane_base + kTmemP + 16u * half, pk);
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&bars->p_full);
-            }
-
-            if (last) {
-                // (C) epilogue of the item: the pair adds its two half sums (half 0 + half 1)
-                if (ok) ok = warp_wait(&bars->pv_done, g & 1, abort, err, wait_ns);
-                if (ok) {
-                    tmem_st1(tmem + lane_base + kTmemX + 2 + half, __float_as_uint(l));
-                    tmem_wait_st();
-                }
-                tc_fence_before();
-                ok = barrier_and(pair_bar, 64, ok);
-                if (!ok) break;
-                tc_fence_after();
-                const float l_other = __uint_as_float(tmem_ld1(tmem + lane_base + kTmemX + 2 + (half ^ 1)));
-                tmem_wait_ld();
-                const float l_row = half == 0 ? l + l_other : l_other + l;
-                const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
-                const bool row_ok = row < args.H;
-                const size_t orow = ((size_t)it.b * args.s_q + s) * args.H + row;
-                const size_t prow_idx = ((size_t)it.piece * args.s_q + s) * args.H + row;
-                const int ocol = 256 * rank + 128 * half;  // this warp's 128 latent columns
-                // 32-byte stores: every store fills whole sectors
-#pragma unroll 1
-                for (int c = 0; c < 128; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + kTmemO + 128u * half + c, v);
-                    tmem_wait_ld();
-                    if (!row_ok) continue;
-                    if (it.split) {
-                        float* dst = args.o_part + prow_idx * kDLatent + ocol + c;
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            uint32_t w[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(__uint_as_float(v[8 * e + i]) * inv_l);
-                            st_global_v8(dst + 8 * e, w);
-                        }
-                    } else {
-                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.o_lat) + orow * kDLatent + ocol + c;
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            uint32_t w[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                w[i] = pack_bf16x2(__uint_as_float(v[16 * e + 2 * i]) * inv_l,
-                                                   __uint_as_float(v[16 * e + 2 * i + 1]) * inv_l);
-                            st_global_v8(dst + 16 * e, w);
-                        }
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(&bars->o_free);
-                if (rank == 0 && half == 0 && row_ok) {
-                    // lse in natural log: x is in log2 units of the scaled score
-                    const float lse_v = l_row > 0.f ? (m + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
-                    if (it.split)
-                        args.lse_part[prow_idx] = lse_v;
-                    else
-                        args.lse[orow] = lse_v;
-                }
-            }
-            pc.advance();
+        if (warp == kWarpProducer) {
+            if ((threadIdx.x & 31) == 0) value_producer(maps, args, bars, smem, part, abort);
+        } else if (warp == kWarpMma) {
+            ok = value_mma(args, bars, smem, tmem, part, abort);
+        } else {
+            ok = value_owarps(maps, args, bars, smem, tmem, part, s, peer, abort);
         }
     }
+    // a role that gave up tells the peer, whose waits then end promptly
+    if (!ok || *abort) st_cluster_b32(mapa_shared(smem_u32(&bars->abort), peer), 1u);
 
     tc_fence_before();
     __syncthreads();
     // the peer may still store into our buffers or arrive on our barriers until
-    // it has finished its last page: leave together
+    // it has finished its last pair: leave together
     cluster_sync_all();
     if (warp == kWarpMma) {
         tc_fence_after();
@@ -671,13 +832,12 @@ cudaLaunchConfig_t make_config(int clusters, cudaStream_t stream, cudaLaunchAttr
 
 }  // namespace
 
-cudaError_t launch_decode(const CUtensorMap* tm_kv, const DecodeArgs& args,
-                          cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, cudaStream_t stream) {
     cudaError_t e = prepare_kernel();
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = make_config(args.num_parts * args.s_q, stream, attr, true);
-    return cudaLaunchKernelEx(&cfg, decode_kernel, *tm_kv, args);
+    return cudaLaunchKernelEx(&cfg, decode_kernel, maps, args);
 }
 
 // Clusters of the decode kernel that can be resident at once on the current device.

@@ -63,7 +63,21 @@ struct DecodeArgs {
 cudaError_t gemm_error_fetch(int* out, cudaStream_t stream);
 int decode_max_active_clusters(int device);
 
-cudaError_t launch_decode(const CUtensorMap* tm_kv, const DecodeArgs& args, cudaStream_t stream);
+// TMA descriptors of the decode kernel (all 128-byte swizzle; dims listed
+// innermost first):
+//  kg: the cache as {64 dims, 8 keys, 9 chunks, num_blocks * 8 key groups},
+//      strides {1152, 128, 9216} B; box {64, 8, 3, 8} = three chunks of a page
+//  v:  the cache as {64 dims, num_blocks * 64 keys, 9 chunks}, strides {1152, 128} B;
+//      box {64, 64, 4} = four value chunks of a page
+//  qg: q_abs as {64 dims, 8 rows, 9 chunks, B * s_q * H / 8 row groups}, strides
+//      {1152, 128, 9216} B; box {64, 8, 3, min(H, 128) / 8}
+//  q:  q_abs as [B * s_q, H, 576], box [1 x min(H, 128) x 64] (the rope dims)
+//  o:  bf16 [B * s_q, H, 512], box [1 x min(H, 32) x 64]   (store)
+//  op: fp32 [pieces * s_q, H, 512], box [1 x min(H, 32) x 32] (store)
+struct DecodeMaps {
+    CUtensorMap kg, v, qg, q, o, op;
+};
+cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, cudaStream_t stream);
 
 cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, const float* o_part,
                            const float* lse_part, void* o_lat, float* lse, cudaStream_t stream);

@@ -11,6 +11,7 @@ namespace mla {
 
 // ----------------------------------------------------------------- status --
 // Device-side error codes, same values as mla_status_t.
+constexpr int kErrUnsupported = 2;
 constexpr int kErrTimeout = 4;
 constexpr int kErrBadBlock = 5;
 // Limit of the waits that drain in-flight copies and MMAs before a CTA exits.
@@ -156,6 +157,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
+                                            int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+        "[%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+
 // TMA store of a box from shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
     asm volatile(
@@ -169,6 +179,9 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 __device__ __forceinline__ void bulk_wait_group_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+
+// Wait until every committed bulk group has completed (writes performed).
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Generic-proxy writes to shared memory become visible to the async proxy
 // (TMA, tcgen05.mma operand reads) after this fence plus a thread sync.
@@ -227,6 +240,24 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+// Same, but the arrival goes to the mbarrier at this barrier's shared-memory
+// offset in every CTA of the cluster whose bit is set in `cta_mask`.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Asynchronous copy of a 128-row x 256-bit (32-byte) slice of a shared-memory
+// matrix (described like an MMA operand) into TMEM: row i -> lane i, its 32
+// bytes into 8 consecutive 32-bit columns. Ordered before tcgen05.mma ops
+// issued later by the same thread.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives
@@ -378,6 +409,24 @@ __device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, float a, float
                      dst_cluster),
                  "f"(a), "f"(b), "f"(c), "f"(d), "r"(mbar_cluster)
                  : "memory");
+}
+
+__device__ __forceinline__ void st_async_u4(uint32_t dst_cluster, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t mbar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     dst_cluster),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(mbar_cluster)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_b32(uint32_t dst_cluster, uint32_t v, uint32_t mbar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst_cluster),
+                 "r"(v), "r"(mbar_cluster)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_b32(uint32_t addr, uint32_t v) {
+    asm volatile("st.relaxed.cluster.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to the

@@ -68,9 +68,9 @@ def test_paged_gather_bit_exact(api):
 
 # ------------------------------------------------------------- tcgen05 tile --
 
-@pytest.mark.parametrize("a_tmem", [False, True])
+@pytest.mark.parametrize("a_tmem", [0, 1, 2])
 @pytest.mark.parametrize("K,N,kmajor", [(64, 64, True), (576, 64, True), (320, 64, True), (64, 256, False),
-                                        (128, 128, False), (576, 256, True), (192, 64, False)])
+                                        (128, 128, False), (576, 256, True), (192, 64, False), (512, 128, True)])
 def test_mma_tile(api, K, N, kmajor, a_tmem):
     g = torch.Generator().manual_seed(K * 1000 + N)
     a = torch.randn(128, K, generator=g).to(torch.bfloat16)
