@@ -253,6 +253,7 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
 
     DecodeArgs a;
     a.q_abs = q_abs;
+    a.kv = kv_cache;
     a.block_table = block_table;
     a.mbps = max_blocks_per_seq;
     a.seqlens = cache_seqlens;

@@ -88,6 +88,8 @@ constexpr uint32_t kTmemS0 = 256;   // score CTA: S buffers, 128 columns each
 constexpr uint32_t kTmemS1 = 384;
 constexpr uint32_t kTmemCols = 512; // value CTA: O, all columns
 
+constexpr int kPrefetchPairs = 3;  // L2 prefetch distance of the score CTA's producer, in page pairs
+
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: tolerate growth up to 2^8 before rescaling O
 
 struct Bars {
@@ -100,7 +102,8 @@ struct Bars {
     // value CTA
     uint64_t p_full[2];  // own arrive + expect_tx, bytes from the score CTA
     uint64_t v_full[kVRing], v_empty[kVRing];
-    uint64_t pv_done, o_full, o_ack, o_free[2], stage_done;
+    uint64_t pv_done, o_full, o_ack[2], o_free[2], stage_done;  // o_ack per P slot: the O warps can run one
+                                                                 // pair ahead, never two on the same slot
     uint64_t drain;
     uint32_t tmem_slot;
     int abort;
@@ -210,9 +213,26 @@ __device__ void score_producer(const DecodeMaps& maps, const DecodeArgs& args, B
     const uint32_t qgbytes = (uint32_t)hq * 128 * kGroupChunks;   // query chunk-group box
     PairIter pi;
     pi.init(args, part);
+    // The ring holds 1.3 pairs, far less than HBM latency times this CTA's share
+    // of the bandwidth; whole pages (contiguous 72 KB) are therefore requested
+    // into L2 kPrefetchPairs ahead, and the ring refills from L2.
+    PairIter pf;
+    pf.init(args, part);
+    auto prefetch_pair = [&]() {
+        if (!pf.valid) return;
+        for (int p = 0; p < pf.np; ++p) {
+            const int j = pf.j + p;
+            const int blk = j < args.mbps ? args.block_table[(size_t)pf.it.b * args.mbps + j] : -1;
+            if (blk >= 0 && blk < args.num_blocks)
+                prefetch_l2_bulk(static_cast<const uint8_t*>(args.kv) + (size_t)blk * kPage * kDQK * 2, kPage * kDQK * 2);
+        }
+        pf.advance();
+    };
+    for (int i = 0; i < kPrefetchPairs; ++i) prefetch_pair();
     bool ok = true;
     int r = 0, nq = 0;  // ring loads issued, rope query loads issued
     for (; ok && pi.valid; pi.advance()) {
+        prefetch_pair();
         const int bs = pi.it.b * args.s_q + s;
         if (pi.first_of_item()) {
             // the batch's query: dims [0, 576) through the ring, three chunks per
@@ -508,7 +528,7 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
         }
         __syncwarp();
         // the O warps have read this message's factors (and rescaled O if asked)
-        ok = warp_wait(&bars->o_ack, n & 1, abort, err, wait_ns);
+        ok = warp_wait(&bars->o_ack[k], (n >> 1) & 1, abort, err, wait_ns);
         if (!ok) break;
         for (int p = 0; ok && p < pi.np; ++p) {
             const int page = pi.j + p;
@@ -605,7 +625,7 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->o_ack);
+        if (lane == 0) mbar_arrive(&bars->o_ack[k]);
         if (!last) continue;
 
         // ---- epilogue of the item: O * (1/l) -> staging (the pair's P slot) -> TMA store
@@ -730,6 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->p_free[i], 1);
             mbar_init(&bars->p_full[i], 1);
             mbar_init(&bars->o_free[i], 4);
+            mbar_init(&bars->o_ack[i], 8);
         }
         mbar_init(&bars->q_drained, 1);
         for (int i = 0; i < kVRing; ++i) {
@@ -738,7 +759,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bars->pv_done, 1);
         mbar_init(&bars->o_full, 1);
-        mbar_init(&bars->o_ack, 8);
         mbar_init(&bars->stage_done, 8);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;

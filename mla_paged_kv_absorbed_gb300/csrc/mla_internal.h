@@ -44,6 +44,7 @@ cudaError_t launch_head_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b, c
 
 struct DecodeArgs {
     const void* q_abs;  // bf16 [B, s_q, H, 576]
+    const void* kv;     // bf16 [num_blocks, 64, 576] (L2 prefetch only; loads go through the tensor maps)
     const int32_t* block_table;
     int mbps;
     const int32_t* seqlens;

@@ -159,6 +159,35 @@ def test_workload_spec(api):
     sampled_check(api, "spec", [0, 65, 131], end_to_end=True)
 
 
+# ------------------------------------------------------ repeated launches --
+
+@pytest.mark.parametrize("name,calls", [("dsv3", 400), ("varlen", 300), ("spec", 60)])
+def test_repeated_calls_no_device_error(api, name, calls):
+    """Hundreds of back-to-back calls, so that the cross-CTA handshakes of the
+    decode kernel meet many different timings: the device error word stays
+    clear (a lost wakeup would end in MLA_ERR_TIMEOUT) and every call returns
+    the first call's bytes (the kernel is deterministic)."""
+    d = gen.make_workload(name).to("cuda")
+    tm, ns = api.mla_get_metadata(d.seqlens, d.s_q, d.H)
+    q_abs = d.q_abs if d.q is None else api.mla_absorb_q(d.q, d.w_uk)
+    ws = api.make_workspace(d.B, d.s_q, d.H, tm.shape[0])
+    o0, lse0 = api.mla_decode_paged(q_abs, d.kv_cache, d.block_table, d.seqlens, tm, ns, d.scale, d.causal,
+                                    workspace=ws)
+    assert api.mla_read_device_error(ws) == 0
+    o, lse = torch.empty_like(o0), torch.empty_like(lse0)
+    api.mla_set_wait_limit_ns(250_000_000)  # a lost wakeup shows up in a quarter second, not four
+    try:
+        for i in range(calls):
+            api.mla_decode_paged(q_abs, d.kv_cache, d.block_table, d.seqlens, tm, ns, d.scale, d.causal,
+                                 o_lat=o, lse=lse, workspace=ws)
+            if i % 50 == 49 or i == calls - 1:
+                assert api.mla_read_device_error(ws) == 0, f"device status after call {i}"
+                assert torch.equal(o.view(torch.int16), o0.view(torch.int16))
+                assert torch.equal(lse, lse0)
+    finally:
+        api.mla_set_wait_limit_ns(0)
+
+
 # ------------------------------------------------------------------ errors --
 
 def test_bad_block_is_reported(api):
