@@ -218,42 +218,39 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     DecodeMaps maps;
-    // row-group views: 8 rows x 64 dims per 1 KB swizzle atom, chunks of 64 dims 128 B apart
-    const uint64_t kg_dims[4] = {64, 8, (uint64_t)kDQK / 64, (uint64_t)num_blocks * (kPage / 8)};
-    const uint64_t kg_strides[3] = {(uint64_t)kDQK * 2, 128, (uint64_t)kDQK * 2 * 8};
-    const uint32_t kg_box[4] = {64, 8, 3, (uint32_t)(kPage / 8)};
-    if (!make_tmap(&maps.kg, kv_cache, 4, kg_dims, kg_strides, kg_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+    // [dims, keys, chunk] views: one box per page (or per 64 query rows)
+    const uint64_t kv_dims[3] = {64, (uint64_t)num_blocks * kPage, (uint64_t)kDQK / 64};
+    const uint64_t kv_strides[2] = {(uint64_t)kDQK * 2, 128};
+    const uint32_t kv_box[3] = {64, (uint32_t)kPage, (uint32_t)kDQK / 64};
+    if (!make_tmap(&maps.kv, kv_cache, 3, kv_dims, kv_strides, kv_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
         return MLA_ERR_CUDA;
-    const uint64_t v_dims[3] = {64, (uint64_t)num_blocks * kPage, (uint64_t)kDQK / 64};
-    const uint64_t v_strides[2] = {(uint64_t)kDQK * 2, 128};
-    const uint32_t v_box[3] = {64, (uint32_t)kPage, 4};
-    if (!make_tmap(&maps.v, kv_cache, 3, v_dims, v_strides, v_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+    const uint32_t v_box[3] = {64, (uint32_t)kPage, (uint32_t)kDLatent / 64};
+    if (!make_tmap(&maps.v, kv_cache, 3, kv_dims, kv_strides, v_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
         return MLA_ERR_CUDA;
     const uint64_t rows = (uint64_t)B * s_q;
-    const uint32_t h_box = (uint32_t)(H < 128 ? H : 128), h_store = (uint32_t)(H < 32 ? H : 32);
-    const uint64_t qg_dims[4] = {64, 8, (uint64_t)kDQK / 64, rows * (uint64_t)H / 8};
-    const uint64_t qg_strides[3] = {(uint64_t)kDQK * 2, 128, (uint64_t)kDQK * 2 * 8};
-    const uint32_t qg_box[4] = {64, 8, 3, h_box / 8};
-    if (!make_tmap(&maps.qg, q_abs, 4, qg_dims, qg_strides, qg_box)) return MLA_ERR_CUDA;
-    const uint64_t q_dims[3] = {(uint64_t)kDQK, (uint64_t)H, rows};
-    const uint64_t q_strides[2] = {(uint64_t)kDQK * 2, (uint64_t)H * kDQK * 2};
-    const uint32_t q_box[3] = {64, h_box, 1};
+    const uint64_t qrows_total = rows * (uint64_t)H;
+    const uint32_t qrows = (uint32_t)(qrows_total < 64 ? qrows_total : 64);
+    const uint64_t q_dims[3] = {64, qrows_total, (uint64_t)kDQK / 64};
+    const uint64_t q_strides[2] = {(uint64_t)kDQK * 2, 128};
+    const uint32_t q_box[3] = {64, qrows, (uint32_t)kDQK / 64};
     if (!make_tmap(&maps.q, q_abs, 3, q_dims, q_strides, q_box)) return MLA_ERR_CUDA;
-    const uint64_t o_dims[3] = {(uint64_t)kDLatent, (uint64_t)H, rows};
-    const uint64_t o_strides[2] = {(uint64_t)kDLatent * 2, (uint64_t)H * kDLatent * 2};
-    const uint32_t o_box[3] = {64, h_store, 1};
-    if (!make_tmap(&maps.o, o_lat, 3, o_dims, o_strides, o_box)) return MLA_ERR_CUDA;
+    // outputs as {128-byte chunk, head row, chunk index, token}: one store box
+    // covers four chunks of every head row of a token
+    const uint32_t h_rows = (uint32_t)(H < 128 ? H : 128);
+    const uint64_t o_dims[4] = {64, (uint64_t)H, (uint64_t)kDLatent / 64, rows};
+    const uint64_t o_strides[3] = {(uint64_t)kDLatent * 2, 128, (uint64_t)H * kDLatent * 2};
+    const uint32_t o_box[4] = {64, h_rows, 4, 1};
+    if (!make_tmap(&maps.o, o_lat, 4, o_dims, o_strides, o_box)) return MLA_ERR_CUDA;
     const uint64_t pieces = ((uint64_t)B + (uint64_t)num_parts) * s_q;
-    const uint64_t op_dims[3] = {(uint64_t)kDLatent, (uint64_t)H, pieces};
-    const uint64_t op_strides[2] = {(uint64_t)kDLatent * 4, (uint64_t)H * kDLatent * 4};
-    const uint32_t op_box[3] = {32, h_store, 1};
-    if (!make_tmap(&maps.op, ws + wl.o_offset, 3, op_dims, op_strides, op_box, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+    const uint64_t op_dims[4] = {32, (uint64_t)H, (uint64_t)kDLatent / 32, pieces};
+    const uint64_t op_strides[3] = {(uint64_t)kDLatent * 4, 128, (uint64_t)H * kDLatent * 4};
+    const uint32_t op_box[4] = {32, h_rows, 4, 1};
+    if (!make_tmap(&maps.op, ws + wl.o_offset, 4, op_dims, op_strides, op_box, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                    CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
         return MLA_ERR_CUDA;
 
     DecodeArgs a;
     a.q_abs = q_abs;
-    a.kv = kv_cache;
     a.block_table = block_table;
     a.mbps = max_blocks_per_seq;
     a.seqlens = cache_seqlens;
@@ -264,6 +261,7 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
     a.s_q = s_q;
     a.H = H;
     a.num_blocks = num_blocks;
+    a.qrows = (int)qrows;
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
     a.causal = causal;
     a.o_lat = o_lat;

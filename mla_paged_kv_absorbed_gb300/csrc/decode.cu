@@ -10,35 +10,32 @@
 // token s; all H heads are the 128 rows of every MMA. The two CTAs split the
 // work by role:
 //  * the score CTA (rank 0) holds the whole absorbed query of the part's
-//    current batch - dims [0, 512) in TMEM as the A operand, the 64 rope dims
-//    in shared memory - and computes S = Q' K^T for two pages at a time
-//    (N = 128 keys) into one of two TMEM buffers. Its softmax threads (one
-//    per row and page) mask, take the row max, rescale lazily, exponentiate
-//    and ship P (bf16, 128-byte-swizzled like an MMA operand) together with
-//    the per-row rescale factor straight into the value CTA's shared memory
-//    (st.async, counted on the value CTA's mbarrier);
+//    current batch in TMEM (576 dims as the A operand), computes S = Q' K^T
+//    page by page (N = 64 keys) into one of two TMEM buffers, and its softmax
+//    threads mask, take the row max, rescale lazily, exponentiate and ship P
+//    (bf16, 128-byte-swizzled like an MMA operand) together with the per-row
+//    rescale factor straight into the value CTA's shared memory (st.async,
+//    counted on the value CTA's mbarrier);
 //  * the value CTA (rank 1) keeps the fp32 output O [128 x 512] in its TMEM
-//    (all 512 columns), loads its own copy of the value rows of each page
-//    (mostly L2 hits: the score CTA has just read the same page), accumulates
-//    O += P . V, rescales O rows when the score CTA moved their reference
-//    max, and writes the normalised rows through shared memory with TMA
-//    stores.
-// Only P crosses between the CTAs (16 KB per page plus 1 KB of factors per
-// pair); no score or exponential is computed twice.
+//    (all 512 columns), loads its own copy of the page's value columns (mostly
+//    L2 hits: the score CTA has just read the same page), accumulates
+//    O += P . V, rescales O rows when the score CTA moved their reference max,
+//    and writes the normalised rows with 64 KB TMA stores, staged in the value
+//    slot of the item's last page (free once its P.V product is done).
+// Only P crosses between the CTAs (16 KB plus 1 KB of factors per page); no
+// score or exponential is computed twice.
 //
-// Loads are few and large: the TMA engine streams whole 24-32 KB boxes at
-// close to HBM speed but only about half of that as 8 KB boxes. Key tiles use
-// a 4-D view of the cache, [8-key group][64-dim chunk][8 keys][64 dims], so
-// one 24 KB box brings three chunks of a page; the two pages of a pair go
-// back to back into one 48 KB ring slot, which is then a valid 128-key MMA
-// operand (8-key groups 3 KB apart). A batch's query comes through the same
-// ring (three 48 KB boxes of 128 rows) and tcgen05.cp moves it into TMEM.
-// Value CTA per page: two 32 KB boxes of [64 keys x 256 value columns], read
-// as an MN-major operand.
+// Loads are few and large: the TMA engine of an SM works through boxes with a
+// high fixed cost per box, so a whole page (9 chunks of [64 keys x 64 dims],
+// one 3-D box over a [dims, keys, chunk] view of the cache) is a single load;
+// 8 KB boxes would stream at a fifth of the rate. The query of a new batch
+// arrives the same way (two boxes of 64 rows) and the softmax threads move it
+// into TMEM.
 // Roles (10 warps per CTA): warps 0-7 softmax (score CTA) or O rescale and
 // epilogue (value CTA), two warps per TMEM lane quadrant - on the score CTA
-// warp half h owns page h of a pair, on the value CTA O columns
-// [256 h, 256 h + 256); warp 8 TMA producer; warp 9 MMA issuer and TMEM owner.
+// warp half h owns keys [32 h, 32 h + 32) of a page, on the value CTA O
+// columns [256 h, 256 h + 256); warp 8 TMA producer; warp 9 MMA issuer and
+// TMEM owner.
 // Every wait is bounded; on expiry the kernel records MLA_ERR_TIMEOUT, tells
 // the peer CTA, drains its copies and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -54,56 +51,51 @@ constexpr int kThreads = 320;
 constexpr int kRows = 128;
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
+constexpr int kChunks = kDQK / 64;  // 9 chunks of 64 dims
 
 // ---- shared memory (offsets from a 1024-byte-aligned base) ----
-constexpr int kChunkBytes = kPage * 128;         // [64 rows x 64 bf16], 128-byte swizzle
-constexpr int kGroupChunks = 3;                  // 64-dim chunks per key box
-constexpr int kBoxBytes = kGroupChunks * kChunkBytes;  // one page, three chunks: [8 groups][3 chunks][8 x 128 B]
-constexpr int kSlotBytes = 2 * kBoxBytes;        // two pages (or 128 query rows), three chunks
-constexpr int kGroupStride = kGroupChunks * 1024;      // bytes between 8-row groups inside a slot
-constexpr int kQRopeBytes = kRows * 128;         // [128 rows x 64 rope dims]
+constexpr int kChunkBytes = kPage * 128;           // [64 rows x 64 bf16], 128-byte swizzle
+constexpr int kPageBytes = kChunks * kChunkBytes;  // a page (or 64 query rows): [9 chunks][64 rows][64 dims]
 constexpr int kOffBars = 0;
-constexpr int kOffX = 1024;                      // score: row-stat exchange; value: rescale factors and 1/l
-constexpr int kOffRole = 3072;
+constexpr int kOffX = 1024;                        // score: row-stat exchange; value: rescale factors and 1/l
+constexpr int kOffRole = 4096;
 // score CTA
-constexpr int kRing = 4;
-constexpr int kOffQRope = kOffRole;              // 2 buffers (batch parity) of the 64 rope query dims
-constexpr int kOffRing = kOffQRope + 2 * kQRopeBytes;
-constexpr int kSmemScore = kOffRing + kRing * kSlotBytes;
+constexpr int kRing = 3;
+constexpr int kOffRing = kOffRole;
+constexpr int kSmemScore = kOffRing + kRing * kPageBytes;
 // value CTA
-constexpr int kPSlotBytes = 2 * kRows * 128;     // P of a page pair: two K-chunks [128 rows x 64 keys] bf16
-constexpr int kVRing = 4;
-constexpr int kVSlotBytes = 4 * kChunkBytes;     // [64 keys x 256 value columns]
+constexpr int kPSlotBytes = kRows * 128;           // P of a page: [128 rows x 64 keys] bf16
+constexpr int kVBytes = 8 * kChunkBytes;           // a page's value columns: [8 chunks][64 keys][64 dims]
+constexpr int kVRing = 2;
 constexpr int kOffP = kOffRole;
 constexpr int kOffV = kOffP + 2 * kPSlotBytes;
-constexpr int kSmemValue = kOffV + kVRing * kVSlotBytes;
-constexpr int kSmemBytes = kSmemScore > kSmemValue ? kSmemScore : kSmemValue;
+constexpr int kSmemValue = kOffV + kVRing * kVBytes;
+constexpr int kSmemUsed = kSmemScore > kSmemValue ? kSmemScore : kSmemValue;
+constexpr int kSmemBytes = kSmemUsed + 1024;       // room to align the base to 1024 bytes
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-// one P message: P (32 KB) + rescale factor and 1/l per row (fp32)
+// one P message: P (16 KB) + rescale factor and 1/l per row (fp32)
 constexpr uint32_t kPMsgBytes = kPSlotBytes + 2 * kRows * 4;
 
 // ---- tensor memory ----
-constexpr uint32_t kTmemQ = 0;      // score CTA: query dims [0, 512) as bf16 pairs (256 columns)
-constexpr uint32_t kTmemS0 = 256;   // score CTA: S buffers, 128 columns each
-constexpr uint32_t kTmemS1 = 384;
-constexpr uint32_t kTmemCols = 512; // value CTA: O, all columns
-
-constexpr int kPrefetchPairs = 3;  // L2 prefetch distance of the score CTA's producer, in page pairs
+constexpr uint32_t kTmemQ = 0;       // score CTA: the 576 query dims as bf16 pairs (288 columns)
+constexpr uint32_t kTmemS = 288;     // score CTA: two S buffers of 64 columns
+constexpr uint32_t kTmemCols = 512;  // value CTA: O, all columns
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: tolerate growth up to 2^8 before rescaling O
 
 struct Bars {
     // score CTA
     uint64_t ring_full[kRing], ring_empty[kRing];
-    uint64_t qr_full[2], qr_empty[2];
-    uint64_t q_drained;
+    uint64_t q_full, q_drained;
     uint64_t s_full[2], s_free[2];
     uint64_t p_free[2];  // score CTA; arrivals come from the value CTA
     // value CTA
     uint64_t p_full[2];  // own arrive + expect_tx, bytes from the score CTA
     uint64_t v_full[kVRing], v_empty[kVRing];
-    uint64_t pv_done, o_full, o_ack[2], o_free[2], stage_done;  // o_ack per P slot: the O warps can run one
-                                                                 // pair ahead, never two on the same slot
+    uint64_t pv_done, o_full;
+    uint64_t o_ack[2];   // per P slot: the O warps may run one page ahead, never two on one slot
+    uint64_t o_free[2];
+    uint64_t stage_full, stage_free;  // epilogue rounds: eight warps staged / staging read by the store
     uint64_t drain;
     uint32_t tmem_slot;
     int abort;
@@ -148,12 +140,11 @@ struct ItemIter {
     }
 };
 
-// Walks the page pairs of a part in order: pages [j, j + np) of item `it`,
-// np in {1, 2}; pairs never straddle two items.
-struct PairIter {
+// Walks the pages of a part in order, with their item context.
+struct PageIter {
     ItemIter items;
     Item it;
-    int j, np, n, n_items;  // first page, pages in the pair, pair counter, items started
+    int j, n, n_items;  // page within the batch, page counter, items started
     bool valid;
     __device__ void init(const DecodeArgs& args, int part) {
         items.init(args, part);
@@ -163,21 +154,19 @@ struct PairIter {
         if (valid) {
             n_items = 1;
             j = it.lo;
-            np = min(2, it.hi - j);
         }
     }
     __device__ bool first_of_item() const { return j == it.lo; }
-    __device__ bool last_of_item() const { return j + np >= it.hi; }
+    __device__ bool last_of_item() const { return j == it.hi - 1; }
     __device__ void advance() {
         ++n;
-        j += np;
-        if (j >= it.hi) {
+        if (++j >= it.hi) {
             valid = items.next(it);
-            if (!valid) return;
-            j = it.lo;
-            ++n_items;
+            if (valid) {
+                j = it.lo;
+                ++n_items;
+            }
         }
-        np = min(2, it.hi - j);
     }
 };
 
@@ -203,70 +192,49 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int slots, int issued
 }
 
 // ============================================================== score CTA ==
+// Ring positions: every batch first takes two positions for its query (rows
+// 0-63 and 64-127), then one per page; producer, MMA warp and softmax warps
+// count them the same way.
 __device__ void score_producer(const DecodeMaps& maps, const DecodeArgs& args, Bars* bars, uint8_t* smem, int part,
                                int s, volatile int* abort) {
+    // the whole warp runs this loop (warp-uniform waits); lane 0 issues the loads
     int* err = args.err;
     const long long wait_ns = args.wait_ns;
+    const int lane = threadIdx.x & 31;
     uint8_t* ring = smem + kOffRing;
-    const int hq = min(args.H, kRows);
-    const uint32_t qbytes = (uint32_t)hq * 128;                    // rope box
-    const uint32_t qgbytes = (uint32_t)hq * 128 * kGroupChunks;   // query chunk-group box
-    PairIter pi;
+    const uint32_t qbytes = (uint32_t)(kChunks * args.qrows * 128);
+    PageIter pi;
     pi.init(args, part);
-    // The ring holds 1.3 pairs, far less than HBM latency times this CTA's share
-    // of the bandwidth; whole pages (contiguous 72 KB) are therefore requested
-    // into L2 kPrefetchPairs ahead, and the ring refills from L2.
-    PairIter pf;
-    pf.init(args, part);
-    auto prefetch_pair = [&]() {
-        if (!pf.valid) return;
-        for (int p = 0; p < pf.np; ++p) {
-            const int j = pf.j + p;
-            const int blk = j < args.mbps ? args.block_table[(size_t)pf.it.b * args.mbps + j] : -1;
-            if (blk >= 0 && blk < args.num_blocks)
-                prefetch_l2_bulk(static_cast<const uint8_t*>(args.kv) + (size_t)blk * kPage * kDQK * 2, kPage * kDQK * 2);
-        }
-        pf.advance();
-    };
-    for (int i = 0; i < kPrefetchPairs; ++i) prefetch_pair();
     bool ok = true;
-    int r = 0, nq = 0;  // ring loads issued, rope query loads issued
+    int r = 0;
     for (; ok && pi.valid; pi.advance()) {
-        prefetch_pair();
-        const int bs = pi.it.b * args.s_q + s;
         if (pi.first_of_item()) {
-            // the batch's query: dims [0, 576) through the ring, three chunks per
-            // slot (the MMA warp moves dims [0, 512) into TMEM), and the rope dims
-            // into the rope buffer of its parity
-            for (int g = 0; g < 3; ++g, ++r) {
-                if (r >= kRing) ok = mbar_wait(&bars->ring_empty[r % kRing], ((r / kRing) - 1) & 1, abort, err, wait_ns);
+            const int row0 = (pi.it.b * args.s_q + s) * args.H;
+            for (int h = 0; h < 2; ++h, ++r) {
+                if (r >= kRing) ok = warp_wait(&bars->ring_empty[r % kRing], ((r / kRing) - 1) & 1, abort, err, wait_ns);
                 if (!ok) break;
-                uint64_t* bar = &bars->ring_full[r % kRing];
-                mbar_arrive_expect_tx(bar, qgbytes);
-                tma_load_4d(ring + (r % kRing) * kSlotBytes, &maps.qg, bar, 0, 0, kGroupChunks * g, bs * args.H / 8);
+                if (lane == 0) {
+                    uint64_t* bar = &bars->ring_full[r % kRing];
+                    mbar_arrive_expect_tx(bar, qbytes);
+                    tma_load_3d(ring + (r % kRing) * kPageBytes, &maps.q, bar, 0, row0 + 64 * h, 0);
+                }
+                __syncwarp();
             }
             if (!ok) break;
-            const int qi = pi.n_items - 1;
-            if (qi >= 2) ok = mbar_wait(&bars->qr_empty[qi & 1], ((qi >> 1) - 1) & 1, abort, err, wait_ns);
-            if (!ok) break;
-            mbar_arrive_expect_tx(&bars->qr_full[qi & 1], qbytes);
-            tma_load_3d(smem + kOffQRope + (qi & 1) * kQRopeBytes, &maps.q, &bars->qr_full[qi & 1], 512, 0, bs);
-            ++nq;
         }
-        const int blk0 = checked_block(args, pi.it.b, pi.j, err);
-        const int blk1 = pi.np == 2 ? checked_block(args, pi.it.b, pi.j + 1, err) : 0;
-        for (int g = 0; g < 3; ++g, ++r) {
-            if (r >= kRing) ok = mbar_wait(&bars->ring_empty[r % kRing], ((r / kRing) - 1) & 1, abort, err, wait_ns);
-            if (!ok) break;
-            uint8_t* dst = ring + (r % kRing) * kSlotBytes;
+        if (r >= kRing) ok = warp_wait(&bars->ring_empty[r % kRing], ((r / kRing) - 1) & 1, abort, err, wait_ns);
+        if (!ok) break;
+        if (lane == 0) {
+            const int blk = checked_block(args, pi.it.b, pi.j, err);
             uint64_t* bar = &bars->ring_full[r % kRing];
-            mbar_arrive_expect_tx(bar, (uint32_t)pi.np * kBoxBytes);
-            tma_load_4d(dst, &maps.kg, bar, 0, 0, kGroupChunks * g, blk0 * (kPage / 8));
-            if (pi.np == 2) tma_load_4d(dst + kBoxBytes, &maps.kg, bar, 0, 0, kGroupChunks * g, blk1 * (kPage / 8));
+            mbar_arrive_expect_tx(bar, (uint32_t)kPageBytes);
+            tma_load_3d(ring + (r % kRing) * kPageBytes, &maps.kv, bar, 0, blk * kPage, 0);
         }
+        __syncwarp();
+        ++r;
     }
-    drain_ring(bars->ring_full, kRing, r, err);
-    drain_ring(bars->qr_full, 2, nq, err);
+    if (lane == 0) drain_ring(bars->ring_full, kRing, r, err);
+    __syncwarp();
 }
 
 // Returns false when it gave up (timeout or abort).
@@ -276,80 +244,51 @@ __device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
     const long long wait_ns = args.wait_ns;
     const int lane = threadIdx.x & 31;
     uint8_t* ring = smem + kOffRing;
-    constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, 2 * kPage, false, false);
-    PairIter pi;
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kPage, false, false);
+    PageIter pi;
     pi.init(args, part);
     bool ok = true, issued = false;
     int r = 0;
     for (; ok && pi.valid; pi.advance()) {
         const int n = pi.n, buf = n & 1, qi = pi.n_items - 1;
         if (pi.first_of_item()) {
-            // the previous batch's last score product has finished reading the query
-            if (qi > 0) ok = warp_wait(&bars->q_drained, (qi - 1) & 1, abort, err, wait_ns);
-            for (int g = 0; ok && g < 3; ++g, ++r) {
-                ok = warp_wait(&bars->ring_full[r % kRing], (r / kRing) & 1, abort, err, wait_ns);
-                if (!ok) break;
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t base = smem_u32(ring + (r % kRing) * kSlotBytes);
-                    // chunks 3g .. 3g + 2 of the query; chunk 8 (rope) stays in shared memory
-                    for (int cc = 0; cc < kGroupChunks; ++cc) {
-                        const int c = kGroupChunks * g + cc;
-                        if (c >= 8) break;
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            tmem_cp_128x256b(tmem + kTmemQ + 32u * c + 8u * kk,
-                                             desc_sw128(base + cc * 1024 + 32 * kk, 0, kGroupStride));
-                    }
-                    mma_commit(&bars->ring_empty[r % kRing]);
-                }
-                __syncwarp();
-                issued = true;
-            }
-            if (ok) ok = warp_wait(&bars->qr_full[qi & 1], (qi >> 1) & 1, abort, err, wait_ns);
+            // the softmax threads have moved the batch's query into TMEM and are
+            // done reading its two ring slots
+            ok = warp_wait(&bars->q_full, qi & 1, abort, err, wait_ns);
             if (!ok) break;
-        }
-        // S buffer `buf` was read by the softmax of pair n - 2
-        if (n >= 2) ok = warp_wait(&bars->s_free[buf], ((n >> 1) - 1) & 1, abort, err, wait_ns);
-        if (!ok) break;
-        const uint32_t d = tmem + (buf ? kTmemS1 : kTmemS0);
-        const uint32_t rope = smem_u32(smem + kOffQRope + (qi & 1) * kQRopeBytes);
-        for (int g = 0; g < 3; ++g, ++r) {
-            ok = warp_wait(&bars->ring_full[r % kRing], (r / kRing) & 1, abort, err, wait_ns);
-            if (!ok) break;
-            tc_fence_after();
             if (lane == 0) {
-                const uint32_t base = smem_u32(ring + (r % kRing) * kSlotBytes);
-#pragma unroll
-                for (int cc = 0; cc < kGroupChunks; ++cc) {
-                    const int c = kGroupChunks * g + cc;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        // keys 0-63 from the first page, 64-127 from the second (8-key groups 3 KB apart)
-                        const uint64_t bd = desc_sw128(base + cc * 1024 + 32 * kk, 0, kGroupStride);
-                        const uint32_t acc = (c | kk) != 0 ? 1u : 0u;
-                        if (c < 8)
-                            mma_bf16_ts(d, tmem + kTmemQ + 32u * c + 8u * kk, bd, idesc_s, acc);
-                        else
-                            mma_bf16_ss(d, desc_sw128(rope + 32 * kk, 0, 1024), bd, idesc_s, acc);
-                    }
-                }
-                mma_commit(&bars->ring_empty[r % kRing]);
+                mbar_arrive(&bars->ring_empty[r % kRing]);
+                mbar_arrive(&bars->ring_empty[(r + 1) % kRing]);
             }
             __syncwarp();
-            issued = true;
+            r += 2;
         }
+        // S buffer `buf` was read by the softmax of page n - 2
+        if (n >= 2) ok = warp_wait(&bars->s_free[buf], ((n >> 1) - 1) & 1, abort, err, wait_ns);
+        if (ok) ok = warp_wait(&bars->ring_full[r % kRing], (r / kRing) & 1, abort, err, wait_ns);
         if (!ok) break;
+        tc_fence_after();
         if (lane == 0) {
-            mma_commit(&bars->s_full[buf]);
-            if (pi.last_of_item()) {
-                mma_commit(&bars->q_drained);
-                mma_commit(&bars->qr_empty[qi & 1]);
+            // one descriptor per page; a K-step moves its start address field
+            // (bytes / 16) by a constant
+            const uint64_t bdesc = desc_sw128(smem_u32(ring + (r % kRing) * kPageBytes), 0, 1024);
+            const uint32_t d = tmem + kTmemS + 64u * (uint32_t)buf;
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ts(d, tmem + kTmemQ + 32u * c + 8u * kk, bdesc + (uint64_t)((c * kChunkBytes + 32 * kk) >> 4),
+                                idesc_s, (c | kk) != 0 ? 1u : 0u);
             }
+            mma_commit(&bars->ring_empty[r % kRing]);
+            mma_commit(&bars->s_full[buf]);
+            if (pi.last_of_item()) mma_commit(&bars->q_drained);
         }
         __syncwarp();
+        issued = true;
+        ++r;
     }
-    // every MMA and copy this warp issued has completed before TMEM is freed
+    // every MMA this warp issued has completed before TMEM is freed
     if (issued) {
         if (lane == 0) mma_commit(&bars->drain);
         __syncwarp();
@@ -367,48 +306,79 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
     const int row = quad * 32 + lane;
     const int pair_bar = 1 + quad;  // named barrier of the two warps sharing these rows
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    uint8_t* ring = smem + kOffRing;
     // the value CTA's P slots, factor arrays and P barriers (same offsets there)
     const uint32_t p_remote = mapa_shared(smem_u32(smem + kOffP), peer);
     const uint32_t x_remote = mapa_shared(smem_u32(smem + kOffX), peer);
     const uint32_t pfull_remote = mapa_shared(smem_u32(&bars->p_full[0]), peer);
     float* xch = reinterpret_cast<float*>(smem + kOffX);  // [2 episodes][2 halves][128 rows]
-    PairIter pi;
+    // this thread's query row inside the two 64-row query boxes
+    const int qbox = quad >> 1, qrow = 32 * (quad & 1) + lane;
+    PageIter pi;
     pi.init(args, part);
     float m = -INFINITY, l = 0.f;
-    int n_valid = 0, xe = 0;
+    int n_valid = 0, xe = 0, r = 0;
     bool ok = true;
     for (; pi.valid; pi.advance()) {
         // every exit goes through a pair barrier, so both warps of a pair leave together
-        const int n = pi.n, buf = n & 1, k = n & 1;
+        const int n = pi.n, buf = n & 1, k = n & 1, qi = pi.n_items - 1;
         const bool first = pi.first_of_item(), last = pi.last_of_item();
         if (first) {
             m = -INFINITY;
             l = 0.f;
             n_valid = visible_keys(pi.it.seqlen, args.s_q, s, args.causal);
+            // the batch's query into TMEM: row -> lane, this warp's chunks
+            // (half 0: chunks 0-4, half 1: chunks 5-8), once the previous
+            // batch's last score product has stopped reading the old one
+            if (ok && qi > 0) ok = warp_wait(&bars->q_drained, (qi - 1) & 1, abort, err, wait_ns);
+            const int rq = r + qbox;
+            if (ok) ok = warp_wait(&bars->ring_full[rq % kRing], (rq / kRing) & 1, abort, err, wait_ns);
+            if (ok) {
+                tc_fence_after();
+                const bool have = qrow < args.qrows;  // fewer than 64 query rows in the whole call
+                const uint8_t* src = ring + (rq % kRing) * kPageBytes + qrow * 128;
+                const int c0 = half ? 5 : 0, c1 = half ? kChunks : 5;
+#pragma unroll 1
+                for (int c = c0; c < c1; ++c) {
+                    uint32_t v[32];
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const uint4 x = have ? *reinterpret_cast<const uint4*>(src + c * args.qrows * 128 +
+                                                                               ((w ^ (qrow & 7)) << 4))
+                                             : make_uint4(0, 0, 0, 0);
+                        v[4 * w] = x.x;
+                        v[4 * w + 1] = x.y;
+                        v[4 * w + 2] = x.z;
+                        v[4 * w + 3] = x.w;
+                    }
+                    tmem_st32(tmem + lane_base + kTmemQ + 32u * c, v);
+                }
+                tmem_wait_st();
+                fence_proxy_async_smem();  // the slots are refilled by TMA after this release
+                tc_fence_before();
+                mbar_arrive(&bars->q_full);
+            }
+            r += 2;
         }
-        float x[64];
+        ++r;
+        float x[32];
         if (ok) ok = warp_wait(&bars->s_full[buf], (n >> 1) & 1, abort, err, wait_ns);
         if (ok) {
             tc_fence_after();
-            const uint32_t col = tmem + lane_base + (buf ? kTmemS1 : kTmemS0) + 64u * half;
             uint32_t v[32];
-            tmem_ld32(col, v);
+            tmem_ld32(tmem + lane_base + kTmemS + 64u * (uint32_t)buf + 32u * (uint32_t)half, v);
             tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]) * args.scale_log2;
-            tmem_ld32(col + 32, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) x[32 + c] = __uint_as_float(v[c]) * args.scale_log2;
             tc_fence_before();
             mbar_arrive(&bars->s_free[buf]);
         }
-        // keys of this half: page j + half; columns past the visible keys (or of a
-        // missing second page) are masked by selection, so garbage never leaks
-        const int vcount = half < pi.np ? min(max(n_valid - (pi.j + half) * kPage, 0), kPage) : 0;
+        // keys of this half; columns past the visible keys are masked by
+        // selection, so whatever the tail rows of the page hold never leaks
+        const int vcount = min(max(n_valid - pi.j * kPage - 32 * half, 0), 32);
         float mh = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < 32; ++c) {
             x[c] = c < vcount ? x[c] : -INFINITY;
             mh = fmaxf(mh, x[c]);
         }
@@ -427,24 +397,25 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
             m = mx;
         }
         const float m_use = m == -INFINITY ? 0.f : m;
-        uint32_t pk[32];
+        uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 0; c < 16; ++c) {
             // the row sum takes the fp32 probabilities; only the P.V operand is bf16
             const float p0 = fast_exp2(x[2 * c] - m_use), p1 = fast_exp2(x[2 * c + 1] - m_use);
             l += p0 + p1;
             pk[c] = pack_bf16x2(p0, p1);
         }
-        // slot k held pair n - 2 until the value CTA released it
+        // slot k held page n - 2 until the value CTA released it
         if (ok && n >= 2) ok = warp_wait(&bars->p_free[k], ((n >> 1) - 1) & 1, abort, err, wait_ns);
         const uint32_t mbar = pfull_remote + (uint32_t)k * 8u;
         if (ok) {
-            // row `row` of K-chunk `half`: 16-byte word q at position q ^ (row % 8)
-            const uint32_t dst = p_remote + (uint32_t)(k * kPSlotBytes + half * kRows * 128 + row * 128);
+            // row `row`, keys [32 half, 32 half + 32): 16-byte words 4 half .. 4 half + 3,
+            // word w stored at position w ^ (row % 8)
+            const uint32_t dst = p_remote + (uint32_t)(k * kPSlotBytes + row * 128);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                st_async_u4(dst + (uint32_t)((q ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
-                            pk[4 * q + 3], mbar);
+            for (int q = 0; q < 4; ++q)
+                st_async_u4(dst + (uint32_t)(((4 * half + q) ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1],
+                            pk[4 * q + 2], pk[4 * q + 3], mbar);
             if (half == 0)
                 st_async_b32(x_remote + (uint32_t)(k * 1024 + row * 4), __float_as_uint(row < args.H ? alpha : 1.f),
                              mbar);
@@ -483,22 +454,18 @@ __device__ void value_producer(const DecodeMaps& maps, const DecodeArgs& args, B
     int* err = args.err;
     const long long wait_ns = args.wait_ns;
     uint8_t* vring = smem + kOffV;
-    PairIter pi;
+    PageIter pi;
     pi.init(args, part);
     bool ok = true;
     int v = 0;
     for (; ok && pi.valid; pi.advance()) {
-        for (int p = 0; ok && p < pi.np; ++p) {
-            const int blk = checked_block(args, pi.it.b, pi.j + p, err);
-            for (int h = 0; h < 2; ++h, ++v) {
-                if (v >= kVRing) ok = mbar_wait(&bars->v_empty[v % kVRing], ((v / kVRing) - 1) & 1, abort, err, wait_ns);
-                if (!ok) break;
-                uint8_t* dst = vring + (v % kVRing) * kVSlotBytes;
-                uint64_t* bar = &bars->v_full[v % kVRing];
-                mbar_arrive_expect_tx(bar, (uint32_t)kVSlotBytes);
-                tma_load_3d(dst, &maps.v, bar, 0, blk * kPage, 4 * h);
-            }
-        }
+        if (v >= kVRing) ok = mbar_wait(&bars->v_empty[v % kVRing], ((v / kVRing) - 1) & 1, abort, err, wait_ns);
+        if (!ok) break;
+        const int blk = checked_block(args, pi.it.b, pi.j, err);
+        uint64_t* bar = &bars->v_full[v % kVRing];
+        mbar_arrive_expect_tx(bar, (uint32_t)kVBytes);
+        tma_load_3d(vring + (v % kVRing) * kVBytes, &maps.v, bar, 0, blk * kPage, 0);
+        ++v;
     }
     drain_ring(bars->v_full, kVRing, v, err);
 }
@@ -510,10 +477,9 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
     const int lane = threadIdx.x & 31;
     uint8_t* vring = smem + kOffV;
     constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, 256, false, true);
-    PairIter pi;
+    PageIter pi;
     pi.init(args, part);
     bool ok = true, issued = false;
-    int v = 0;
     for (; ok && pi.valid; pi.advance()) {
         const int n = pi.n, k = n & 1, qi = pi.n_items - 1;
         const bool first = pi.first_of_item(), last = pi.last_of_item();
@@ -521,59 +487,53 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
         if (!ok) break;
         if (lane == 0) {
             // P was written by the peer's generic stores: make it visible to the
-            // tensor pipe, then arm the slot for pair n + 2 (its bytes can only
-            // come after this pair has released the slot)
+            // tensor pipe, then arm the slot for page n + 2 (its bytes can only
+            // come after this page has released the slot)
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&bars->p_full[k], kPMsgBytes);
         }
         __syncwarp();
         // the O warps have read this message's factors (and rescaled O if asked)
         ok = warp_wait(&bars->o_ack[k], (n >> 1) & 1, abort, err, wait_ns);
+        // a batch's first product overwrites O: its previous epilogue must have read it
+        if (ok && first && qi > 0) ok = warp_wait(&bars->o_free[0], (qi - 1) & 1, abort, err, wait_ns);
+        if (ok && first && qi > 0) ok = warp_wait(&bars->o_free[1], (qi - 1) & 1, abort, err, wait_ns);
+        if (ok) ok = warp_wait(&bars->v_full[n % kVRing], (n / kVRing) & 1, abort, err, wait_ns);
         if (!ok) break;
-        for (int p = 0; ok && p < pi.np; ++p) {
-            const int page = pi.j + p;
-            const int tail = page == pi.it.nblk - 1 ? pi.it.seqlen - page * kPage : kPage;
-            for (int h = 0; h < 2; ++h, ++v) {
-                // a batch's first product overwrites O: its previous epilogue must have read it
-                if (first && p == 0 && qi > 0) ok = warp_wait(&bars->o_free[h], (qi - 1) & 1, abort, err, wait_ns);
-                if (ok) ok = warp_wait(&bars->v_full[v % kVRing], (v / kVRing) & 1, abort, err, wait_ns);
-                if (!ok) break;
-                uint8_t* vs = vring + (v % kVRing) * kVSlotBytes;
-                if (tail < kPage) {
-                    // rows past seqlen hold arbitrary bytes: zero them so that
-                    // 0-probability keys cannot inject NaN/Inf into P.V
-                    const int per_chunk = (kPage - tail) * 8;  // 16-byte words
-                    for (int i = lane; i < 4 * per_chunk; i += 32) {
-                        const int c = i / per_chunk, w = i % per_chunk;
-                        reinterpret_cast<uint4*>(vs + c * kChunkBytes + tail * 128)[w] = make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t a_base = smem_u32(smem + kOffP + k * kPSlotBytes + p * kRows * 128);
-                    const uint32_t v_base = smem_u32(vs);
-#pragma unroll
-                    for (int kk = 0; kk < kPage / 16; ++kk)
-                        mma_bf16_ss(tmem + 256u * h, desc_sw128(a_base + 32 * kk, 0, 1024),
-                                    desc_sw128(v_base + 2048 * kk, kChunkBytes, 1024), idesc_pv,
-                                    (first && p == 0 && kk == 0) ? 0u : 1u);
-                    mma_commit(&bars->v_empty[v % kVRing]);
-                }
-                __syncwarp();
-                issued = true;
+        uint8_t* vs = vring + (n % kVRing) * kVBytes;
+        const int tail = pi.j == pi.it.nblk - 1 ? pi.it.seqlen - pi.j * kPage : kPage;
+        if (tail < kPage) {
+            // rows past seqlen hold arbitrary bytes: zero them so that
+            // 0-probability keys cannot inject NaN/Inf into P.V
+            const int per_chunk = (kPage - tail) * 8;  // 16-byte words
+            for (int i = lane; i < 8 * per_chunk; i += 32) {
+                const int c = i / per_chunk, w = i % per_chunk;
+                reinterpret_cast<uint4*>(vs + c * kChunkBytes + tail * 128)[w] = make_uint4(0, 0, 0, 0);
             }
+            fence_proxy_async_smem();
+            __syncwarp();
         }
-        if (!ok) break;
+        tc_fence_after();
         if (lane == 0) {
+            const uint64_t adesc = desc_sw128(smem_u32(smem + kOffP + k * kPSlotBytes), 0, 1024);
+            const uint64_t vdesc = desc_sw128(smem_u32(vs), kChunkBytes, 1024);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int kk = 0; kk < kPage / 16; ++kk)
+                    mma_bf16_ss(tmem + 256u * h, adesc + (uint64_t)((32 * kk) >> 4),
+                                vdesc + (uint64_t)((4 * h * kChunkBytes + 2048 * kk) >> 4), idesc_pv,
+                                (first && kk == 0) ? 0u : 1u);
+            }
+            // the last page's slot becomes the epilogue's staging area, which
+            // hands it back to the producer
+            if (!last) mma_commit(&bars->v_empty[n % kVRing]);
             mma_commit(&bars->pv_done);
-            if (last)
-                mma_commit(&bars->o_full);  // the epilogue hands the slot back after staging in it
-            else
-                mma_commit_multicast(&bars->p_free[k], (uint16_t)1u);  // arrives on the score CTA (rank 0)
+            if (last) mma_commit(&bars->o_full);
+            mma_commit_multicast(&bars->p_free[k], (uint16_t)1u);  // arrives on the score CTA (rank 0)
         }
         __syncwarp();
+        issued = true;
     }
     if (issued) {
         if (lane == 0) mma_commit(&bars->drain);
@@ -584,7 +544,7 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
 }
 
 __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bars* bars, uint8_t* smem,
-                             uint32_t tmem, int part, int s, uint32_t peer, volatile int* abort) {
+                             uint32_t tmem, int part, int s, volatile int* abort) {
     int* err = args.err;
     const long long wait_ns = args.wait_ns;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -593,10 +553,11 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const float* xv = reinterpret_cast<const float*>(smem + kOffX);  // [slot][factor 128 | 1/l 128]
     const uint32_t ocol = tmem + lane_base + 256u * (uint32_t)half;
-    PairIter pi;
+    PageIter pi;
     pi.init(args, part);
     bool ok = true;
     bool stored = false;
+    int erounds = 0;  // epilogue rounds so far (phase of stage_full / stage_free)
     for (; ok && pi.valid; pi.advance()) {
         const int n = pi.n, k = n & 1, qi = pi.n_items - 1;
         const bool first = pi.first_of_item(), last = pi.last_of_item();
@@ -628,97 +589,108 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
         if (lane == 0) mbar_arrive(&bars->o_ack[k]);
         if (!last) continue;
 
-        // ---- epilogue of the item: O * (1/l) -> staging (the pair's P slot) -> TMA store
+        // ---- epilogue of the item: O * (1/l) -> staging -> TMA store. The
+        // staging area is the value slot of this last page: 64 KB, i.e. 256 bf16
+        // or 128 fp32 columns of all rows per round, stored as one box
+        // [4 chunks][rows][128 B] (128-byte swizzle) by thread 0 once the eight
+        // warps have written their parts (stage_full), after which the area is
+        // free for the next round (stage_free).
         ok = warp_wait(&bars->o_full, qi & 1, abort, err, wait_ns);
         if (!ok) break;
         tc_fence_after();
         const Item& it = pi.it;
-        const bool store = quad * 32 < args.H;
-        uint8_t* stage = smem + kOffP + k * kPSlotBytes + warp * 4096;  // [32 rows x 128 B], 128-byte swizzle
-        uint8_t* srow = stage + lane * 128;
-        if (!it.split) {
-            const int z = it.b * args.s_q + s;
+        const bool row_ok = row < args.H;
+        const int hrows = min(args.H, kRows);
+        uint8_t* stage = smem + kOffV + (n % kVRing) * kVBytes;
+        const int rounds = it.split ? 4 : 2;
+        const int z = it.split ? it.piece * args.s_q + s : it.b * args.s_q + s;
+        for (int rnd = 0; rnd < rounds; ++rnd) {
+            // this warp: chunks 2 half, 2 half + 1 of the round (64 bf16 or 32 fp32 columns each)
 #pragma unroll 1
-            for (int i = 0; i < 4; ++i) {
-                const int col = 64 * i;
-                uint32_t v0[32], v1[32];
-                tmem_ld32(ocol + col, v0);
-                tmem_ld32(ocol + col + 32, v1);
-                tmem_wait_ld();
-                if (!store) continue;
+            for (int cc = 0; cc < 2; ++cc) {
+                const int chunk = 2 * half + cc;
+                uint8_t* dst = stage + chunk * hrows * 128 + row * 128;
+                if (!it.split) {
+                    const uint32_t col = (uint32_t)(256 * rnd + 64 * chunk);  // absolute O column
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(tmem + lane_base + col, v0);
+                    tmem_ld32(tmem + lane_base + col + 32, v1);
+                    tmem_wait_ld();
+                    if (row_ok) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4 w0, w1;
-                    w0.x = pack_bf16x2(__uint_as_float(v0[8 * q + 0]) * inv_l, __uint_as_float(v0[8 * q + 1]) * inv_l);
-                    w0.y = pack_bf16x2(__uint_as_float(v0[8 * q + 2]) * inv_l, __uint_as_float(v0[8 * q + 3]) * inv_l);
-                    w0.z = pack_bf16x2(__uint_as_float(v0[8 * q + 4]) * inv_l, __uint_as_float(v0[8 * q + 5]) * inv_l);
-                    w0.w = pack_bf16x2(__uint_as_float(v0[8 * q + 6]) * inv_l, __uint_as_float(v0[8 * q + 7]) * inv_l);
-                    w1.x = pack_bf16x2(__uint_as_float(v1[8 * q + 0]) * inv_l, __uint_as_float(v1[8 * q + 1]) * inv_l);
-                    w1.y = pack_bf16x2(__uint_as_float(v1[8 * q + 2]) * inv_l, __uint_as_float(v1[8 * q + 3]) * inv_l);
-                    w1.z = pack_bf16x2(__uint_as_float(v1[8 * q + 4]) * inv_l, __uint_as_float(v1[8 * q + 5]) * inv_l);
-                    w1.w = pack_bf16x2(__uint_as_float(v1[8 * q + 6]) * inv_l, __uint_as_float(v1[8 * q + 7]) * inv_l);
-                    *reinterpret_cast<uint4*>(srow + ((q ^ (lane & 7)) << 4)) = w0;
-                    *reinterpret_cast<uint4*>(srow + (((q + 4) ^ (lane & 7)) << 4)) = w1;
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d(&maps.o, stage, 256 * half + col, quad * 32, z);
-                    bulk_commit_group();
-                    bulk_wait_group_read0();
-                }
-                __syncwarp();
-                stored = true;
-            }
-        } else {
-            const int z = it.piece * args.s_q + s;
-#pragma unroll 1
-            for (int i = 0; i < 8; ++i) {
-                const int col = 32 * i;
-                uint32_t v0[32];
-                tmem_ld32(ocol + col, v0);
-                tmem_wait_ld();
-                if (!store) continue;
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 w0, w1;
+                            w0.x = pack_bf16x2(__uint_as_float(v0[8 * q + 0]) * inv_l, __uint_as_float(v0[8 * q + 1]) * inv_l);
+                            w0.y = pack_bf16x2(__uint_as_float(v0[8 * q + 2]) * inv_l, __uint_as_float(v0[8 * q + 3]) * inv_l);
+                            w0.z = pack_bf16x2(__uint_as_float(v0[8 * q + 4]) * inv_l, __uint_as_float(v0[8 * q + 5]) * inv_l);
+                            w0.w = pack_bf16x2(__uint_as_float(v0[8 * q + 6]) * inv_l, __uint_as_float(v0[8 * q + 7]) * inv_l);
+                            w1.x = pack_bf16x2(__uint_as_float(v1[8 * q + 0]) * inv_l, __uint_as_float(v1[8 * q + 1]) * inv_l);
+                            w1.y = pack_bf16x2(__uint_as_float(v1[8 * q + 2]) * inv_l, __uint_as_float(v1[8 * q + 3]) * inv_l);
+                            w1.z = pack_bf16x2(__uint_as_float(v1[8 * q + 4]) * inv_l, __uint_as_float(v1[8 * q + 5]) * inv_l);
+                            w1.w = pack_bf16x2(__uint_as_float(v1[8 * q + 6]) * inv_l, __uint_as_float(v1[8 * q + 7]) * inv_l);
+                            *reinterpret_cast<uint4*>(dst + ((q ^ (row & 7)) << 4)) = w0;
+                            *reinterpret_cast<uint4*>(dst + (((q + 4) ^ (row & 7)) << 4)) = w1;
+                        }
+                    }
+                } else {
+                    const uint32_t col = (uint32_t)(128 * rnd + 32 * chunk);
+                    uint32_t v0[32];
+                    tmem_ld32(tmem + lane_base + col, v0);
+                    tmem_wait_ld();
+                    if (row_ok) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float4 w;
-                    w.x = __uint_as_float(v0[4 * q + 0]) * inv_l;
-                    w.y = __uint_as_float(v0[4 * q + 1]) * inv_l;
-                    w.z = __uint_as_float(v0[4 * q + 2]) * inv_l;
-                    w.w = __uint_as_float(v0[4 * q + 3]) * inv_l;
-                    *reinterpret_cast<float4*>(srow + ((q ^ (lane & 7)) << 4)) = w;
+                        for (int q = 0; q < 8; ++q) {
+                            float4 w;
+                            w.x = __uint_as_float(v0[4 * q + 0]) * inv_l;
+                            w.y = __uint_as_float(v0[4 * q + 1]) * inv_l;
+                            w.z = __uint_as_float(v0[4 * q + 2]) * inv_l;
+                            w.w = __uint_as_float(v0[4 * q + 3]) * inv_l;
+                            *reinterpret_cast<float4*>(dst + ((q ^ (row & 7)) << 4)) = w;
+                        }
+                    }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d(&maps.op, stage, 256 * half + col, quad * 32, z);
-                    bulk_commit_group();
-                    bulk_wait_group_read0();
-                }
-                __syncwarp();
-                stored = true;
             }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(&bars->o_free[half]);
-            mbar_arrive(&bars->stage_done);
-        }
-        if (warp == 0) {
-            // all eight warps are done with the staging area: give the P slot back
-            ok = warp_wait(&bars->stage_done, qi & 1, abort, err, wait_ns);
-            if (ok && lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&bars->p_free[k]), peer));
+            if (rnd == rounds - 1) {
+                // O has been read: the next item's products may overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->o_free[half]);
+            }
+            fence_proxy_async_smem();
             __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->stage_full);
+            if (warp == 0) {
+                ok = warp_wait(&bars->stage_full, erounds & 1, abort, err, wait_ns);
+                if (ok && lane == 0) {
+                    if (it.split)
+                        tma_store_4d(&maps.op, stage, 0, 0, 4 * rnd, z);
+                    else
+                        tma_store_4d(&maps.o, stage, 0, 0, 4 * rnd, z);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();  // the next round rewrites the staging area
+                    stored = true;
+                    mbar_arrive(&bars->stage_free);
+                }
+                __syncwarp();
+            }
+            if (ok) ok = warp_wait(&bars->stage_free, erounds & 1, abort, err, wait_ns);
+            ++erounds;
+            if (!ok) break;
         }
+        if (!ok) break;
+        // staging read by the last store: the slot goes back to the producer
+        if (threadIdx.x == 0) mbar_arrive(&bars->v_empty[n % kVRing]);
     }
-    if (stored && lane == 0) bulk_wait_group0();
+    if (stored) bulk_wait_group0();
     return ok;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeMaps maps, DecodeArgs args) {
-    extern __shared__ __align__(16) uint8_t smem[];
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms; both CTAs run the same
+    // kernel, so the offsets used for remote addresses agree
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
     volatile int* abort = &bars->abort;
 
@@ -729,43 +701,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int part = cluster_id / args.s_q;
     const int s = cluster_id % args.s_q;
 
-    // the layout needs 1024-byte-aligned swizzle atoms and leaves no room to
-    // realign; both CTAs see the same base and leave together
-    if ((smem_u32(smem) & 1023u) != 0) {
-        if (threadIdx.x == 0) record_error(args.err, kErrUnsupported);
-        cluster_sync_all();
-        return;
-    }
-
     if (threadIdx.x == 0) {
         for (int i = 0; i < kRing; ++i) {
             mbar_init(&bars->ring_full[i], 1);
             mbar_init(&bars->ring_empty[i], 1);
         }
+        mbar_init(&bars->q_full, 256);
+        mbar_init(&bars->q_drained, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars->qr_full[i], 1);
-            mbar_init(&bars->qr_empty[i], 1);
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->s_free[i], 256);
             mbar_init(&bars->p_free[i], 1);
             mbar_init(&bars->p_full[i], 1);
-            mbar_init(&bars->o_free[i], 4);
             mbar_init(&bars->o_ack[i], 8);
+            mbar_init(&bars->o_free[i], 4);
         }
-        mbar_init(&bars->q_drained, 1);
         for (int i = 0; i < kVRing; ++i) {
             mbar_init(&bars->v_full[i], 1);
             mbar_init(&bars->v_empty[i], 1);
         }
         mbar_init(&bars->pv_done, 1);
         mbar_init(&bars->o_full, 1);
-        mbar_init(&bars->stage_done, 8);
+        mbar_init(&bars->stage_full, 8);
+        mbar_init(&bars->stage_free, 1);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_mbarrier_init_cluster();
         if (rank == 0) {
-            tma_prefetch_desc(&maps.kg);
-            tma_prefetch_desc(&maps.qg);
+            tma_prefetch_desc(&maps.kv);
             tma_prefetch_desc(&maps.q);
         } else {
             tma_prefetch_desc(&maps.v);
@@ -793,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     if (rank == 0) {
         if (warp == kWarpProducer) {
-            if ((threadIdx.x & 31) == 0) score_producer(maps, args, bars, smem, part, s, abort);
+            score_producer(maps, args, bars, smem, part, s, abort);
         } else if (warp == kWarpMma) {
             ok = score_mma(args, bars, smem, tmem, part, abort);
         } else {
@@ -805,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == kWarpMma) {
             ok = value_mma(args, bars, smem, tmem, part, abort);
         } else {
-            ok = value_owarps(maps, args, bars, smem, tmem, part, s, peer, abort);
+            ok = value_owarps(maps, args, bars, smem, tmem, part, s, abort);
         }
     }
     // a role that gave up tells the peer, whose waits then end promptly
@@ -814,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     // the peer may still store into our buffers or arrive on our barriers until
-    // it has finished its last pair: leave together
+    // it has finished its last page: leave together
     cluster_sync_all();
     if (warp == kWarpMma) {
         tc_fence_after();

@@ -44,7 +44,6 @@ cudaError_t launch_head_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b, c
 
 struct DecodeArgs {
     const void* q_abs;  // bf16 [B, s_q, H, 576]
-    const void* kv;     // bf16 [num_blocks, 64, 576] (L2 prefetch only; loads go through the tensor maps)
     const int32_t* block_table;
     int mbps;
     const int32_t* seqlens;
@@ -52,6 +51,7 @@ struct DecodeArgs {
     const int32_t* num_splits;
     int num_parts;
     int B, s_q, H, num_blocks;
+    int qrows;         // rows of one query box: min(64, B * s_q * H)
     float scale_log2;  // softmax_scale * log2(e)
     int causal;
     void* o_lat;       // bf16 [B, s_q, H, 512]
@@ -66,17 +66,17 @@ int decode_max_active_clusters(int device);
 
 // TMA descriptors of the decode kernel (all 128-byte swizzle; dims listed
 // innermost first):
-//  kg: the cache as {64 dims, 8 keys, 9 chunks, num_blocks * 8 key groups},
-//      strides {1152, 128, 9216} B; box {64, 8, 3, 8} = three chunks of a page
-//  v:  the cache as {64 dims, num_blocks * 64 keys, 9 chunks}, strides {1152, 128} B;
-//      box {64, 64, 4} = four value chunks of a page
-//  qg: q_abs as {64 dims, 8 rows, 9 chunks, B * s_q * H / 8 row groups}, strides
-//      {1152, 128, 9216} B; box {64, 8, 3, min(H, 128) / 8}
-//  q:  q_abs as [B * s_q, H, 576], box [1 x min(H, 128) x 64] (the rope dims)
-//  o:  bf16 [B * s_q, H, 512], box [1 x min(H, 32) x 64]   (store)
-//  op: fp32 [pieces * s_q, H, 512], box [1 x min(H, 32) x 32] (store)
+//  kv: the cache as {64 dims, num_blocks * 64 keys, 9 chunks}, strides {1152, 128} B;
+//      box {64, 64, 9} = one whole page, [chunk][key][64 dims] in shared memory
+//  v:  the same view, box {64, 64, 8} = the page's 512 value columns
+//  q:  q_abs as {64 dims, B * s_q * H rows, 9 chunks}, strides {1152, 128} B;
+//      box {64, qrows, 9} with qrows = min(64, B * s_q * H)
+//  o:  o_lat as {64 cols, H rows, 8 chunks, B * s_q}, strides {1024, 128, H * 1024} B;
+//      box {64, min(H, 128), 4, 1} (store)
+//  op: o_part as {32 cols, H rows, 16 chunks, pieces * s_q}, strides {2048, 128, H * 2048} B;
+//      box {32, min(H, 128), 4, 1} (store)
 struct DecodeMaps {
-    CUtensorMap kg, v, qg, q, o, op;
+    CUtensorMap kv, v, q, o, op;
 };
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, cudaStream_t stream);
 
