@@ -601,17 +601,21 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
         const Item& it = pi.it;
         const bool row_ok = row < args.H;
         const int hrows = min(args.H, kRows);
-        uint8_t* stage = smem + kOffV + (n % kVRing) * kVBytes;
-        const int rounds = it.split ? 4 : 2;
+        // after the part's last item no page is loaded any more and both value
+        // slots can stage: one round of eight chunks instead of two of four
+        const bool wide = it.b == pi.items.row[2];
+        uint8_t* stage = wide ? smem + kOffV : smem + kOffV + (n % kVRing) * kVBytes;
+        const int cpr = wide ? 8 : 4;  // 128-byte chunks per round (64 bf16 or 32 fp32 columns)
+        const int rounds = (it.split ? 16 : 8) / cpr;
         const int z = it.split ? it.piece * args.s_q + s : it.b * args.s_q + s;
         for (int rnd = 0; rnd < rounds; ++rnd) {
-            // this warp: chunks 2 half, 2 half + 1 of the round (64 bf16 or 32 fp32 columns each)
+            // this warp: chunks [cpr/2 half, cpr/2 half + cpr/2) of the round
 #pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-                const int chunk = 2 * half + cc;
+            for (int cc = 0; cc < cpr / 2; ++cc) {
+                const int chunk = (cpr / 2) * half + cc;
                 uint8_t* dst = stage + chunk * hrows * 128 + row * 128;
                 if (!it.split) {
-                    const uint32_t col = (uint32_t)(256 * rnd + 64 * chunk);  // absolute O column
+                    const uint32_t col = (uint32_t)(64 * (cpr * rnd + chunk));  // absolute O column
                     uint32_t v0[32], v1[32];
                     tmem_ld32(tmem + lane_base + col, v0);
                     tmem_ld32(tmem + lane_base + col + 32, v1);
@@ -633,7 +637,7 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
                         }
                     }
                 } else {
-                    const uint32_t col = (uint32_t)(128 * rnd + 32 * chunk);
+                    const uint32_t col = (uint32_t)(32 * (cpr * rnd + chunk));
                     uint32_t v0[32];
                     tmem_ld32(tmem + lane_base + col, v0);
                     tmem_wait_ld();
@@ -662,10 +666,14 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
             if (warp == 0) {
                 ok = warp_wait(&bars->stage_full, erounds & 1, abort, err, wait_ns);
                 if (ok && lane == 0) {
-                    if (it.split)
-                        tma_store_4d(&maps.op, stage, 0, 0, 4 * rnd, z);
-                    else
-                        tma_store_4d(&maps.o, stage, 0, 0, 4 * rnd, z);
+                    // boxes of four chunks
+                    for (int b4 = 0; b4 < cpr / 4; ++b4) {
+                        uint8_t* src = stage + b4 * 4 * hrows * 128;
+                        if (it.split)
+                            tma_store_4d(&maps.op, src, 0, 0, cpr * rnd + 4 * b4, z);
+                        else
+                            tma_store_4d(&maps.o, src, 0, 0, cpr * rnd + 4 * b4, z);
+                    }
                     bulk_commit_group();
                     bulk_wait_group_read0();  // the next round rewrites the staging area
                     stored = true;
