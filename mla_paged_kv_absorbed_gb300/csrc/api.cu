@@ -92,19 +92,21 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA
 int head_gemm(const void* a, int a_row_elems, const void* w, int K, int N, int n_cta, void* out, int out_row_elems,
               const void* rope_src, int B, int s_q, int H, cudaStream_t stream) {
     const int R = B * s_q;
-    CUtensorMap tm_a, tm_b;
-    const uint64_t a_dims[3] = {(uint64_t)a_row_elems, (uint64_t)H, (uint64_t)R};
-    const uint64_t a_strides[2] = {(uint64_t)a_row_elems * 2, (uint64_t)H * a_row_elems * 2};
-    const uint32_t a_box[3] = {64, 1, 128};
-    const uint64_t b_dims[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)H};
-    const uint64_t b_strides[2] = {(uint64_t)N * 2, (uint64_t)K * N * 2};
-    const uint32_t b_box[3] = {64, 64, 1};
-    CUtensorMap tm_out;
-    const uint64_t o_dims[3] = {(uint64_t)out_row_elems, (uint64_t)H, (uint64_t)R};
-    const uint64_t o_strides[2] = {(uint64_t)out_row_elems * 2, (uint64_t)H * out_row_elems * 2};
-    if (!make_tmap(&tm_a, a, 3, a_dims, a_strides, a_box)) return MLA_ERR_CUDA;
-    if (!make_tmap(&tm_b, w, 3, b_dims, b_strides, b_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) return MLA_ERR_CUDA;
-    if (!make_tmap(&tm_out, out, 3, o_dims, o_strides, a_box)) return MLA_ERR_CUDA;
+    // [64-column chunk][row] views (4-D, innermost first): one box is 128 rows
+    // x several chunks of a head
+    CUtensorMap tm_a, tm_b, tm_out;
+    const uint64_t a_dims[4] = {64, (uint64_t)R, (uint64_t)a_row_elems / 64, (uint64_t)H};
+    const uint64_t a_strides[3] = {(uint64_t)H * a_row_elems * 2, 128, (uint64_t)a_row_elems * 2};
+    const uint32_t a_box[4] = {64, 128, 2, 1};
+    const uint64_t b_dims[4] = {64, (uint64_t)K, (uint64_t)N / 64, (uint64_t)H};
+    const uint64_t b_strides[3] = {(uint64_t)N * 2, 128, (uint64_t)K * N * 2};
+    const uint32_t b_box[4] = {64, 128, (uint32_t)n_cta / 64, 1};
+    const uint64_t o_dims[4] = {64, (uint64_t)R, (uint64_t)out_row_elems / 64, (uint64_t)H};
+    const uint64_t o_strides[3] = {(uint64_t)H * out_row_elems * 2, 128, (uint64_t)out_row_elems * 2};
+    const uint32_t o_box[4] = {64, 128, (uint32_t)n_cta / 64, 1};
+    if (!make_tmap(&tm_a, a, 4, a_dims, a_strides, a_box)) return MLA_ERR_CUDA;
+    if (!make_tmap(&tm_b, w, 4, b_dims, b_strides, b_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) return MLA_ERR_CUDA;
+    if (!make_tmap(&tm_out, out, 4, o_dims, o_strides, o_box)) return MLA_ERR_CUDA;
     GemmArgs args;
     args.R = R;
     args.H = H;

@@ -8,10 +8,14 @@
 // One CTA computes a [128 rows x n_cta] tile of one head: rows are the
 // B * s_q query tokens (TMA zero-fills rows past the end), the accumulator
 // lives in TMEM (n_cta fp32 columns), A (activations, K-major) and B (the
-// head's weight, N-major) stream through a TMA ring of 64-wide K chunks in
-// 128-byte-swizzled shared memory. Warp 0 produces, one thread of warp 1
-// issues the MMAs, and all four warps run the epilogue: TMEM -> bf16 -> the
-// (now idle) stage buffers in the same swizzled layout -> TMA tensor stores.
+// head's weight, N-major) stream through a TMA ring of 128-deep K stages in
+// 128-byte-swizzled shared memory. Each stage is two boxes only - A as
+// [2 chunks][128 rows][64], B as [n_cta/64 chunks][128 k][64] through 4-D
+// views - because the TMA engine of an SM spends a large fixed time per box
+// (8-16 KB boxes stream at 20-35 GB/s per SM, 64 KB boxes at ~110).
+// Warp 0 produces, one thread of warp 1 issues the MMAs, and all four warps
+// run the epilogue: TMEM -> bf16 -> the (now idle) stage buffers in the same
+// swizzled layout -> one TMA tensor store.
 #include <cuda_bf16.h>
 
 #include "mla_internal.h"
@@ -25,15 +29,16 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kBM = 128;
-constexpr int kBK = 64;
+constexpr int kBK = 128;  // K per stage: two 64-wide swizzle chunks
 
 template <int NCTA, int STAGES>
 struct GemmSmem {
-    static constexpr int kABytes = kBM * kBK * 2;          // 16 KB
-    static constexpr int kBBytes = kBK * NCTA * 2;         // NCTA/64 atoms of 8 KB
+    static constexpr int kABytes = kBM * kBK * 2;          // 32 KB: [2][128 rows][64]
+    static constexpr int kBBytes = kBK * NCTA * 2;         // [NCTA/64][128 k][64]
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kBarOffset = STAGES * kStageBytes;
     static constexpr int kBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
+    static_assert(kStageBytes * STAGES >= kBM * NCTA * 2, "epilogue staging fits the stage buffers");
 };
 
 template <int NCTA, int STAGES>
@@ -90,9 +95,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* a_dst = smem + s * L::kStageBytes;
             uint8_t* b_dst = a_dst + L::kABytes;
             mbar_arrive_expect_tx(&full[s], L::kStageBytes);
-            tma_load_3d(a_dst, &tm_a, &full[s], kc * kBK, h, m0);
-#pragma unroll
-            for (int j = 0; j < NCTA / 64; ++j) tma_load_3d(b_dst + j * 8192, &tm_b, &full[s], n0 + 64 * j, kc * kBK, h);
+            tma_load_4d(a_dst, &tm_a, &full[s], 0, m0, 2 * kc, h);
+            tma_load_4d(b_dst, &tm_b, &full[s], 0, kc * kBK, n0 / 64, h);
             issued = kc + 1;
         }
         // never leave with a copy in flight: wait for the last load of every stage
@@ -110,10 +114,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 const uint32_t a_base = smem_u32(smem + s * L::kStageBytes);
                 const uint32_t b_base = a_base + L::kABytes;
+                const uint64_t ad0 = desc_sw128(a_base, 0, 1024);
+                const uint64_t bd0 = desc_sw128(b_base, kBK * 128, 1024);  // n-chunks are 128 k-rows apart
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk) {
-                    const uint64_t ad = desc_sw128(a_base + kk * 32, 0, 1024);
-                    const uint64_t bd = desc_sw128(b_base + kk * 2048, 8192, 1024);
+                    const uint64_t ad = ad0 + (uint64_t)(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+                    const uint64_t bd = bd0 + (uint64_t)((kk * 2048) >> 4);
                     mma_bf16_ss(tmem, ad, bd, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(&empty[s]);
@@ -125,8 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // epilogue: thread t owns tile row t (output row m0 + t). Every load and MMA
-    // is complete once `done` fires, so the stage buffers hold the bf16 tile in
-    // 64-column swizzled boxes, which TMA stores (rows past R are clipped).
+    // is complete once `done` fires, so the stage buffers take the bf16 tile as
+    // [NCTA/64 chunks][128 rows][128 B] (swizzled), which one TMA box stores
+    // (rows past R are clipped).
     const bool ok = mbar_wait(done, 0, nullptr, err, kDrainNs) && !*abort;
     tc_fence_after();
     const int t = threadIdx.x;
@@ -136,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), v);
         tmem_wait_ld();
-        uint8_t* box = smem + (c / 2) * (kBM * 128) + t * 128;  // box of 64 columns, row t
+        uint8_t* box = smem + (c / 2) * (kBM * 128) + t * 128;  // chunk of 64 columns, row t
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int gidx = (c & 1) * 4 + i;  // 16-byte granule inside the 128-byte row
@@ -150,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     __syncthreads();
     if (t == 0 && ok) {
-        for (int c = 0; c < NCTA / 64; ++c) tma_store_3d(&tm_out, smem + c * (kBM * 128), n0 + 64 * c, h, m0);
+        tma_store_4d(&tm_out, smem, 0, m0, n0 / 64, h);
         bulk_commit_group();
         bulk_wait_group_read0();
     }
@@ -162,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kDRope * 2 / 16; ++i) dst[i] = src[i];
     }
+    if (t == 0 && ok) bulk_wait_group0();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, NCTA);
@@ -200,8 +208,9 @@ cudaError_t gemm_error_fetch(int* out, cudaStream_t stream) {
 
 cudaError_t launch_head_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const CUtensorMap* tm_out,
                              const GemmArgs& args, long long wait_ns, cudaStream_t stream) {
-    if (args.n_cta == 256) return launch_variant<256, 2>(tm_a, tm_b, tm_out, args, wait_ns, stream);
-    if (args.n_cta == 128) return launch_variant<128, 4>(tm_a, tm_b, tm_out, args, wait_ns, stream);
+    // absorb: K = 128, one stage (two CTAs fit an SM); out-proj: K = 512 through three stages
+    if (args.n_cta == 256) return launch_variant<256, 1>(tm_a, tm_b, tm_out, args, wait_ns, stream);
+    if (args.n_cta == 128) return launch_variant<128, 3>(tm_a, tm_b, tm_out, args, wait_ns, stream);
     return cudaErrorInvalidValue;
 }
 
