@@ -7,10 +7,16 @@
 // decode kernel for Hopper GPUs", usage example) but not the formula; this is
 // the standard merge of softmax pieces.
 //
-// One CTA per (batch, query token); one warp per head row; each lane owns 16
-// of the 512 latent columns as four float4 (coalesced 512-byte rows). Batches
-// with a single piece were written directly by the decode kernel and are
-// skipped; batches with no piece (seqlen 0) get o = 0, lse = -inf.
+// Work units of four query rows (b, s, h .. h + 3), one warp per row, so that
+// even a few long sequences spread over many SMs; a CTA walks a contiguous
+// range of units (consecutive units mostly share their batch, so a batch that
+// was not split costs one cached read per unit). Each lane owns 16 of the 512 latent
+// columns as four float4 (coalesced 512-byte rows per instruction). The
+// lanes read the pieces' lse values and reduce max and sum by shuffles; the
+// pieces are then accumulated in ascending order, four at a time so that 16
+// loads per lane are in flight. Batches with a single piece were written
+// directly by the decode kernel and are skipped; batches with no piece
+// (seqlen 0) get o = 0, lse = -inf.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -20,61 +26,107 @@
 namespace mla {
 namespace {
 
-constexpr int kThreads = 256;
+// 128 threads: with its ~110 registers a CTA still fits on an SM beside a
+// decode CTA, so the combine CTAs can wait at griddepcontrol before the
+// decode ends
+constexpr int kThreads = 128;
+constexpr int kRowsPerCta = kThreads / 32;
 
-__global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __restrict__ num_splits, int s_q, int H,
-                                                           const float* __restrict__ o_part,
+__device__ void combine_row(const int32_t* __restrict__ num_splits, int row, int s_q, int H,
+                            const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                            __nv_bfloat16* __restrict__ o_lat, float* __restrict__ lse) {
+    const int lane = threadIdx.x & 31;
+    const int h = row % H;
+    const int s = (row / H) % s_q;
+    const int b = row / (H * s_q);
+    const int first = num_splits[b];
+    const int n = num_splits[b + 1] - first;
+    if (n == 1) return;
+    // lse of piece i of this row
+    auto lse_of = [&](int i) { return lse_part[((size_t)(first + i) * s_q + s) * H + h]; };
+    float L = -INFINITY;
+    for (int i = lane; i < n; i += 32) L = fmaxf(L, lse_of(i));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, o));
+    float total = -INFINITY;
+    float4 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (L != -INFINITY) {
+        float sum = 0.f;
+        for (int i = lane; i < n; i += 32) sum += expf(lse_of(i) - L);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        total = L + logf(sum);
+        for (int i0 = 0; i0 < n; i0 += 4) {
+            float4 v[4][4];
+            float w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j;
+                w[j] = 0.f;
+                if (i < n) {
+                    const size_t prow = ((size_t)(first + i) * s_q + s) * H + h;
+                    w[j] = expf(lse_part[prow] - total);
+                    const float4* src = reinterpret_cast<const float4*>(o_part + prow * kDLatent);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) v[j][k] = src[lane + 32 * k];
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) v[j][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    acc[k].x += w[j] * v[j][k].x;
+                    acc[k].y += w[j] * v[j][k].y;
+                    acc[k].z += w[j] * v[j][k].z;
+                    acc[k].w += w[j] * v[j][k].w;
+                }
+        }
+    }
+    uint2* dst = reinterpret_cast<uint2*>(o_lat + (size_t)row * kDLatent);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x, acc[k].y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z, acc[k].w);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&lo);
+        u.y = *reinterpret_cast<uint32_t*>(&hi);
+        dst[lane + 32 * k] = u;
+    }
+    if (lane == 0) lse[row] = total;
+}
+
+__global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __restrict__ num_splits, int rows, int s_q,
+                                                           int H, const float* __restrict__ o_part,
                                                            const float* __restrict__ lse_part,
                                                            __nv_bfloat16* __restrict__ o_lat,
                                                            float* __restrict__ lse) {
     // launched as a programmatic dependent of the decode kernel: wait for it
     griddep_wait();
     griddep_launch_dependents();
-    const int b = blockIdx.x / s_q;
-    const int s = blockIdx.x % s_q;
-    const int first = num_splits[b];
-    const int n = num_splits[b + 1] - first;
-    if (n == 1) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int h = warp; h < H; h += kThreads / 32) {
-        const size_t row = ((size_t)b * s_q + s) * H + h;
-        float4 acc[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        float total = -INFINITY;
-        if (n > 1) {
-            float L = -INFINITY;
-            for (int i = 0; i < n; ++i) L = fmaxf(L, lse_part[((size_t)(first + i) * s_q + s) * H + h]);
-            if (L != -INFINITY) {
-                float sum = 0.f;
-                for (int i = 0; i < n; ++i) sum += expf(lse_part[((size_t)(first + i) * s_q + s) * H + h] - L);
-                total = L + logf(sum);
-                for (int i = 0; i < n; ++i) {
-                    const size_t prow = ((size_t)(first + i) * s_q + s) * H + h;
-                    const float w = expf(lse_part[prow] - total);
-                    const float4* src = reinterpret_cast<const float4*>(o_part + prow * kDLatent);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float4 v = src[lane + 32 * k];
-                        acc[k].x += w * v.x;
-                        acc[k].y += w * v.y;
-                        acc[k].z += w * v.z;
-                        acc[k].w += w * v.w;
-                    }
-                }
-            }
+    const int units = (rows + kRowsPerCta - 1) / kRowsPerCta;
+    const int per_cta = (units + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int u0 = (int)blockIdx.x * per_cta, u1 = min(units, u0 + per_cta);
+    for (int base = u0; base < u1; base += 32) {
+        // the piece counts of this warp's rows in up to 32 units, read at once
+        // (lane j: unit base + j); only rows of split or empty batches have work
+        const int row_j = (base + lane) * kRowsPerCta + warp;  // ((b * s_q) + s) * H + h
+        int n_j = 1;
+        if (base + lane < u1 && row_j < rows) {
+            const int b = row_j / (H * s_q);
+            n_j = num_splits[b + 1] - num_splits[b];
         }
-        uint2* dst = reinterpret_cast<uint2*>(o_lat + row * kDLatent);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x, acc[k].y);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z, acc[k].w);
-            uint2 v;
-            v.x = *reinterpret_cast<uint32_t*>(&lo);
-            v.y = *reinterpret_cast<uint32_t*>(&hi);
-            dst[lane + 32 * k] = v;
+        unsigned todo = __ballot_sync(0xffffffffu, n_j != 1);
+        while (todo) {
+            const int j = __ffs(todo) - 1;
+            todo &= todo - 1;
+            combine_row(num_splits, (base + j) * kRowsPerCta + warp, s_q, H, o_part, lse_part, o_lat, lse);
         }
-        if (lane == 0) lse[row] = total;
     }
 }
 
@@ -83,7 +135,18 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __rest
 cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, const float* o_part,
                            const float* lse_part, void* o_lat, float* lse, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(B * s_q, 1, 1);
+    const int rows = B * s_q * H;
+    const int units = (rows + kRowsPerCta - 1) / kRowsPerCta;
+    static int sm_count = 0;
+    if (sm_count == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sm_count <= 0)
+            sm_count = 152;
+    }
+    // at most two CTAs per SM: enough rows in flight for a few long sequences
+    // whose pieces cover the whole part list
+    cfg.gridDim = dim3(units < 1 ? 1 : (units < 2 * sm_count ? units : 2 * sm_count), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -91,7 +154,7 @@ cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, num_splits, s_q, H, o_part, lse_part,
+    return cudaLaunchKernelEx(&cfg, combine_kernel, num_splits, rows, s_q, H, o_part, lse_part,
                               static_cast<__nv_bfloat16*>(o_lat), lse);
 }
 
