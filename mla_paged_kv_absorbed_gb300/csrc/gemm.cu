@@ -102,6 +102,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         // never leave with a copy in flight: wait for the last load of every stage
         for (int kc = issued - STAGES > 0 ? issued - STAGES : 0; kc < issued; ++kc)
             mbar_wait(&full[kc % STAGES], (kc / STAGES) & 1, nullptr, err, kDrainNs);
+    } else if (warp >= 2 && args.rope_src != nullptr) {
+        // rope columns (absorb): q[r,h,128:192] -> q_abs[r,h,512:576], 128 bytes per
+        // row. The CTAs of the head's n tiles share the tile's rows; eight
+        // consecutive threads move one row, so each warp instruction covers four
+        // whole 128-byte rows. Done by the two idle warps while the stage loads.
+        const int nt = (int)gridDim.x;
+        const int rows_per = (kBM + nt - 1) / nt;
+        const int r0 = m0 + (int)blockIdx.x * rows_per;
+        const int r1 = min(min(r0 + rows_per, m0 + kBM), args.R);
+        const int tt = threadIdx.x - 64;  // 0..63
+        for (int base = r0 * 8; base < r1 * 8; base += 64 * 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int idx = base + i * 64 + tt;  // row * 8 + 16-byte word
+                if (idx < r1 * 8) {
+                    const int row = idx >> 3, w = idx & 7;
+                    v[i] = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.rope_src) +
+                                                          ((size_t)row * args.H + h) * kDQ + kDNope)[w];
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int idx = base + i * 64 + tt;
+                if (idx < r1 * 8) {
+                    const int row = idx >> 3, w = idx & 7;
+                    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) +
+                                             ((size_t)row * args.H + h) * args.out_row_elems + kDLatent)[w] = v[i];
+                }
+            }
+        }
     } else if (warp == 1) {
         // MMA issuer
         constexpr uint32_t idesc = idesc_bf16_f32(kBM, NCTA, false, true);
@@ -137,7 +168,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool ok = mbar_wait(done, 0, nullptr, err, kDrainNs) && !*abort;
     tc_fence_after();
     const int t = threadIdx.x;
-    const int row = m0 + t;
 #pragma unroll 1
     for (int c = 0; c < NCTA / 32; ++c) {
         uint32_t v[32];
@@ -160,14 +190,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_store_4d(&tm_out, smem, 0, m0, n0 / 64, h);
         bulk_commit_group();
         bulk_wait_group_read0();
-    }
-    if (args.rope_src != nullptr && blockIdx.x == 0 && row < args.R) {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.rope_src) +
-                                                          ((size_t)row * args.H + h) * kDQ + kDNope);
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) +
-                                              ((size_t)row * args.H + h) * args.out_row_elems + kDLatent);
-#pragma unroll
-        for (int i = 0; i < kDRope * 2 / 16; ++i) dst[i] = src[i];
     }
     if (t == 0 && ok) bulk_wait_group0();
     tc_fence_before();
