@@ -203,12 +203,30 @@ __device__ void score_producer(const DecodeMaps& maps, const DecodeArgs& args, B
     const int lane = threadIdx.x & 31;
     uint8_t* ring = smem + kOffRing;
     const uint32_t qbytes = (uint32_t)(kChunks * args.qrows * 128);
+    // The part's first batch is the first entry of its schedule row (a part
+    // never starts on an empty batch), so its query is requested right after
+    // that one read, while the walk below still reads the batch's length.
+    const int* trow = args.tile_meta + 8 * part;
+    const int b_first = trow[0];
+    const bool q_early = trow[5] > 0;
+    if (q_early && lane == 0) {
+        const int row0 = (b_first * args.s_q + s) * args.H;
+        for (int h = 0; h < 2; ++h) {
+            mbar_arrive_expect_tx(&bars->ring_full[h], qbytes);
+            tma_load_3d(ring + h * kPageBytes, &maps.q, &bars->ring_full[h], 0, row0 + 64 * h, 0);
+        }
+    }
+    __syncwarp();
     PageIter pi;
     pi.init(args, part);
+    // a schedule from other sequence lengths could start elsewhere
+    if (q_early && lane == 0 && (!pi.valid || pi.it.b != b_first)) record_error(err, kErrBadBlock);
     bool ok = true;
     int r = 0;
     for (; ok && pi.valid; pi.advance()) {
-        if (pi.first_of_item()) {
+        if (pi.first_of_item() && q_early && pi.n_items == 1) {
+            r = 2;  // the first query went out above
+        } else if (pi.first_of_item()) {
             const int row0 = (pi.it.b * args.s_q + s) * args.H;
             for (int h = 0; h < 2; ++h, ++r) {
                 if (r >= kRing) ok = warp_wait(&bars->ring_empty[r % kRing], ((r / kRing) - 1) & 1, abort, err, wait_ns);
@@ -233,6 +251,7 @@ __device__ void score_producer(const DecodeMaps& maps, const DecodeArgs& args, B
         __syncwarp();
         ++r;
     }
+    if (q_early && r < 2) r = 2;  // the early query loads land before the CTA may leave
     if (lane == 0) drain_ring(bars->ring_full, kRing, r, err);
     __syncwarp();
 }
