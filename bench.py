@@ -21,11 +21,17 @@ Inputs stay resident in HBM; several independent input sets (one per emulated
 layer) rotate so that the bytes touched between two uses of a set exceed
 twice the L2 size, so the KV cache streams from HBM.
 
-The timed loop calls the C ABI directly with pre-marshalled arguments; CUDA
-events on the launching stream bracket the whole region and every decode call
-(for the roofline of the dominant kernel). `e2e` repeats the step through the
-same C ABI with the step's inputs copied from pinned host buffers and the
-result copied back inside the timed region. `--impl reference` times the CPU
+The timed region is one CUDA graph of the K steps' C-ABI calls (captured on
+a stream of its own from pre-marshalled arguments after the warm-up steps,
+replayed once untimed), so that the host's launch cost and jitter (the Grace
+cores are shared with the node's other GPUs) stay out of a device-timed
+number; CUDA events bracket the region. The decode kernel's launch duration
+(for the roofline of the dominant kernel) comes from a second graph of the
+same K decode calls alone, bracketed the same way. `--eager` (and
+`--profile`) time the eager calls instead, with events around every decode
+call. `e2e` repeats the step through the same C ABI with the
+step's inputs copied from pinned host buffers and the result copied back
+inside the timed region, the host synchronising on the result every step. `--impl reference` times the CPU
 oracle (the reference implementation of this path) on a bounded sample of the
 same workload.
 """
@@ -63,6 +69,7 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--profile", action="store_true", help="short run for a profiler: no clocks, e2e or cpu leg")
+    p.add_argument("--eager", action="store_true", help="time eager C-ABI calls instead of replaying a CUDA graph")
     return p.parse_args()
 
 
@@ -215,6 +222,42 @@ def run_step(L, a: StepArgs, ev=None, meta=False):
     return rc
 
 
+def make_step_graph(torch, api, L, sets, num_parts, ws, dev, S):
+    """Captures S consecutive steps (absorb, decode + combine, out-proj through
+    the C ABI over the rotating input sets) on a stream of their own, and a
+    second graph of the same S decode calls alone; replays both once untimed.
+    Returns (step graph, decode graph, stream), or None when the capture is
+    refused (the caller then times the eager loop)."""
+    stream = torch.cuda.Stream(dev)
+    n = len(sets)
+    gsteps = [StepArgs(api, s, num_parts, ws, stream.cuda_stream) for s in sets]
+    try:
+        with torch.cuda.stream(stream):
+            rc = 0
+            for a in gsteps:
+                rc |= L.mla_get_metadata(*a.meta)
+            for i in range(2 * n):
+                rc |= run_step(L, gsteps[i % n])
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(S):
+                    rc |= run_step(L, gsteps[i % n])
+            # the decode calls (with their combine) alone, for the kernel's launch duration
+            gd = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gd, stream=stream):
+                for i in range(S):
+                    rc |= L.mla_decode_paged(*gsteps[i % n].decode)
+            g.replay()
+            gd.replay()
+            stream.synchronize()
+        if rc != 0 or api.mla_read_device_error(ws) != 0:
+            return None
+        return g, gd, stream
+    except Exception:
+        return None
+
+
 def workload_flops(inp):
     s = inp.seqlens.clamp(min=0).long()
     if inp.causal and inp.s_q > 1:
@@ -278,32 +321,62 @@ def run_ours(args, world, rank, local):
         meta_us = m0.elapsed_time(m1) * 1e3 / 200
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
-    if not args.profile:
+    use_graph = not (args.profile or args.eager) and K <= 8192
+    graph = make_step_graph(torch, api, L, sets, num_parts, ws, dev, K) if use_graph else None
+    if graph is not None:
+        # The K steps (absorb, decode + combine, out-proj over the rotating input
+        # sets) as one CUDA graph, replayed once untimed and once timed: the
+        # host's launch cost and jitter stay out of the device timing.
+        g, gd, gstream = graph
         clocks.start()
         time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    t_start.record()
-    rc = 0
-    for i in range(K):
-        rc |= run_step(L, steps[i % n_sets], ev[i])
-    t_end.record()
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop() if not args.profile else {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-    if rc != 0:
-        raise RuntimeError("a C-ABI call returned an error in the timed region")
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(gstream):
+            t_start.record()
+            g.replay()
+            t_end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        clk = clocks.stop()
+        # the decode kernel's launch duration: the K decode calls alone, replayed
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(gstream):
+            d0.record()
+            gd.replay()
+            d1.record()
+        torch.cuda.synchronize()
+        dec_ms = [d0.elapsed_time(d1) / K]
+        timed = ("one CUDA graph of the K steps' C-ABI calls, replayed, CUDA events around it; the decode "
+                 "launch duration from a graph of the K decode calls alone")
+    else:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        if not args.profile:
+            clocks.start()
+            time.sleep(0.3)
+        barrier(world)
+        torch.cuda.synchronize()
+        t_start.record()
+        rc = 0
+        for i in range(K):
+            rc |= run_step(L, steps[i % n_sets], ev[i])
+        t_end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        clk = clocks.stop() if not args.profile else {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if rc != 0:
+            raise RuntimeError("a C-ABI call returned an error in the timed region")
+        dec_ms = [e[0].elapsed_time(e[1]) for e in ev]
+        timed = "C-ABI calls, CUDA events on the launching stream"
     st = api.mla_read_device_error(ws)
     if st != 0:
         raise RuntimeError(f"device error in the timed region: {api.status_string(st)}")
     total_ms = t_start.elapsed_time(t_end)
     ms_step = max_over_ranks(total_ms / K, world, dev)
-    dec_ms = [e[0].elapsed_time(e[1]) for e in ev]
     dec_avg_ms = statistics.mean(dec_ms)
-    dec_med_ms = statistics.median(dec_ms)
+    dec_med_ms = statistics.median(dec_ms) if len(dec_ms) > 1 else None
 
     kv_bytes = sets[0].kv_bytes()
     attn_flops, proj_flops = workload_flops(sets[0])
@@ -319,7 +392,8 @@ def run_ours(args, world, rank, local):
                 "frac": round(achieved_tflops / tc_sustained, 4)}
     roof.update({"traffic": recorded_traffic(), "kernel": "mla_decode_paged (decode + combine launches)",
                  "algorithmic_bytes_per_launch": kv_bytes, "algorithmic_flops_per_launch": attn_flops,
-                 "avg_launch_us": round(dec_avg_ms * 1e3, 3), "median_launch_us": round(dec_med_ms * 1e3, 3),
+                 "avg_launch_us": round(dec_avg_ms * 1e3, 3),
+                 "median_launch_us": None if dec_med_ms is None else round(dec_med_ms * 1e3, 3),
                  "binding_roofline_frac": round(t_roof_ms / dec_avg_ms, 4),
                  "tensor_tflops": round(achieved_tflops, 1), "tensor_frac_of_sustained": round(achieved_tflops / tc_sustained, 4),
                  "peak_source": peak_src})
@@ -335,7 +409,7 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replicas x{world} (sequences shard, no collective)",
                    "l2": f"rotate {n_sets} resident input sets, {n_sets * per_set / 1e6:.0f} MB > 2 x L2 "
                          f"({l2 / 1e6:.0f} MB)",
-                   "num_parts": num_parts, "timed": "C-ABI calls, CUDA events on the launching stream"},
+                   "num_parts": num_parts, "timed": timed},
         "roofline": roof,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")} | {"samples": clk.get("samples", 0)},
         "gpu_launches": 4 * K,
@@ -346,18 +420,22 @@ def run_ours(args, world, rank, local):
     }
 
     if not args.no_e2e and not args.profile:
-        result["e2e"] = run_e2e(args, api, L, sets, steps, dev, world)
+        result["e2e"] = run_e2e(args, api, L, sets, num_parts, ws, dev, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
         result["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0)
     return result
 
 
-def run_e2e(args, api, L, sets, steps, dev, world):
+def run_e2e(args, api, L, sets, num_parts, ws, dev, world):
     """Same step through the C ABI with the step's inputs in pinned host memory:
     H2D of q, cache_seqlens and block_table, the four calls, D2H of out and lse,
-    and a stream synchronisation so the host holds the result, every step."""
+    and a stream synchronisation so the host holds the result, every step. The
+    calls go to a stream of their own; the reported value replays a CUDA graph
+    of exactly these calls (captured once per input set), as a serving loop
+    would, and the eager loop's time is reported beside it."""
     import torch
-    stream = torch.cuda.current_stream(dev)
+    stream = torch.cuda.Stream(dev)
+    steps = [StepArgs(api, s, num_parts, ws, stream.cuda_stream) for s in sets]
     host = []
     for s, a in zip(sets, steps):
         host.append({
@@ -370,7 +448,7 @@ def run_e2e(args, api, L, sets, steps, dev, world):
     d2h = host[0]["out"].numel() * 2 + host[0]["lse"].numel() * 4
     n = len(sets)
 
-    def one(i):
+    def enqueue(i):
         s, a, h = sets[i % n], steps[i % n], host[i % n]
         s.q.copy_(h["q"], non_blocking=True)
         s.seqlens.copy_(h["seqlens"], non_blocking=True)
@@ -378,25 +456,54 @@ def run_e2e(args, api, L, sets, steps, dev, world):
         rc = run_step(L, a, meta=True)
         h["out"].copy_(a.out, non_blocking=True)
         h["lse"].copy_(a.lse, non_blocking=True)
-        stream.synchronize()
         return rc
 
-    for i in range(5):
-        one(i)
     K = args.e2e_steps
-    barrier(world)
-    t0 = time.perf_counter()
     rc = 0
-    for i in range(K):
-        rc |= one(i)
-    t1 = time.perf_counter()
-    barrier(world)
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            rc |= enqueue(i)
+            stream.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(K):
+            rc |= enqueue(i)
+            stream.synchronize()
+        t1 = time.perf_counter()
+        barrier(world)
+        eager_us = max_over_ranks((t1 - t0) / K * 1e6, world, dev)
+        graphs, why = [], None
+        try:
+            for i in range(n):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    rc |= enqueue(i)
+                graphs.append(g)
+        except Exception as ex:  # capture refused: report the eager loop
+            graphs, why = [], f"{type(ex).__name__}: {ex}"[:200]
+        us, mode = eager_us, "eager C-ABI calls"
+        if graphs:
+            for i in range(5):
+                graphs[i % n].replay()
+                stream.synchronize()
+            barrier(world)
+            t0 = time.perf_counter()
+            for i in range(K):
+                graphs[i % n].replay()
+                stream.synchronize()
+            t1 = time.perf_counter()
+            barrier(world)
+            us = max_over_ranks((t1 - t0) / K * 1e6, world, dev)
+            mode = "CUDA graph of the C-ABI calls and copies, one per input set, replayed"
     if rc != 0:
         raise RuntimeError("C-ABI error in the e2e loop")
-    us = max_over_ranks((t1 - t0) / K * 1e6, world, dev)
-    return {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": K, "note": "KV cache and weights stay resident (model state); per step the queries, "
+    out = {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+           "mode": mode, "eager_value": round(eager_us, 3),
+           "steps": K, "note": "KV cache and weights stay resident (model state); per step the queries, "
                                 "lengths and page table go up and the projected output and lse come back"}
+    if why:
+        out["graph_error"] = why
+    return out
 
 
 # ------------------------------------------------------------ oracle timing --
