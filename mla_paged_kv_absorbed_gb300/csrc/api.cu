@@ -184,7 +184,7 @@ int mla_absorb_q(const mla_bf16_t* q, const mla_bf16_t* w_uk, mla_bf16_t* q_abs,
     if (!aligned16(q) || !aligned16(w_uk) || !aligned16(q_abs)) return MLA_ERR_INVALID_ARG;
     int dev = check_device();
     if (dev != MLA_OK) return dev;
-    return head_gemm(q, kDQ, w_uk, kDNope, kDLatent, 256, q_abs, kDQK, q, B, s_q, H,
+    return head_gemm(q, kDQ, w_uk, kDNope, kDLatent, 128, q_abs, kDQK, q, B, s_q, H,
                      static_cast<cudaStream_t>(stream));
 }
 

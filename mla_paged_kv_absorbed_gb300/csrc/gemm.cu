@@ -217,6 +217,292 @@ cudaError_t launch_variant(const CUtensorMap* tm_a, const CUtensorMap* tm_b, con
     return cudaLaunchKernelEx(&cfg, kern, *tm_a, *tm_b, *tm_out, args, wait_ns);
 }
 
+// ---------------------------------------------------------------------------
+// absorb_kernel: the absorb projection (K = 128) as a persistent kernel. Work
+// units are (head, 128-row tile, 128-column quarter of the 512 outputs); each
+// CTA (one per SM) walks a contiguous range of them, so it keeps the head's
+// query tile across its units, and the units' stages overlap: the weight tile
+// of a later unit loads while an earlier unit's output is being stored. (One
+// CTA per 256-column tile loaded, multiplied and stored in lockstep with all
+// the others, so HBM saw a read phase and then a write phase.)
+// Warps: 0 TMA producer, 1 MMA issuer and TMEM owner, 2-5 epilogue (one
+// thread per tile row: TMEM -> bf16 -> swizzled staging -> TMA store), 6 the
+// rope columns of the units with quarter 0.
+constexpr int kAbsThreads = 224;
+constexpr int kAbsN = 128;      // output columns per unit
+constexpr int kAbsQuarters = 4; // 512 / kAbsN
+constexpr int kAbsBSlots = 3;
+
+struct AbsSmem {
+    static constexpr int kA = kBM * 128 * 2;       // [2 chunks][128 rows][64]: the query tile (K = 128)
+    static constexpr int kB = 128 * kAbsN * 2;     // [2 n-chunks][128 k][64]
+    static constexpr int kStage = kBM * kAbsN * 2; // [2 chunks][128 rows][64] bf16 output
+    static constexpr int kOffA = 0;                // two query slots
+    static constexpr int kOffB = kOffA + 2 * kA;   // weight ring
+    static constexpr int kOffS = kOffB + kAbsBSlots * kB;  // two staging buffers
+    static constexpr int kOffBar = kOffS + 2 * kStage;
+    static constexpr int kBytes = kOffBar + 256 + 1024;    // + barriers + alignment slack
+};
+static_assert(AbsSmem::kBytes <= 232448, "absorb kernel shared memory");
+
+// At most one bulk store group of this thread still reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
+struct AbsUnit {
+    int h, mt, nq, g;  // head, row tile, column quarter, group = (h, mt)
+};
+__device__ __forceinline__ AbsUnit abs_unit(int u, int mtiles) {
+    AbsUnit x;
+    x.g = u / kAbsQuarters;
+    x.nq = u % kAbsQuarters;
+    x.h = x.g / mtiles;
+    x.mt = x.g % mtiles;
+    return x;
+}
+
+__global__ void __launch_bounds__(kAbsThreads, 1)
+    absorb_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                  const __grid_constant__ CUtensorMap tm_out, GemmArgs args, long long wait_ns) {
+    using L = AbsSmem;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+    uint64_t* a_empty = a_full + 2;
+    uint64_t* b_full = a_empty + 2;
+    uint64_t* b_empty = b_full + kAbsBSlots;
+    uint64_t* acc_full = b_empty + kAbsBSlots;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* done = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mtiles = (args.R + kBM - 1) / kBM;
+    const int units = args.H * mtiles * kAbsQuarters;
+    const int u0 = (int)(((long long)blockIdx.x * units) / gridDim.x);
+    const int u1 = (int)(((long long)(blockIdx.x + 1) * units) / gridDim.x);
+    int* err = &g_gemm_error;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&a_full[i], 1);
+            mbar_init(&a_empty[i], 1);
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);  // one arrival per epilogue warp
+        }
+        for (int i = 0; i < kAbsBSlots; ++i) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_empty[i], 1);
+        }
+        mbar_init(done, 1);
+        *abort = 0;
+        fence_mbarrier_init_cluster();
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+        tma_prefetch_desc(&tm_out);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 2 * kAbsN);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // launched as a programmatic dependent: the set-up above overlaps the
+    // previous kernel; no global memory is touched before it has completed
+    griddep_wait();
+    griddep_launch_dependents();
+
+    if (warp == 0) {
+        // producer: the whole warp walks the units (uniform waits), lane 0 loads
+        bool ok = true;
+        int gi = -1, prev_g = -1, issued = 0;
+        for (int u = u0; ok && u < u1; ++u) {
+            const int i = u - u0;
+            const AbsUnit x = abs_unit(u, mtiles);
+            if (x.g != prev_g) {
+                prev_g = x.g;
+                ++gi;
+                const int sa = gi & 1;
+                // the query slot held group gi - 2 until its last product
+                if (gi >= 2) ok = warp_wait(&a_empty[sa], ((gi >> 1) - 1) & 1, abort, err, wait_ns);
+                if (!ok) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&a_full[sa], L::kA);
+                    tma_load_4d(smem + L::kOffA + sa * L::kA, &tm_a, &a_full[sa], 0, x.mt * kBM, 0, x.h);
+                }
+                __syncwarp();
+            }
+            const int sb = i % kAbsBSlots;
+            if (i >= kAbsBSlots) ok = warp_wait(&b_empty[sb], ((i / kAbsBSlots) - 1) & 1, abort, err, wait_ns);
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&b_full[sb], L::kB);
+                tma_load_4d(smem + L::kOffB + sb * L::kB, &tm_b, &b_full[sb], 0, 0, x.nq * (kAbsN / 64), x.h);
+            }
+            __syncwarp();
+            issued = i + 1;
+        }
+        // never leave with a copy in flight: the last load of every slot has landed
+        if (lane == 0) {
+            for (int i = issued - kAbsBSlots > 0 ? issued - kAbsBSlots : 0; i < issued; ++i)
+                mbar_wait(&b_full[i % kAbsBSlots], (i / kAbsBSlots) & 1, nullptr, err, kDrainNs);
+            for (int g = gi - 1 > 0 ? gi - 1 : 0; g <= gi; ++g)
+                mbar_wait(&a_full[g & 1], (g >> 1) & 1, nullptr, err, kDrainNs);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // MMA issuer: unit i into accumulator i % 2
+        constexpr uint32_t idesc = idesc_bf16_f32(kBM, kAbsN, false, true);
+        bool ok = true, issued = false;
+        int gi = -1, prev_g = -1;
+        for (int u = u0; ok && u < u1; ++u) {
+            const int i = u - u0;
+            const AbsUnit x = abs_unit(u, mtiles);
+            if (x.g != prev_g) {
+                prev_g = x.g;
+                ++gi;
+            }
+            const int sa = gi & 1, sb = i % kAbsBSlots, ac = i & 1;
+            ok = warp_wait(&a_full[sa], (gi >> 1) & 1, abort, err, wait_ns);
+            if (ok) ok = warp_wait(&b_full[sb], (i / kAbsBSlots) & 1, abort, err, wait_ns);
+            // the epilogue has read unit i - 2 out of this accumulator
+            if (ok && i >= 2) ok = warp_wait(&acc_empty[ac], ((i >> 1) - 1) & 1, abort, err, wait_ns);
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint64_t ad0 = desc_sw128(smem_u32(smem + L::kOffA + sa * L::kA), 0, 1024);
+                const uint64_t bd0 = desc_sw128(smem_u32(smem + L::kOffB + sb * L::kB), 128 * 128, 1024);  // n-chunks 128 k-rows apart
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t ad = ad0 + (uint64_t)(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+                    const uint64_t bd = bd0 + (uint64_t)((kk * 2048) >> 4);
+                    mma_bf16_ss(tmem + (uint32_t)(ac * kAbsN), ad, bd, idesc, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&b_empty[sb]);
+                mma_commit(&acc_full[ac]);
+                const bool last_of_group = (u + 1 == u1) || ((u + 1) / kAbsQuarters != x.g);
+                if (last_of_group) mma_commit(&a_empty[sa]);
+            }
+            __syncwarp();
+            issued = true;
+        }
+        if (issued) {
+            if (lane == 0) mma_commit(done);
+            __syncwarp();
+            warp_wait(done, 0, nullptr, err, kDrainNs);
+        }
+        if (!ok) *abort = 1;
+    } else if (warp >= 2 && warp < 6) {
+        // epilogue: thread = tile row 32 (warp % 4) + lane (TMEM lane quadrant of the warp)
+        const int row = 32 * (warp & 3) + lane;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const bool storer = warp == 2 && lane == 0;
+        bool ok = true, stored = false;
+        for (int u = u0; u < u1; ++u) {
+            const int i = u - u0;
+            const AbsUnit x = abs_unit(u, mtiles);
+            const int ac = i & 1;
+            uint8_t* stage = smem + L::kOffS + ac * L::kStage;
+            // the store of unit i - 2 has read this staging buffer (at most one store outstanding)
+            if (storer && i >= 2) bulk_wait_group_read1();
+            ok = barrier_and(1, 128, ok);
+            if (!ok) break;
+            ok = warp_wait(&acc_full[ac], (i >> 1) & 1, abort, err, wait_ns);
+            ok = barrier_and(2, 128, ok);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < kAbsN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + (uint32_t)(ac * kAbsN + c * 32), v);
+                tmem_wait_ld();
+                uint8_t* box = stage + (c / 2) * (kBM * 128) + row * 128;  // chunk of 64 columns, this row
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int gidx = (c & 1) * 4 + q;  // 16-byte granule inside the 128-byte row
+                    *reinterpret_cast<uint4*>(box + ((gidx ^ (row & 7)) * 16)) =
+                        make_uint4(pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
+                                   pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                                   pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                                   pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                }
+            }
+            // the accumulator may take unit i + 2
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[ac]);
+            fence_proxy_async_smem();
+            ok = barrier_and(3, 128, ok);
+            if (!ok) break;
+            if (storer) {
+                tma_store_4d(&tm_out, stage, 0, x.mt * kBM, x.nq * (kAbsN / 64), x.h);
+                bulk_commit_group();
+                stored = true;
+            }
+        }
+        if (storer && stored) bulk_wait_group0();
+    } else if (warp == 6 && args.rope_src != nullptr) {
+        // rope columns q[r,h,128:192] -> q_abs[r,h,512:576] of the units with
+        // quarter 0: eight lanes per 128-byte row, eight words per lane in flight
+        for (int u = u0; u < u1; ++u) {
+            const AbsUnit x = abs_unit(u, mtiles);
+            if (x.nq != 0) continue;
+            const int r0 = x.mt * kBM, r1 = min(r0 + kBM, args.R);
+            for (int base = r0 * 8; base < r1 * 8; base += 32 * 8) {
+                uint4 v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int idx = base + j * 32 + lane;  // row * 8 + 16-byte word
+                    if (idx < r1 * 8) {
+                        const int r = idx >> 3, w = idx & 7;
+                        v[j] = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.rope_src) +
+                                                              ((size_t)r * args.H + x.h) * kDQ + kDNope)[w];
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int idx = base + j * 32 + lane;
+                    if (idx < r1 * 8) {
+                        const int r = idx >> 3, w = idx & 7;
+                        reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) +
+                                                 ((size_t)r * args.H + x.h) * args.out_row_elems + kDLatent)[w] = v[j];
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 2 * kAbsN);
+}
+
+cudaError_t launch_absorb(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const CUtensorMap* tm_out,
+                          const GemmArgs& args, long long wait_ns, cudaStream_t stream) {
+    static int sm_count = 0;
+    if (sm_count == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sm_count <= 0)
+            sm_count = 152;
+    }
+    cudaError_t e = cudaFuncSetAttribute(absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AbsSmem::kBytes);
+    if (e != cudaSuccess) return e;
+    const int units = args.H * ((args.R + kBM - 1) / kBM) * kAbsQuarters;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(units < sm_count ? units : sm_count, 1, 1);
+    cfg.blockDim = dim3(kAbsThreads, 1, 1);
+    cfg.dynamicSmemBytes = AbsSmem::kBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, absorb_kernel, *tm_a, *tm_b, *tm_out, args, wait_ns);
+}
+
 }  // namespace
 
 // Reads the projection kernels' error word into *out and clears it, in stream order
@@ -230,7 +516,10 @@ cudaError_t gemm_error_fetch(int* out, cudaStream_t stream) {
 
 cudaError_t launch_head_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const CUtensorMap* tm_out,
                              const GemmArgs& args, long long wait_ns, cudaStream_t stream) {
-    // absorb: K = 128, one stage (two CTAs fit an SM); out-proj: K = 512 through three stages
+    // absorb: K = 128, the persistent kernel over 128-column units; out-proj:
+    // K = 512 through three stages, one CTA per head and row tile
+    if (args.K == 128 && args.N == kAbsN * kAbsQuarters && args.n_cta == kAbsN)
+        return launch_absorb(tm_a, tm_b, tm_out, args, wait_ns, stream);
     if (args.n_cta == 256) return launch_variant<256, 1>(tm_a, tm_b, tm_out, args, wait_ns, stream);
     if (args.n_cta == 128) return launch_variant<128, 3>(tm_a, tm_b, tm_out, args, wait_ns, stream);
     return cudaErrorInvalidValue;
