@@ -5,7 +5,8 @@
 //   out-proj out[r,h,:]       = o_lat[r,h,:] . W_UV[h]    (K = 512, N = 128)
 // ("DeepSeek-V3 MLA deep engineering", sec. 2.2 and sec. 2.4.)
 //
-// One CTA computes a [128 rows x n_cta] tile of one head: rows are the
+// head_gemm_kernel (the out-projection; also usable for any K that is a
+// multiple of 128) - one CTA computes a [128 rows x n_cta] tile of one head: rows are the
 // B * s_q query tokens (TMA zero-fills rows past the end), the accumulator
 // lives in TMEM (n_cta fp32 columns), A (activations, K-major) and B (the
 // head's weight, N-major) stream through a TMA ring of 128-deep K stages in
@@ -16,6 +17,9 @@
 // Warp 0 produces, one thread of warp 1 issues the MMAs, and all four warps
 // run the epilogue: TMEM -> bf16 -> the (now idle) stage buffers in the same
 // swizzled layout -> one TMA tensor store.
+//
+// absorb_kernel (the absorb, K = 128) - further down: a persistent kernel over
+// 128-column units that overlaps one unit's store with the next units' loads.
 #include <cuda_bf16.h>
 
 #include "mla_internal.h"
@@ -520,7 +524,6 @@ cudaError_t launch_head_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b, c
     // K = 512 through three stages, one CTA per head and row tile
     if (args.K == 128 && args.N == kAbsN * kAbsQuarters && args.n_cta == kAbsN)
         return launch_absorb(tm_a, tm_b, tm_out, args, wait_ns, stream);
-    if (args.n_cta == 256) return launch_variant<256, 1>(tm_a, tm_b, tm_out, args, wait_ns, stream);
     if (args.n_cta == 128) return launch_variant<128, 3>(tm_a, tm_b, tm_out, args, wait_ns, stream);
     return cudaErrorInvalidValue;
 }
