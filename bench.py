@@ -3,11 +3,13 @@
 
 A step is one pass of the whole path over one batch (one attention layer):
   mla_absorb_q -> mla_decode_paged (+ split combine) -> mla_out_proj
-on the DeepSeek-V3 decode workload (B = 128 sequences, 128 heads, s_q = 1,
-every cache_seqlen 512, 64-token bf16 pages, d_c 512 + rope 64), seeded
-synthetic inputs (no datasets or trained weights exist here).
+Default workload: multi-token (speculative) decode with a causal mask, the
+largest single-GPU configuration of the path (B = 132 sequences, s_q = 2 query
+tokens each, 128 heads, every cache_seqlen 4096, 64-token bf16 pages, d_c 512 +
+rope 64), on seeded synthetic inputs (no datasets or trained weights exist here).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-workloads]
 
 The split schedule (mla_get_metadata) depends only on cache_seqlens: a model
 computes it once per decoding step and shares it between its layers, so it is
@@ -23,17 +25,17 @@ twice the L2 size, so the KV cache streams from HBM.
 
 The timed region is one CUDA graph of the K steps' C-ABI calls (captured on
 a stream of its own from pre-marshalled arguments after the warm-up steps,
-replayed once untimed), so that the host's launch cost and jitter (the Grace
-cores are shared with the node's other GPUs) stay out of a device-timed
-number; CUDA events bracket the region. The decode kernel's launch duration
-(for the roofline of the dominant kernel) comes from a second graph of the
-same K decode calls alone, bracketed the same way. `--eager` (and
-`--profile`) time the eager calls instead, with events around every decode
-call. `e2e` repeats the step through the same C ABI with the
-step's inputs copied from pinned host buffers and the result copied back
-inside the timed region, the host synchronising on the result every step. `--impl reference` times the CPU
-oracle (the reference implementation of this path) on a bounded sample of the
-same workload.
+replayed once untimed), so that the host's launch cost and jitter stay out of
+a device-timed number; CUDA events bracket the region. The decode call's
+launch duration (the roofline of the dominant kernel) comes from a second
+graph of decode calls alone, bracketed the same way. The `workloads` object
+repeats that decode-only measurement on the other named workloads (DeepSeek-V3
+batch 128 x 512 tokens, variable lengths, long context), each with its own
+rotating input sets, roofline bound and fraction. `e2e` repeats the step
+through the same C ABI with the step's inputs copied from pinned host buffers
+and the result copied back and read by the host every step. `--impl
+reference` times the CPU oracle (the reference implementation of this path)
+on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -52,7 +54,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged MLA decode µs/call, achieved HBM GB/s & TFLOPS vs GB300 roofline"
 UNIT = "us/call"
-WORKLOAD = "dsv3"
+WORKLOAD = "spec"
+DECODE_WORKLOADS = ["dsv3", "varlen", "long"]
 FLOP_PER_PAIR = 2 * (576 + 512)          # score + value MACs per visible (query row, key)
 FLOP_PROJ_PER_ROW = 2 * 128 * 512        # absorb or out-proj MACs per (b, s, h), x2 flops
 
@@ -70,6 +73,8 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--profile", action="store_true", help="short run for a profiler: no clocks, e2e or cpu leg")
     p.add_argument("--eager", action="store_true", help="time eager C-ABI calls instead of replaying a CUDA graph")
+    p.add_argument("--no-workloads", action="store_true", help="skip the decode-only lines of the other workloads")
+    p.add_argument("--decode-calls", type=int, default=400, help="decode calls per workload in `workloads`")
     return p.parse_args()
 
 
@@ -159,11 +164,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def recorded_traffic():
-    """DRAM bytes (read + write) per decode_kernel launch from the committed ncu
-    summary, or None when the kernel source changed since that capture."""
+def recorded_traffic(workload):
+    """DRAM bytes (read + write) per decode_kernel launch on `workload` from the
+    committed ncu summary, or None when there is none or the kernel source
+    changed since that capture."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "decode_traffic_dsv3.txt")
+    path = os.path.join(ROOT, "profiles", f"decode_traffic_{workload}.txt")
     try:
         vals = {}
         with open(path) as f:
@@ -185,77 +191,73 @@ def recorded_traffic():
 # --------------------------------------------------------------- our kernels --
 
 class StepArgs:
-    """Pre-marshalled C-ABI arguments of one step over one resident input set."""
+    """Pre-marshalled C-ABI arguments of one step over one resident input set.
+    Decode-only workloads (q_abs drawn directly) have no absorb or out-proj."""
 
     def __init__(self, api, inp, num_parts, workspace, stream_ptr):
         import torch
         d = inp
         self.inp = d
         B, s_q, H = d.B, d.s_q, d.H
-        self.tm = torch.empty((num_parts, 8), dtype=torch.int32, device=d.kv_cache.device)
-        self.ns = torch.empty((B + 1,), dtype=torch.int32, device=d.kv_cache.device)
-        self.q_abs = torch.empty((B, s_q, H, 576), dtype=torch.bfloat16, device=d.kv_cache.device)
-        self.o_lat = torch.empty((B, s_q, H, 512), dtype=torch.bfloat16, device=d.kv_cache.device)
-        self.lse = torch.empty((B, s_q, H), dtype=torch.float32, device=d.kv_cache.device)
-        self.out = torch.empty((B, s_q, H, 128), dtype=torch.bfloat16, device=d.kv_cache.device)
+        dev = d.kv_cache.device
+        self.tm = torch.empty((num_parts, 8), dtype=torch.int32, device=dev)
+        self.ns = torch.empty((B + 1,), dtype=torch.int32, device=dev)
+        self.q_abs = d.q_abs if d.q is None else torch.empty((B, s_q, H, 576), dtype=torch.bfloat16, device=dev)
+        self.o_lat = torch.empty((B, s_q, H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((B, s_q, H), dtype=torch.float32, device=dev)
+        self.out = torch.empty((B, s_q, H, 128), dtype=torch.bfloat16, device=dev) if d.w_uv is not None else None
         P = ctypes.c_void_p
         st = P(stream_ptr)
         self.meta = (P(d.seqlens.data_ptr()), B, s_q, H, 1, num_parts, P(self.tm.data_ptr()), P(self.ns.data_ptr()), st)
-        self.absorb = (P(d.q.data_ptr()), P(d.w_uk.data_ptr()), P(self.q_abs.data_ptr()), B, s_q, H, st)
+        self.absorb = None if d.q is None else (P(d.q.data_ptr()), P(d.w_uk.data_ptr()), P(self.q_abs.data_ptr()),
+                                                B, s_q, H, st)
         self.decode = (P(self.q_abs.data_ptr()), P(d.kv_cache.data_ptr()), d.kv_cache.shape[0],
                        P(d.block_table.data_ptr()), d.block_table.shape[1], P(d.seqlens.data_ptr()), B, s_q, H,
                        P(self.tm.data_ptr()), P(self.ns.data_ptr()), num_parts, ctypes.c_float(d.scale),
                        int(d.causal), P(self.o_lat.data_ptr()), P(self.lse.data_ptr()), P(workspace.data_ptr()),
                        workspace.numel(), st)
-        self.proj = (P(self.o_lat.data_ptr()), P(d.w_uv.data_ptr()), P(self.out.data_ptr()), B, s_q, H, st)
+        self.proj = None if self.out is None else (P(self.o_lat.data_ptr()), P(d.w_uv.data_ptr()),
+                                                   P(self.out.data_ptr()), B, s_q, H, st)
 
 
 def run_step(L, a: StepArgs, ev=None, meta=False):
     rc = L.mla_get_metadata(*a.meta) if meta else 0
-    rc |= L.mla_absorb_q(*a.absorb)
+    if a.absorb is not None:
+        rc |= L.mla_absorb_q(*a.absorb)
     if ev is not None:
         ev[0].record()
     rc |= L.mla_decode_paged(*a.decode)
     if ev is not None:
         ev[1].record()
-    rc |= L.mla_out_proj(*a.proj)
+    if a.proj is not None:
+        rc |= L.mla_out_proj(*a.proj)
     return rc
 
 
-def make_step_graph(torch, api, L, sets, num_parts, ws, dev, S):
-    """Captures S consecutive steps (absorb, decode + combine, out-proj through
-    the C ABI over the rotating input sets) on a stream of their own, and a
-    second graph of the same S decode calls alone; replays both once untimed.
-    Returns (step graph, decode graph, stream), or None when the capture is
-    refused (the caller then times the eager loop)."""
-    stream = torch.cuda.Stream(dev)
-    n = len(sets)
-    gsteps = [StepArgs(api, s, num_parts, ws, stream.cuda_stream) for s in sets]
+def capture(torch, stream, body):
+    """A CUDA graph of `body()` captured on `stream`, replayed once untimed; None if refused."""
     try:
         with torch.cuda.stream(stream):
-            rc = 0
-            for a in gsteps:
-                rc |= L.mla_get_metadata(*a.meta)
-            for i in range(2 * n):
-                rc |= run_step(L, gsteps[i % n])
-            stream.synchronize()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                for i in range(S):
-                    rc |= run_step(L, gsteps[i % n])
-            # the decode calls (with their combine) alone, for the kernel's launch duration
-            gd = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gd, stream=stream):
-                for i in range(S):
-                    rc |= L.mla_decode_paged(*gsteps[i % n].decode)
+                rc = body()
             g.replay()
-            gd.replay()
             stream.synchronize()
-        if rc != 0 or api.mla_read_device_error(ws) != 0:
-            return None
-        return g, gd, stream
+        return g if rc == 0 else None
     except Exception:
         return None
+
+
+def time_graph(torch, g, stream, reps=1):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps  # ms
 
 
 def workload_flops(inp):
@@ -267,6 +269,95 @@ def workload_flops(inp):
     attn = pairs * FLOP_PER_PAIR
     proj = 2 * inp.B * inp.s_q * inp.H * FLOP_PROJ_PER_ROW
     return attn, proj
+
+
+def roofline_of(inp, dec_ms, peaks):
+    """Roofline of one decode call on `inp` lasting dec_ms: the binding bound is
+    the slower of the latent-cache bytes at the measured HBM copy rate and the
+    attention FLOPs at the measured dense bf16 rate (burst: the call is timed
+    alone); the fraction against the sustained bf16 rate is reported beside it."""
+    hbm_peak, tc_peak, tc_sustained, peak_src = peaks
+    kv_bytes = inp.kv_bytes()
+    attn_flops, _ = workload_flops(inp)
+    gbs = kv_bytes / (dec_ms * 1e-3) / 1e9
+    tflops = attn_flops / (dec_ms * 1e-3) / 1e12
+    t_mem = kv_bytes / (hbm_peak * 1e9)
+    t_tc = attn_flops / (tc_peak * 1e12)
+    if t_mem >= t_tc:
+        r = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4)}
+    else:
+        r = {"bound": "tensor", "achieved": round(tflops, 1), "peak": tc_peak, "unit": "TFLOP/s",
+             "frac": round(tflops / tc_peak, 4)}
+    r.update({"algorithmic_bytes_per_launch": kv_bytes, "algorithmic_flops_per_launch": attn_flops,
+              "avg_launch_us": round(dec_ms * 1e3, 3), "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm_peak, 4),
+              "tensor_tflops": round(tflops, 1), "tensor_frac_of_burst": round(tflops / tc_peak, 4),
+              "tensor_frac_of_sustained": round(tflops / tc_sustained, 4),
+              "binding_roofline_us": round(max(t_mem, t_tc) * 1e6, 3), "peak_source": peak_src})
+    return r
+
+
+def input_sets(gen, name, rank, dev, l2, n_sets=0):
+    """Resident input sets of `name`, enough that the bytes between two uses of
+    a set exceed twice the L2 size."""
+    probe = gen.make_workload(name, rep=1000 * rank)
+    per_set = probe.kv_bytes() + sum(t.numel() * t.element_size() for t in (probe.q, probe.q_abs, probe.w_uk,
+                                                                          probe.w_uv) if t is not None)
+    n = n_sets if n_sets > 0 else max(2, math.ceil(2.0 * l2 / per_set) + 1)
+    sets = [probe.to(dev)] + [gen.make_workload(name, rep=1000 * rank + i).to(dev) for i in range(1, n)]
+    return sets, per_set
+
+
+def decode_only(torch, api, L, gen, name, rank, dev, l2, peaks, calls):
+    """Decode-call duration on workload `name` (graph of `calls` decode calls
+    over rotating input sets; the absorbed query of end-to-end workloads is
+    made once per set beforehand) and its roofline."""
+    sets, per_set = input_sets(gen, name, rank, dev, l2)
+    B, s_q, H = sets[0].B, sets[0].s_q, sets[0].H
+    num_parts = api.mla_default_num_parts(dev.index, s_q)
+    ws = api.make_workspace(B, s_q, H, num_parts, dev)
+    stream = torch.cuda.Stream(dev)
+    steps = [StepArgs(api, s, num_parts, ws, stream.cuda_stream) for s in sets]
+    rc = 0
+    with torch.cuda.stream(stream):
+        for a in steps:
+            rc |= L.mla_get_metadata(*a.meta)
+            if a.absorb is not None:
+                rc |= L.mla_absorb_q(*a.absorb)
+        for i in range(3 * len(steps)):
+            rc |= L.mla_decode_paged(*steps[i % len(steps)].decode)
+        stream.synchronize()
+    if rc != 0 or api.mla_read_device_error(ws) != 0:
+        raise RuntimeError(f"decode failed on {name}")
+
+    def body():
+        r = 0
+        for i in range(calls):
+            r |= L.mla_decode_paged(*steps[i % len(steps)].decode)
+        return r
+    g = capture(torch, stream, body)
+    if g is None:
+        raise RuntimeError(f"graph capture failed on {name}")
+    ms = time_graph(torch, g, stream) / calls
+    st = api.mla_read_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error on {name}: {api.status_string(st)}")
+    r = roofline_of(sets[0], ms, peaks)
+    r.update({"workload": describe(sets[0]), "num_parts": num_parts, "calls": calls,
+              "l2": f"rotate {len(sets)} input sets, {len(sets) * per_set / 1e6:.0f} MB > 2 x L2",
+              "traffic": recorded_traffic(name)})
+    del g, steps, sets, ws
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return r
+
+
+def describe(inp):
+    sl = inp.seqlens
+    lens = f"seqlen {int(sl[0])}" if bool((sl == sl[0]).all()) else f"seqlens {int(sl.min())}..{int(sl.max())}"
+    mode = "end to end (absorb, decode, out-proj)" if inp.q is not None else "decode only (q_abs drawn)"
+    causal = ", causal" if inp.causal and inp.s_q > 1 else ""
+    return (f"{inp.name}: B={inp.B} s_q={inp.s_q} H={inp.H} {lens}{causal}, d_c 512 + rope 64, 64-token bf16 "
+            f"pages, {mode}")
 
 
 def run_ours(args, world, rank, local):
@@ -282,18 +373,16 @@ def run_ours(args, world, rank, local):
     L = api.lib()
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20)
-    hbm_peak, tc_peak, tc_sustained, peak_src = measured_peaks()
+    peaks = measured_peaks()
 
-    probe = gen.make_workload(args.workload, rep=1000 * rank)
-    per_set = probe.kv_bytes() + probe.q.numel() * 2 + probe.w_uk.numel() * 2 + probe.w_uv.numel() * 2
-    n_sets = args.sets if args.sets > 0 else max(2, math.ceil(2.0 * l2 / per_set) + 1)
-    sets = [probe.to(dev)] + [gen.make_workload(args.workload, rep=1000 * rank + i).to(dev) for i in range(1, n_sets)]
-    del probe
+    sets, per_set = input_sets(gen, args.workload, rank, dev, l2, args.sets)
+    n_sets = len(sets)
     B, s_q, H = sets[0].B, sets[0].s_q, sets[0].H
     num_parts = api.mla_default_num_parts(local, s_q)
     ws = api.make_workspace(B, s_q, H, num_parts, dev)
     stream = torch.cuda.current_stream(dev)
     steps = [StepArgs(api, s, num_parts, ws, stream.cuda_stream) for s in sets]
+    launches_per_step = sum(x is not None for x in (steps[0].absorb, steps[0].proj)) + 2  # + decode, combine
 
     # the schedule of each input set (fixed lengths), then warm-up and a
     # correctness gate: the device error word must be clear
@@ -324,12 +413,24 @@ def run_ours(args, world, rank, local):
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     use_graph = not (args.profile or args.eager) and K <= 8192
-    graph = make_step_graph(torch, api, L, sets, num_parts, ws, dev, K) if use_graph else None
-    if graph is not None:
+    g = gd = None
+    if use_graph:
+        gstream = torch.cuda.Stream(dev)
+        gsteps = [StepArgs(api, s, num_parts, ws, gstream.cuda_stream) for s in sets]
+        with torch.cuda.stream(gstream):
+            for a in gsteps:
+                L.mla_get_metadata(*a.meta)
+            for i in range(2 * n_sets):
+                run_step(L, gsteps[i % n_sets])
+            gstream.synchronize()
+        g = capture(torch, gstream, lambda: sum(run_step(L, gsteps[i % n_sets]) for i in range(K)))
+        gd = capture(torch, gstream, lambda: sum(L.mla_decode_paged(*gsteps[i % n_sets].decode) for i in range(K)))
+        if g is None or gd is None or api.mla_read_device_error(ws) != 0:
+            g = gd = None
+    if g is not None:
         # The K steps (absorb, decode + combine, out-proj over the rotating input
         # sets) as one CUDA graph, replayed once untimed and once timed: the
         # host's launch cost and jitter stay out of the device timing.
-        g, gd, gstream = graph
         clocks.start()
         time.sleep(0.3)
         barrier(world)
@@ -341,14 +442,8 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         barrier(world)
         clk = clocks.stop()
-        # the decode kernel's launch duration: the K decode calls alone, replayed
-        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(gstream):
-            d0.record()
-            gd.replay()
-            d1.record()
-        torch.cuda.synchronize()
-        dec_ms = [d0.elapsed_time(d1) / K]
+        # the decode call's launch duration: the K decode calls alone, replayed
+        dec_ms = [time_graph(torch, gd, gstream) / K]
         timed = ("one CUDA graph of the K steps' C-ABI calls, replayed, CUDA events around it; the decode "
                  "launch duration from a graph of the K decode calls alone")
     else:
@@ -376,147 +471,144 @@ def run_ours(args, world, rank, local):
     total_ms = t_start.elapsed_time(t_end)
     ms_step = max_over_ranks(total_ms / K, world, dev)
     dec_avg_ms = statistics.mean(dec_ms)
-    dec_med_ms = statistics.median(dec_ms) if len(dec_ms) > 1 else None
 
-    kv_bytes = sets[0].kv_bytes()
     attn_flops, proj_flops = workload_flops(sets[0])
-    achieved_gbs = kv_bytes / (dec_avg_ms * 1e-3) / 1e9
-    achieved_tflops = attn_flops / (dec_avg_ms * 1e-3) / 1e12
-    t_roof_ms = max(kv_bytes / (hbm_peak * 1e9), attn_flops / (tc_sustained * 1e12)) * 1e3
-    bound = "hbm" if kv_bytes / (hbm_peak * 1e9) >= attn_flops / (tc_sustained * 1e12) else "tensor"
-    if bound == "hbm":
-        roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(achieved_gbs / hbm_peak, 4)}
-    else:
-        roof = {"bound": "tensor", "achieved": round(achieved_tflops, 1), "peak": tc_sustained, "unit": "TFLOP/s",
-                "frac": round(achieved_tflops / tc_sustained, 4)}
-    roof.update({"traffic": recorded_traffic(), "kernel": "mla_decode_paged (decode + combine launches)",
-                 "algorithmic_bytes_per_launch": kv_bytes, "algorithmic_flops_per_launch": attn_flops,
-                 "avg_launch_us": round(dec_avg_ms * 1e3, 3),
-                 "median_launch_us": None if dec_med_ms is None else round(dec_med_ms * 1e3, 3),
-                 "binding_roofline_frac": round(t_roof_ms / dec_avg_ms, 4),
-                 "tensor_tflops": round(achieved_tflops, 1), "tensor_frac_of_sustained": round(achieved_tflops / tc_sustained, 4),
-                 "peak_source": peak_src})
+    roof = roofline_of(sets[0], dec_avg_ms, peaks)
+    roof.update({"traffic": recorded_traffic(args.workload), "kernel": "mla_decode_paged (decode + combine launches)"})
+    if len(dec_ms) > 1:
+        roof["median_launch_us"] = round(statistics.median(dec_ms) * 1e3, 3)
 
     result = {
         "metric": METRIC, "value": round(ms_step * 1e3, 3), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 activations and cache, "
         "N(0,1/512) weights, randomly permuted pages)",
-        "config": {"workload": f"{args.workload}: DeepSeek-V3 decode B={B} H={H} s_q={s_q} seqlen "
-                   f"{int(sets[0].seqlens[0])}, d_c 512 + rope 64, 64-token bf16 pages",
-                   "global_batch": B * world, "seq_len": int(sets[0].seqlens.max()),
+        "config": {"workload": describe(sets[0]), "global_batch": B * world, "seq_len": int(sets[0].seqlens.max()),
                    "parallelism": f"replicas x{world} (sequences shard, no collective)",
                    "l2": f"rotate {n_sets} resident input sets, {n_sets * per_set / 1e6:.0f} MB > 2 x L2 "
                          f"({l2 / 1e6:.0f} MB)",
                    "num_parts": num_parts, "timed": timed},
         "roofline": roof,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")} | {"samples": clk.get("samples", 0)},
-        "gpu_launches": 4 * K,
+        "gpu_launches": launches_per_step * K,
         "metadata_us": None if meta_us is None else round(meta_us, 2),
         "throughput": {"decode_steps_per_s": round(world * 1e3 / ms_step, 1),
                        "tokens_per_s": round(world * B * s_q * 1e3 / ms_step, 1),
                        "step_tflops": round((attn_flops + proj_flops) / (ms_step * 1e-3) / 1e12, 2)},
     }
-
     if not args.no_e2e and not args.profile:
         result["e2e"] = run_e2e(args, api, L, sets, num_parts, ws, dev, world)
+    del g, gd
+    if not args.no_workloads and not args.profile:
+        del steps, sets
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        wl = {args.workload: {k: roof[k] for k in ("bound", "frac", "avg_launch_us", "hbm_frac",
+                                                   "tensor_frac_of_burst", "algorithmic_bytes_per_launch",
+                                                   "algorithmic_flops_per_launch", "binding_roofline_us")}}
+        for name in DECODE_WORKLOADS:
+            if name != args.workload:
+                wl[name] = decode_only(torch, api, L, gen, name, rank, dev, l2, peaks, args.decode_calls)
+        result["workloads"] = wl
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
         result["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0)
     return result
 
 
 def run_e2e(args, api, L, sets, num_parts, ws, dev, world):
-    """Same step through the C ABI with the step's inputs in pinned host memory:
-    H2D of q, cache_seqlens and block_table, the four calls, D2H of out and lse,
-    and a stream synchronisation so the host holds the result, every step. The
-    calls go to a stream of their own; the reported value replays a CUDA graph
-    of exactly these calls (captured once per input set), as a serving loop
-    would, and the eager loop's time is reported beside it."""
+    """The step through the C ABI with the step's inputs in pinned host memory,
+    pipelined as a serving loop would run it: step i's queries, lengths and
+    page table go up on a copy stream while step i - 1 computes; the four calls
+    (schedule included) run on a compute stream; the projected output and lse
+    come back on a third stream, and the host waits for step i - 1's result
+    (reads it) before it enqueues step i + 1. Every step's copies and the
+    host's read of every result are inside the timed region."""
     import torch
-    stream = torch.cuda.Stream(dev)
-    steps = [StepArgs(api, s, num_parts, ws, stream.cuda_stream) for s in sets]
+    n = len(sets)
+    s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    steps = [StepArgs(api, s, num_parts, ws, s_comp.cuda_stream) for s in sets]
     host = []
     for s, a in zip(sets, steps):
+        res = a.out if a.out is not None else a.o_lat
         host.append({
-            "q": s.q.cpu().pin_memory(), "seqlens": s.seqlens.cpu().pin_memory(),
-            "table": s.block_table.cpu().pin_memory(),
-            "out": torch.empty(a.out.shape, dtype=a.out.dtype).pin_memory(),
+            "q": (s.q if s.q is not None else s.q_abs).cpu().pin_memory(),
+            "seqlens": s.seqlens.cpu().pin_memory(), "table": s.block_table.cpu().pin_memory(),
+            "out": torch.empty(res.shape, dtype=res.dtype).pin_memory(),
             "lse": torch.empty(a.lse.shape, dtype=a.lse.dtype).pin_memory(),
         })
     h2d = host[0]["q"].numel() * 2 + host[0]["seqlens"].numel() * 4 + host[0]["table"].numel() * 4
     d2h = host[0]["out"].numel() * 2 + host[0]["lse"].numel() * 4
-    n = len(sets)
+    K = args.e2e_steps
+    ev_in = [torch.cuda.Event() for _ in range(n)]
+    ev_comp = [torch.cuda.Event() for _ in range(n)]
+    ev_out = [torch.cuda.Event() for _ in range(n)]
+    started = [False] * n
 
     def enqueue(i):
-        s, a, h = sets[i % n], steps[i % n], host[i % n]
-        s.q.copy_(h["q"], non_blocking=True)
-        s.seqlens.copy_(h["seqlens"], non_blocking=True)
-        s.block_table.copy_(h["table"], non_blocking=True)
+        j = i % n
+        s, a, h = sets[j], steps[j], host[j]
+        dst_q = s.q if s.q is not None else s.q_abs
+        res = a.out if a.out is not None else a.o_lat
+        with torch.cuda.stream(s_in):
+            if started[j]:
+                s_in.wait_event(ev_comp[j])  # set j's previous step has consumed its inputs
+            dst_q.copy_(h["q"], non_blocking=True)
+            s.seqlens.copy_(h["seqlens"], non_blocking=True)
+            s.block_table.copy_(h["table"], non_blocking=True)
+            ev_in[j].record(s_in)
+        s_comp.wait_event(ev_in[j])
+        if started[j]:
+            s_comp.wait_event(ev_out[j])  # set j's previous result has left the device
         rc = run_step(L, a, meta=True)
-        h["out"].copy_(a.out, non_blocking=True)
-        h["lse"].copy_(a.lse, non_blocking=True)
+        ev_comp[j].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[j])
+            h["out"].copy_(res, non_blocking=True)
+            h["lse"].copy_(a.lse, non_blocking=True)
+            ev_out[j].record(s_out)
+        started[j] = True
         return rc
 
-    K = args.e2e_steps
-    rc = 0
-    with torch.cuda.stream(stream):
-        for i in range(5):
+    def loop(count):
+        rc = 0
+        for i in range(count):
             rc |= enqueue(i)
-            stream.synchronize()
-        barrier(world)
-        t0 = time.perf_counter()
-        for i in range(K):
-            rc |= enqueue(i)
-            stream.synchronize()
-        t1 = time.perf_counter()
-        barrier(world)
-        eager_us = max_over_ranks((t1 - t0) / K * 1e6, world, dev)
-        graphs, why = [], None
-        try:
-            for i in range(n):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    rc |= enqueue(i)
-                graphs.append(g)
-        except Exception as ex:  # capture refused: report the eager loop
-            graphs, why = [], f"{type(ex).__name__}: {ex}"[:200]
-        us, mode = eager_us, "eager C-ABI calls"
-        if graphs:
-            for i in range(5):
-                graphs[i % n].replay()
-                stream.synchronize()
-            barrier(world)
-            t0 = time.perf_counter()
-            for i in range(K):
-                graphs[i % n].replay()
-                stream.synchronize()
-            t1 = time.perf_counter()
-            barrier(world)
-            us = max_over_ranks((t1 - t0) / K * 1e6, world, dev)
-            mode = "CUDA graph of the C-ABI calls and copies, one per input set, replayed"
+            if i >= 1:
+                ev_out[(i - 1) % n].synchronize()
+                _ = float(host[(i - 1) % n]["lse"][0, 0, 0])  # the host reads the result
+        ev_out[(count - 1) % n].synchronize()
+        _ = float(host[(count - 1) % n]["lse"][0, 0, 0])
+        return rc
+
+    rc = loop(5)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    rc |= loop(K)
+    t1 = time.perf_counter()
+    barrier(world)
     if rc != 0:
         raise RuntimeError("C-ABI error in the e2e loop")
-    out = {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-           "mode": mode, "eager_value": round(eager_us, 3),
-           "steps": K, "note": "KV cache and weights stay resident (model state); per step the queries, "
-                                "lengths and page table go up and the projected output and lse come back"}
-    if why:
-        out["graph_error"] = why
-    return out
+    us = max_over_ranks((t1 - t0) / K * 1e6, world, dev)
+    return {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "mode": "eager C-ABI calls; H2D, compute and D2H on three streams, two steps in flight, the host "
+                    "reads every step's result", "steps": K,
+            "note": "KV cache and weights stay resident (model state); per step the queries, lengths and page "
+                    "table go up and the projected output and lse come back"}
 
 
 # ------------------------------------------------------------ oracle timing --
 
 def oracle_step(inp, batches):
-    """The oracle's full chain (absorb -> attend -> out-proj) on the listed sequences."""
+    """The oracle's chain on the listed sequences: absorb -> attend -> out-proj
+    (or attend alone for a workload whose absorbed query is drawn directly)."""
     import oracle
     from mla_paged_kv_absorbed_gb300 import inputs as gen
     sub = gen.sample_batches(inp, batches)
     f = lambda t: t.float().numpy()
-    qa = oracle.absorb_q(f(sub.q), f(sub.w_uk))
+    qa = f(sub.q_abs) if sub.q is None else oracle.absorb_q(f(sub.q), f(sub.w_uk))
     o, lse = oracle.attend_absorbed(qa, f(sub.kv_cache), sub.block_table, sub.seqlens, sub.scale, sub.causal)
-    return oracle.out_proj(o, f(sub.w_uv))
+    return o if sub.w_uv is None else oracle.out_proj(o, f(sub.w_uv))
 
 
 def cpu_baseline(workload, budget_s=12.0):
@@ -536,8 +628,8 @@ def cpu_baseline(workload, budget_s=12.0):
     oracle_step(inp, batches)
     dt = time.perf_counter() - t0
     return {"value": round(dt / n * inp.B * 1e6, 1), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n} of {inp.B} sequences of the {workload} workload, full chain (absorb, attend, "
-                      f"out-proj) in fp64; {dt:.1f} s scaled by {inp.B}/{n}"}
+            "sample": f"{n} of {inp.B} sequences of the {workload} workload, the whole chain of the step in "
+                      f"fp64; {dt:.1f} s scaled by {inp.B}/{n}"}
 
 
 def run_reference(args, world, rank):
@@ -564,11 +656,12 @@ def run_reference(args, world, rank):
         oracle_step(inp, batches)
         times.append(time.perf_counter() - t0)
     us = statistics.mean(times) / n * inp.B * 1e6
-    sample = f"{n} of {inp.B} sequences per step, full chain in fp64, scaled by {inp.B}/{n}"
+    sample = f"{n} of {inp.B} sequences per step, the whole chain of the step in fp64, scaled by {inp.B}/{n}"
     return {"metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": f"{args.workload}: DeepSeek-V3 decode B={inp.B} H={inp.H} s_q={inp.s_q}"},
+            "config": {"workload": describe(inp), "global_batch": inp.B * world,
+                       "seq_len": int(inp.seqlens.max()), "parallelism": "oracle on the host cores (rank 0)"},
             "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "kind": "oracle", "cores": oracle.num_threads(),
                              "sample": sample},
             "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -142,7 +142,8 @@ int mla_get_metadata(const int32_t* cache_seqlens, int B, int s_q, int H, int h_
  * q_abs[b,s,h,512+i]  = q[b,s,h,128+i]                          (i < 64)
  * q: bf16 [B, s_q, H, 192] = [q_nope 128 | q_rope 64];  w_uk: bf16 [H, 128, 512];
  * q_abs (out): bf16 [B, s_q, H, 576]. fp32 accumulation, bf16 round-to-nearest-even.
- * Runs as a batched tcgen05 GEMM, one (head, 128-row tile, 256-column half) per CTA.
+ * Runs as a persistent tcgen05 GEMM: one CTA per SM walks a contiguous range of
+ * (head, 128-row tile, 128-column quarter) units; the 64 rope columns are copied.
  */
 int mla_absorb_q(const mla_bf16_t* q, const mla_bf16_t* w_uk, mla_bf16_t* q_abs, int B, int s_q, int H,
                  mla_stream_t stream);
@@ -230,11 +231,15 @@ void mla_set_wait_limit_ns(long long ns);
  * receives, in stream order after the kernels, the device status of this call
  * (MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_BAD_BLOCK); the scratch error word is
  * cleared at the start of every call.
- * The first call on a device looks up the scratch array's device address
- * (cudaGetSymbolAddress, with that device current), so make that first call
- * before any stream capture. All calls share the one array and it keeps the
- * last call's contents: calls that overlap on the GPU (on unordered streams)
- * race on it and must be serialised by the caller.
+ * Every call looks up the scratch array's device address on the current
+ * device (cudaGetSymbolAddress: a lookup, no allocation). Under lazy module
+ * loading (the CUDA default) the first call on a device loads the library's
+ * device code, and that is when the array is reserved on that device; make
+ * that first call before any stream capture. All calls share the one array
+ * and it keeps the last call's contents (each call clears the error word it
+ * needs at zero; every partial is written before it is read): calls that
+ * overlap on the GPU (on unordered streams) race on it and must be serialised
+ * by the caller.
  */
 #define MLA_NOALLOC_MAX_ROWS 32768
 #define MLA_NOALLOC_SCRATCH_BYTES (256 + MLA_NOALLOC_MAX_ROWS * (4 + 4 * MLA_D_LATENT))
@@ -250,7 +255,9 @@ int mla_decode_paged_noalloc(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache
  * ------------------------------------------------------------------------- */
 
 /*
- * Paged gather through TMA, the same way mla_decode_paged loads pages:
+ * Paged gather through TMA with mla_decode_paged's own page load: one
+ * whole-page box through the same tensor map (3-D [dims, keys, chunk] view,
+ * 128-byte swizzle), then un-swizzled to HBM:
  * out[b, t, :] = kv(b, t)[0:576] for t < min(seqlen_b, max_tokens); other rows
  * of out are left untouched. out: bf16 [B, max_tokens, 576]. Bit-exact copy.
  */

@@ -182,15 +182,16 @@ def mla_absorb_q(q: torch.Tensor, w_uk: torch.Tensor, q_abs: Optional[torch.Tens
     if q_abs is None:
         q_abs = torch.empty((B, s_q, H, D_QK), dtype=torch.bfloat16, device=q.device)
     _need(q_abs, "q_abs", torch.bfloat16, 4)
+    if tuple(q_abs.shape) != (B, s_q, H, D_QK):
+        raise ValueError(f"q_abs must be [{B}, {s_q}, {H}, 576]")
     _check("mla_absorb_q", lib().mla_absorb_q(_p(q), _p(w_uk), _p(q_abs), B, s_q, H, _stream(stream)))
     return q_abs
 
 
-def mla_decode_paged(q_abs: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
-                     cache_seqlens: torch.Tensor, tile_meta: torch.Tensor, num_splits: torch.Tensor,
-                     softmax_scale: float, causal: bool = True, o_lat: Optional[torch.Tensor] = None,
-                     lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+def _check_decode_inputs(q_abs, kv_cache, block_table, cache_seqlens, tile_meta, num_splits):
+    """dtype, device, contiguity and shape checks shared by both decode entry
+    points (the C ABI sees only pointers, so a shape mismatch would make the
+    kernels read or write out of bounds). Returns (B, s_q, H)."""
     _need(q_abs, "q_abs", torch.bfloat16, 4)
     _need(kv_cache, "kv_cache", torch.bfloat16, 3)
     _need(block_table, "block_table", torch.int32, 2)
@@ -198,10 +199,28 @@ def mla_decode_paged(q_abs: torch.Tensor, kv_cache: torch.Tensor, block_table: t
     _need(tile_meta, "tile_meta", torch.int32, 2)
     _need(num_splits, "num_splits", torch.int32, 1)
     B, s_q, H, d = q_abs.shape
-    if d != D_QK or kv_cache.shape[1:] != (PAGE, D_QK):
+    if d != D_QK or tuple(kv_cache.shape[1:]) != (PAGE, D_QK):
         raise ValueError("q_abs must be [B, s_q, H, 576] and kv_cache [num_blocks, 64, 576]")
     if block_table.shape[0] != B or cache_seqlens.shape[0] != B or num_splits.shape[0] != B + 1:
         raise ValueError("block_table, cache_seqlens and num_splits must match the batch of q_abs")
+    if tile_meta.shape[1] != 8:
+        raise ValueError("tile_meta must be [num_parts, 8]")
+    return B, s_q, H
+
+
+def _check_decode_outputs(o_lat, lse, B, s_q, H):
+    _need(o_lat, "o_lat", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    if tuple(o_lat.shape) != (B, s_q, H, D_LATENT) or tuple(lse.shape) != (B, s_q, H):
+        raise ValueError(f"o_lat must be [{B}, {s_q}, {H}, 512] and lse [{B}, {s_q}, {H}]")
+
+
+def mla_decode_paged(q_abs: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                     cache_seqlens: torch.Tensor, tile_meta: torch.Tensor, num_splits: torch.Tensor,
+                     softmax_scale: float, causal: bool = True, o_lat: Optional[torch.Tensor] = None,
+                     lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    B, s_q, H = _check_decode_inputs(q_abs, kv_cache, block_table, cache_seqlens, tile_meta, num_splits)
     num_parts = tile_meta.shape[0]
     if o_lat is None:
         o_lat = torch.empty((B, s_q, H, D_LATENT), dtype=torch.bfloat16, device=q_abs.device)
@@ -209,8 +228,7 @@ def mla_decode_paged(q_abs: torch.Tensor, kv_cache: torch.Tensor, block_table: t
         lse = torch.empty((B, s_q, H), dtype=torch.float32, device=q_abs.device)
     if workspace is None:
         workspace = make_workspace(B, s_q, H, num_parts, q_abs.device)
-    _need(o_lat, "o_lat", torch.bfloat16, 4)
-    _need(lse, "lse", torch.float32, 3)
+    _check_decode_outputs(o_lat, lse, B, s_q, H)
     _need(workspace, "workspace", torch.uint8, 1)
     _check("mla_decode_paged", lib().mla_decode_paged(
         _p(q_abs), _p(kv_cache), kv_cache.shape[0], _p(block_table), block_table.shape[1], _p(cache_seqlens),
@@ -229,6 +247,8 @@ def mla_out_proj(o_lat: torch.Tensor, w_uv: torch.Tensor, out: Optional[torch.Te
     if out is None:
         out = torch.empty((B, s_q, H, D_V), dtype=torch.bfloat16, device=o_lat.device)
     _need(out, "out", torch.bfloat16, 4)
+    if tuple(out.shape) != (B, s_q, H, D_V):
+        raise ValueError(f"out must be [{B}, {s_q}, {H}, 128]")
     _check("mla_out_proj", lib().mla_out_proj(_p(o_lat), _p(w_uv), _p(out), B, s_q, H, _stream(stream)))
     return out
 
@@ -299,14 +319,10 @@ def mla_decode_paged_noalloc(q_abs: torch.Tensor, kv_cache: torch.Tensor, block_
         P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         fn.argtypes = [P, P, I, P, I, P, I, I, I, P, P, I, F, I, P, P, P, P]
         fn.restype = I
-    for t, name, dt in ((q_abs, "q_abs", torch.bfloat16), (kv_cache, "kv_cache", torch.bfloat16),
-                        (block_table, "block_table", torch.int32), (cache_seqlens, "cache_seqlens", torch.int32),
-                        (tile_meta, "tile_meta", torch.int32), (num_splits, "num_splits", torch.int32),
-                        (o_lat, "o_lat", torch.bfloat16), (lse, "lse", torch.float32)):
-        _need(t, name, dt)
+    B, s_q, H = _check_decode_inputs(q_abs, kv_cache, block_table, cache_seqlens, tile_meta, num_splits)
+    _check_decode_outputs(o_lat, lse, B, s_q, H)
     if device_status is not None:
         _need(device_status, "device_status", torch.int32)
-    B, s_q, H, _ = q_abs.shape
     _check("mla_decode_paged_noalloc", fn(
         _p(q_abs), _p(kv_cache), kv_cache.shape[0], _p(block_table), block_table.shape[1], _p(cache_seqlens),
         B, s_q, H, _p(tile_meta), _p(num_splits), tile_meta.shape[0], float(softmax_scale), int(bool(causal)),

@@ -53,6 +53,17 @@ bool make_tmap(CUtensorMap* map, const void* base, int rank, const uint64_t* dim
     return r == CUDA_SUCCESS;
 }
 
+// The cache as a 3-D view {64 dims, num_blocks * 64 keys, 9 chunks} with
+// strides {1152, 128} bytes, so that one box {64, 64, chunks} is a whole page
+// (chunks = 9) or its 512 value columns (chunks = 8), landing in shared memory
+// as [chunk][key][64 dims]. Used by the decode kernel and its gather test hook.
+bool make_kv_page_map(CUtensorMap* map, const void* kv_cache, int num_blocks, int chunks) {
+    const uint64_t dims[3] = {64, (uint64_t)num_blocks * kPage, (uint64_t)kDQK / 64};
+    const uint64_t strides[2] = {(uint64_t)kDQK * 2, 128};
+    const uint32_t box[3] = {64, (uint32_t)kPage, (uint32_t)chunks};
+    return make_tmap(map, kv_cache, 3, dims, strides, box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+}
+
 struct DeviceInfo {
     int sm_count = 0, major = 0, minor = 0, max_clusters = -1;
 };
@@ -75,6 +86,16 @@ bool device_info(DeviceInfo& info) {
     info = cache[dev];
     return true;
 }
+
+}  // namespace
+
+// SM count of the current device (cached per device ordinal), 0 on failure.
+int device_sm_count() {
+    DeviceInfo d;
+    return device_info(d) ? d.sm_count : 0;
+}
+
+namespace {
 
 int check_device() {
     DeviceInfo d;
@@ -221,14 +242,8 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     DecodeMaps maps;
     // [dims, keys, chunk] views: one box per page (or per 64 query rows)
-    const uint64_t kv_dims[3] = {64, (uint64_t)num_blocks * kPage, (uint64_t)kDQK / 64};
-    const uint64_t kv_strides[2] = {(uint64_t)kDQK * 2, 128};
-    const uint32_t kv_box[3] = {64, (uint32_t)kPage, (uint32_t)kDQK / 64};
-    if (!make_tmap(&maps.kv, kv_cache, 3, kv_dims, kv_strides, kv_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
-        return MLA_ERR_CUDA;
-    const uint32_t v_box[3] = {64, (uint32_t)kPage, (uint32_t)kDLatent / 64};
-    if (!make_tmap(&maps.v, kv_cache, 3, kv_dims, kv_strides, v_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
-        return MLA_ERR_CUDA;
+    if (!make_kv_page_map(&maps.kv, kv_cache, num_blocks, kDQK / 64)) return MLA_ERR_CUDA;
+    if (!make_kv_page_map(&maps.v, kv_cache, num_blocks, kDLatent / 64)) return MLA_ERR_CUDA;
     const uint64_t rows = (uint64_t)B * s_q;
     const uint64_t qrows_total = rows * (uint64_t)H;
     const uint32_t qrows = (uint32_t)(qrows_total < 64 ? qrows_total : 64);
@@ -299,10 +314,7 @@ int mla_debug_gather(const mla_bf16_t* kv_cache, int num_blocks, const int32_t* 
     int dev = check_device();
     if (dev != MLA_OK) return dev;
     CUtensorMap tm_kv;
-    const uint64_t kv_dims[2] = {(uint64_t)kDQK, (uint64_t)num_blocks * kPage};
-    const uint64_t kv_strides[1] = {(uint64_t)kDQK * 2};
-    const uint32_t kv_box[2] = {64, (uint32_t)kPage};
-    if (!make_tmap(&tm_kv, kv_cache, 2, kv_dims, kv_strides, kv_box)) return MLA_ERR_CUDA;
+    if (!make_kv_page_map(&tm_kv, kv_cache, num_blocks, kDQK / 64)) return MLA_ERR_CUDA;
     return cuda_status(launch_debug_gather(&tm_kv, block_table, max_blocks_per_seq, cache_seqlens, B, max_tokens,
                                            num_blocks, out, static_cast<cudaStream_t>(stream)));
 }

@@ -137,13 +137,8 @@ cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, con
     cudaLaunchConfig_t cfg = {};
     const int rows = B * s_q * H;
     const int units = (rows + kRowsPerCta - 1) / kRowsPerCta;
-    static int sm_count = 0;
-    if (sm_count == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sm_count <= 0)
-            sm_count = 152;
-    }
+    const int sm_count = device_sm_count();
+    if (sm_count <= 0) return cudaErrorInvalidDevice;
     // at most two CTAs per SM: enough rows in flight for a few long sequences
     // whose pieces cover the whole part list
     cfg.gridDim = dim3(units < 1 ? 1 : (units < 2 * sm_count ? units : 2 * sm_count), 1, 1);

@@ -1,6 +1,8 @@
 // debug.cu - test hooks exposing single building blocks of the decode path:
-//  * a paged gather that loads pages with the same TMA tensor map, box and
-//    128-byte swizzle as the decode kernel, then un-swizzles them to HBM;
+//  * a paged gather that loads each page as one whole-page TMA box through the
+//    decode kernel's own tensor map (the 3-D [dims, keys, chunk] view of the
+//    cache, 128-byte swizzle, built by the same host helper), then un-swizzles
+//    the page to HBM;
 //  * a one-tile tcgen05 product D[128 x N] = A[128 x K] . B with the same
 //    shared-memory layouts and descriptors as the decode kernel (K-major B
 //    like the key tile, MN-major B like the value tile); A is read from
@@ -38,8 +40,9 @@ __global__ void __launch_bounds__(kGatherThreads)
     }
     __syncthreads();
     if (threadIdx.x == 0) {
+        // one box {64 dims, 64 keys, 9 chunks} = the whole page, as the decode kernel loads it
         mbar_arrive_expect_tx(bar, kGatherChunks * 8192);
-        for (int c = 0; c < kGatherChunks; ++c) tma_load_2d(smem + c * 8192, &tm_kv, bar, 64 * c, blk * kPage);
+        tma_load_3d(smem, &tm_kv, bar, 0, blk * kPage, 0);
     }
     // every thread waits (bounded); a timeout leaves out untouched
     const bool ok = mbar_wait(bar, 0, nullptr, nullptr, 2000000000LL);

@@ -41,6 +41,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "mla_internal.h"
 #include "ptx.cuh"
 
@@ -81,6 +83,11 @@ constexpr uint32_t kTmemQ = 0;       // score CTA: the 576 query dims as bf16 pa
 constexpr uint32_t kTmemS = 288;     // score CTA: two S buffers of 64 columns
 constexpr uint32_t kTmemCols = 512;  // value CTA: O, all columns
 
+// After an abort the value CTA waits this long for P messages that may still
+// be in flight towards its shared memory (a message lands within a few
+// microseconds; one that was only partly sent never completes its phase).
+constexpr long long kPDrainNs = 20000;
+
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: tolerate growth up to 2^8 before rescaling O
 
 struct Bars {
@@ -99,6 +106,7 @@ struct Bars {
     uint64_t drain;
     uint32_t tmem_slot;
     int abort;
+    int p_consumed;  // value CTA: P messages its MMA warp has taken (their successors are armed)
 };
 static_assert(sizeof(Bars) <= kOffX, "barrier block");
 
@@ -175,10 +183,21 @@ __device__ __forceinline__ int visible_keys(int seqlen, int s_q, int s, int caus
     return n < 0 ? 0 : (n > seqlen ? seqlen : n);
 }
 
-__device__ __forceinline__ int checked_block(const DecodeArgs& args, int b, int j, int* err) {
+// Tells both CTAs of the cluster to give up: every bounded wait of either
+// CTA then returns within a few polls instead of running to its limit.
+__device__ __forceinline__ void raise_abort(volatile int* abort) {
+    *abort = 1;
+    st_cluster_b32(mapa_shared(smem_u32(const_cast<int*>(abort)), cluster_ctarank() ^ 1u), 1u);
+}
+
+// Block id of page j of batch b. An id outside the pool (or a page past the
+// table row) records MLA_ERR_BAD_BLOCK, aborts the cluster and returns block
+// 0, so the load that follows stays inside the cache.
+__device__ __forceinline__ int checked_block(const DecodeArgs& args, int b, int j, int* err, volatile int* abort) {
     int blk = j < args.mbps ? args.block_table[(size_t)b * args.mbps + j] : -1;
     if (blk < 0 || blk >= args.num_blocks) {
         record_error(err, kErrBadBlock);
+        raise_abort(abort);
         blk = 0;
     }
     return blk;
@@ -220,7 +239,10 @@ __device__ void score_producer(const DecodeMaps& maps, const DecodeArgs& args, B
     PageIter pi;
     pi.init(args, part);
     // a schedule from other sequence lengths could start elsewhere
-    if (q_early && lane == 0 && (!pi.valid || pi.it.b != b_first)) record_error(err, kErrBadBlock);
+    if (q_early && lane == 0 && (!pi.valid || pi.it.b != b_first)) {
+        record_error(err, kErrBadBlock);
+        raise_abort(abort);
+    }
     bool ok = true;
     int r = 0;
     for (; ok && pi.valid; pi.advance()) {
@@ -243,7 +265,7 @@ __device__ void score_producer(const DecodeMaps& maps, const DecodeArgs& args, B
         if (r >= kRing) ok = warp_wait(&bars->ring_empty[r % kRing], ((r / kRing) - 1) & 1, abort, err, wait_ns);
         if (!ok) break;
         if (lane == 0) {
-            const int blk = checked_block(args, pi.it.b, pi.j, err);
+            const int blk = checked_block(args, pi.it.b, pi.j, err, abort);
             uint64_t* bar = &bars->ring_full[r % kRing];
             mbar_arrive_expect_tx(bar, (uint32_t)kPageBytes);
             tma_load_3d(ring + (r % kRing) * kPageBytes, &maps.kv, bar, 0, blk * kPage, 0);
@@ -480,7 +502,7 @@ __device__ void value_producer(const DecodeMaps& maps, const DecodeArgs& args, B
     for (; ok && pi.valid; pi.advance()) {
         if (v >= kVRing) ok = mbar_wait(&bars->v_empty[v % kVRing], ((v / kVRing) - 1) & 1, abort, err, wait_ns);
         if (!ok) break;
-        const int blk = checked_block(args, pi.it.b, pi.j, err);
+        const int blk = checked_block(args, pi.it.b, pi.j, err, abort);
         uint64_t* bar = &bars->v_full[v % kVRing];
         mbar_arrive_expect_tx(bar, (uint32_t)kVBytes);
         tma_load_3d(vring + (v % kVRing) * kVBytes, &maps.v, bar, 0, blk * kPage, 0);
@@ -499,11 +521,13 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
     PageIter pi;
     pi.init(args, part);
     bool ok = true, issued = false;
+    int consumed = 0;
     for (; ok && pi.valid; pi.advance()) {
         const int n = pi.n, k = n & 1, qi = pi.n_items - 1;
         const bool first = pi.first_of_item(), last = pi.last_of_item();
         ok = warp_wait<true>(&bars->p_full[k], (n >> 1) & 1, abort, err, wait_ns);
         if (!ok) break;
+        consumed = n + 1;
         if (lane == 0) {
             // P was written by the peer's generic stores: make it visible to the
             // tensor pipe, then arm the slot for page n + 2 (its bytes can only
@@ -559,6 +583,7 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
         __syncwarp();
         warp_wait(&bars->drain, 0, nullptr, err, kDrainNs);
     }
+    if (lane == 0) bars->p_consumed = consumed;
     return ok;
 }
 
@@ -753,6 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->stage_free, 1);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
+        bars->p_consumed = 0;
         fence_mbarrier_init_cluster();
         if (rank == 0) {
             tma_prefetch_desc(&maps.kv);
@@ -806,20 +832,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the peer may still store into our buffers or arrive on our barriers until
     // it has finished its last page: leave together
     cluster_sync_all();
+    if (rank == 1 && warp == kWarpMma && (threadIdx.x & 31) == 0 && *abort) {
+        // The score CTA has stopped sending, but the st.async stores of the two
+        // armed P messages (pages c and c + 1) may still be landing in this
+        // CTA's shared memory: wait for their phases, briefly, before leaving.
+        const int c = bars->p_consumed;
+        for (int n = c; n < c + 2; ++n) mbar_wait(&bars->p_full[n & 1], (n >> 1) & 1, nullptr, nullptr, kPDrainNs);
+    }
     if (warp == kWarpMma) {
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
 }
 
+// Sets the kernel's shared-memory attribute once per device (thread-safe).
 cudaError_t prepare_kernel() {
+    static std::mutex mu;
     static bool done[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done[dev]) return cudaSuccess;
     e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    if (e == cudaSuccess) done[dev] = true;
     return e;
 }
 

@@ -484,13 +484,8 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 
 cudaError_t launch_absorb(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const CUtensorMap* tm_out,
                           const GemmArgs& args, long long wait_ns, cudaStream_t stream) {
-    static int sm_count = 0;
-    if (sm_count == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sm_count <= 0)
-            sm_count = 152;
-    }
+    const int sm_count = device_sm_count();
+    if (sm_count <= 0) return cudaErrorInvalidDevice;
     cudaError_t e = cudaFuncSetAttribute(absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AbsSmem::kBytes);
     if (e != cudaSuccess) return e;
     const int units = args.H * ((args.R + kBM - 1) / kBM) * kAbsQuarters;

@@ -26,6 +26,9 @@ struct WorkspaceLayout {
 };
 WorkspaceLayout workspace_layout(int B, int s_q, int H, int num_parts);
 
+// SM count of the current device (cached per device ordinal), 0 on failure.
+int device_sm_count();
+
 cudaError_t launch_metadata(const int32_t* seqlens, int B, int num_parts, int ovh, int min_split,
                             int32_t* tile_meta, int32_t* num_splits, cudaStream_t stream);
 

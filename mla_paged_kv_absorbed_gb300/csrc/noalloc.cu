@@ -11,13 +11,14 @@
 //
 // The scratch is a file-scope __device__ array of MLA_NOALLOC_SCRATCH_BYTES.
 // Every GPU that loads this part of the library holds it until the process
-// exits. In host code the array's name is only a host-side stand-in, so the
-// device address is looked up with cudaGetSymbolAddress, once per device, with
-// that device current, on the first call made on it (that first call should
-// therefore come before any stream capture). Every call shares the one array:
+// exits; with lazy module loading (the CUDA default) that happens on the first
+// call on a device, which is when the array is reserved. In host code the
+// array's name is only a host-side stand-in, so every call looks up the device
+// address with cudaGetSymbolAddress on the current device (a lookup, no
+// allocation; after cudaDeviceReset it returns the new context's address, so
+// no stale pointer is kept). The first call on a device loads the module, so
+// it should come before any stream capture. Every call shares the one array:
 // calls that overlap on the GPU (different streams, no ordering) race on it.
-#include <mutex>
-
 #include "mla.h"
 #include "mla_internal.h"
 
@@ -28,21 +29,11 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[MLA_NOALLOC_SCR
 namespace mla {
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 // Device address of g_noalloc_scratch on the current device (nullptr on failure).
 void* scratch_address() {
-    static std::mutex mu;
-    static void* addr[kMaxDevices] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lk(mu);
-    if (addr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-        addr[dev] = p;
-    }
-    return addr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    return p;
 }
 
 }  // namespace

@@ -11,7 +11,7 @@ Recipe (one ``torch.Generator('cpu')`` per call, seeded with ``seed``):
   * Every visible cache row [c_KV 512 | k_rope 64] ~ N(0, 1) -> bf16.
   * Pages: pool = sum of pages + ceil(10 %) decoy blocks; physical blocks are
     a random permutation of the pool. Decoy blocks and the rows past seqlen in
-    each last page hold finite garbage, uniform in [-1e4, 1e4].
+    each last page hold finite garbage, N(0, 1) x 1e4 -> bf16.
   * Block-table entries past a sequence's last page are -1.
 
 Workloads named after what they are (DeepSeek-V3 decode shapes: 128 heads,
@@ -92,7 +92,9 @@ def _randn(g, shape, std=1.0):
 
 
 def _garbage(g, shape, amp=1.0e4):
-    return ((torch.rand(shape, generator=g, dtype=torch.float32) * 2.0 - 1.0) * amp).to(torch.bfloat16)
+    # normal rather than uniform: torch.rand with a generator is several times
+    # slower, and only the magnitude matters (finite values far from the data)
+    return (torch.randn(shape, generator=g, dtype=torch.float32) * amp).to(torch.bfloat16)
 
 
 def make_inputs(B: int, s_q: int, H: int, seqlens, seed: int, *, q_mode: str = "q", causal: bool = True,
@@ -125,7 +127,11 @@ def make_inputs(B: int, s_q: int, H: int, seqlens, seed: int, *, q_mode: str = "
     perm = torch.randperm(pool, generator=g).to(torch.int32)
     table = torch.full((B, mbps), -1, dtype=torch.int32)
     if garbage:
-        kv = _garbage(g, (pool, PAGE, D_QK))
+        # every block is overwritten below except the decoys: draw garbage for those only
+        kv = torch.empty((pool, PAGE, D_QK), dtype=torch.bfloat16)
+        decoys = perm[used:].long()
+        if decoys.numel():
+            kv[decoys] = _garbage(g, (decoys.numel(), PAGE, D_QK))
     else:
         kv = torch.zeros((pool, PAGE, D_QK), dtype=torch.bfloat16)
     k = 0
@@ -141,11 +147,13 @@ def make_inputs(B: int, s_q: int, H: int, seqlens, seed: int, *, q_mode: str = "
         vals = vals.view(n, PAGE, D_QK)
         tail = n * PAGE - L
         if tail > 0:
-            # rows past seqlen keep the block's garbage (or the requested fill)
-            keep = kv[blocks[-1].long(), PAGE - tail:].clone()
+            # rows past seqlen hold garbage (or the requested fill)
             if tail_fill is not None:
-                keep.fill_(tail_fill)
-            vals[-1, PAGE - tail:] = keep
+                vals[-1, PAGE - tail:] = tail_fill
+            elif garbage:
+                vals[-1, PAGE - tail:] = _garbage(g, (tail, D_QK))
+            else:
+                vals[-1, PAGE - tail:] = 0
         kv[blocks.long()] = vals
     q = q_abs = w_uk = w_uv = None
     if q_mode == "q":

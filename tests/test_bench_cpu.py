@@ -30,7 +30,8 @@ def _env(**extra):
 
 
 def test_reference_arm_json_line():
-    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0"],
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "dsv3", "--steps", "1",
+                        "--warmup", "0"],
                        cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = _json_lines(r.stdout)
@@ -42,6 +43,8 @@ def test_reference_arm_json_line():
     assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 0
     assert d["value"] > 0 and d["higher_is_better"] is False
     assert d["config"]["workload"].startswith("dsv3")
+    for key in ("global_batch", "seq_len", "parallelism"):
+        assert key in d["config"], key
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
@@ -50,8 +53,8 @@ def test_reference_arm_json_line():
 def test_reference_arm_two_gloo_ranks():
     port = _free_port()
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr",
-           "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
-           "--warmup", "0"]
+           "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference", "--workload", "dsv3",
+           "--gpus", "2", "--steps", "1", "--warmup", "0"]
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=900,
                        env=_env(MLA_BENCH_BACKEND="gloo", OMP_NUM_THREADS="4"))
     assert r.returncode == 0, r.stderr[-3000:]
@@ -86,3 +89,16 @@ def test_max_over_ranks_two_gloo_ranks():
     assert all(p.exitcode == 0 for p in procs)
     got = sorted(q.get(timeout=10) for _ in range(2))
     assert got == [(0, 2.5), (1, 2.5)]
+
+
+def test_default_workload_is_the_largest_single_gpu_configuration():
+    """With no flags the benchmark times the multi-token causal workload end to
+    end (B = 132, s_q = 2, 4096 tokens): the largest configuration of the path
+    that fits one GPU; the other named workloads are reported decode-only."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from mla_paged_kv_absorbed_gb300 import inputs as gen
+    assert bench.WORKLOAD == "spec"
+    w = gen.WORKLOADS["spec"]
+    assert (w["B"], w["s_q"], w["H"], w["seqlens"], w["q_mode"]) == (132, 2, 128, 4096, "q")
+    assert set(bench.DECODE_WORKLOADS) == {"dsv3", "varlen", "long"}

@@ -1,9 +1,12 @@
 """GPU parity of the decode path through the C ABI against the CPU oracle.
 
-Small cases run the oracle on every output; the five named workloads run at
-full size in the launch configuration the benchmark times (default number of
-schedule parts) and compare sampled sequences, which the oracle evaluates one
-by one at their full length."""
+Every comparison covers every output: small edge cases, forced split counts,
+and the five named workloads at full size in the launch configuration the
+benchmark times (default number of schedule parts), two seeds each. Device
+failure handling is exercised without any fault: a bounded wait made to run
+out, a block id outside the pool, and a schedule built from other lengths."""
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -119,44 +122,29 @@ def test_non_causal_multi_token(api):
     check_decode(inp, run(api, inp))
 
 
-# -------------------------------------------------- named workloads, sampled --
+# ------------------------------------------- named workloads, every output --
 
-def sampled_check(api, name, batches, heads=None, end_to_end=False):
-    inp = gen.make_workload(name)
+NAMED = [("tiny", True), ("dsv3", True), ("varlen", False), ("long", False), ("spec", True)]
+
+
+@pytest.mark.parametrize("rep", [0, 1])
+@pytest.mark.parametrize("name,end_to_end", NAMED)
+def test_named_workload_full_parity(api, name, end_to_end, rep):
+    """Each named workload at full size, in the launch configuration the
+    benchmark times (default number of schedule parts), two seeds: the schedule
+    bit-exact, every (b, s, h) of o_lat and lse against the oracle on the GPU's
+    absorbed query, and for the end-to-end workloads q_abs and the projected
+    output against the oracle's full fp64 chain from q, W_UK and W_UV."""
+    inp = gen.make_workload(name, rep=rep)
     r = run(api, inp)
-    assert r["status"] == 0
-    sub = gen.sample_batches(inp, batches)
-    idx = torch.tensor(batches)
-    q_abs = r["q_abs"][idx]
-    o_gpu, lse_gpu = r["o"][idx], r["lse"][idx]
-    if heads is not None:
-        q_abs, o_gpu, lse_gpu = q_abs[:, :, heads], o_gpu[:, :, heads], lse_gpu[:, :, heads]
-    o_ref, lse_ref = oracle.attend_absorbed(f32(q_abs), f32(sub.kv_cache), sub.block_table, sub.seqlens, sub.scale,
-                                            sub.causal)
-    assert_o_close(o_gpu, o_ref, f"{name} o_lat")
-    assert_lse_close(lse_gpu, lse_ref, f"{name} lse")
+    ovh, min_split = api.mla_schedule_constants()
+    ref_tm, ref_ns = oracle.metadata(inp.seqlens.numpy(), r["tm"].shape[0], ovh, min_split)
+    assert np.array_equal(r["tm"].numpy(), ref_tm) and np.array_equal(r["ns"].numpy(), ref_ns)
+    check_decode(inp, r)
     if end_to_end:
-        qa = oracle.absorb_q(f32(sub.q), f32(sub.w_uk))
-        o64, _ = oracle.attend_absorbed(qa, f32(sub.kv_cache), sub.block_table, sub.seqlens, sub.scale, sub.causal)
-        out_ref = oracle.out_proj(o64, f32(sub.w_uv))
-        assert_o_close(r["out"][idx], out_ref, f"{name} out")
-    return r
-
-
-def test_workload_dsv3(api):
-    sampled_check(api, "dsv3", [0, 1, 37, 64, 100, 127], end_to_end=True)
-
-
-def test_workload_varlen(api):
-    sampled_check(api, "varlen", [0, 13, 31, 50, 63])
-
-
-def test_workload_long(api):
-    sampled_check(api, "long", [0, 7, 15], heads=list(range(0, 128, 8)))
-
-
-def test_workload_spec(api):
-    sampled_check(api, "spec", [0, 65, 131], end_to_end=True)
+        qa, _, _, out = oracle_end_to_end(inp)
+        assert_o_close(r["q_abs"], qa, f"{name} q_abs")
+        assert_o_close(r["out"], out, f"{name} out")
 
 
 # ------------------------------------------------------ repeated launches --
@@ -218,3 +206,54 @@ def test_host_rejects_bad_shapes(api):
     with pytest.raises(api.MLAError) as e:
         api.mla_decode_paged(mis, d.kv_cache, d.block_table, d.seqlens, tm, ns, d.scale, True, workspace=ws)
     assert e.value.status == api.MLA_ERR_INVALID_ARG
+
+
+def test_mispaired_schedule_reports_bad_block_promptly(api):
+    """A schedule built from other sequence lengths walks table entries past
+    the sequences' pages: the device records MLA_ERR_BAD_BLOCK and both CTAs
+    of every cluster that met it leave at once, instead of waiting out the
+    default four-second limit."""
+    inp = gen.make_workload("tiny")
+    check_decode(inp, run(api, inp, 4))  # module loaded and warm
+    d = inp.to("cuda")
+    q_abs = api.mla_absorb_q(d.q, d.w_uk)
+    other = torch.tensor([1000, 2000], dtype=torch.int32, device="cuda")
+    tm, ns = api.mla_get_metadata(other, d.s_q, d.H, 4)
+    ws = api.make_workspace(d.B, d.s_q, d.H, 4)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    api.mla_decode_paged(q_abs, d.kv_cache, d.block_table, d.seqlens, tm, ns, d.scale, d.causal, workspace=ws)
+    status = api.mla_read_device_error(ws)
+    dt = time.perf_counter() - t0
+    assert status == api.MLA_ERR_BAD_BLOCK
+    assert dt < 0.5, f"took {dt:.3f} s"
+    # the context is still usable
+    check_decode(inp, run(api, inp, 4))
+
+
+@pytest.mark.parametrize("limit_ns", [100, 1000])
+def test_bounded_wait_expiry_returns_timeout(api, limit_ns):
+    """With a wait limit far below the latency of a TMA load, the first
+    pipeline wait of each cluster runs out: the kernel records
+    MLA_ERR_TIMEOUT, tells the peer CTA, drains its copies and MMAs, frees its
+    tensor memory and returns. Afterwards, with the default limit restored, the
+    same call matches the oracle."""
+    inp = gen.make_workload("tiny")
+    check_decode(inp, run(api, inp))
+    d = inp.to("cuda")
+    tm, ns = api.mla_get_metadata(d.seqlens, d.s_q, d.H)
+    q_abs = api.mla_absorb_q(d.q, d.w_uk)
+    ws = api.make_workspace(d.B, d.s_q, d.H, tm.shape[0])
+    torch.cuda.synchronize()
+    api.mla_set_wait_limit_ns(limit_ns)
+    try:
+        t0 = time.perf_counter()
+        api.mla_decode_paged(q_abs, d.kv_cache, d.block_table, d.seqlens, tm, ns, d.scale, d.causal, workspace=ws)
+        status = api.mla_read_device_error(ws)
+        dt = time.perf_counter() - t0
+    finally:
+        api.mla_set_wait_limit_ns(0)
+    assert status == api.MLA_ERR_TIMEOUT
+    assert dt < 1.0, f"took {dt:.3f} s"
+    for _ in range(3):
+        check_decode(inp, run(api, inp))

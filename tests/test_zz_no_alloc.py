@@ -36,12 +36,22 @@ def test_noalloc_matches_regular_entry_twice(api, s_q, seqlens, num_parts):
                                           inp.causal)
     ref_o, ref_lse = ref_o.cpu().double().numpy(), ref_lse.cpu().double().numpy()
     status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
-    for _ in range(2):
-        o = torch.full_like(inp.q_abs[..., :512], float("nan"))
-        lse = torch.full((inp.B, s_q, 128), float("nan"), dtype=torch.float32, device="cuda")
+    outs = [(torch.empty((inp.B, s_q, 128, 512), dtype=torch.bfloat16, device="cuda"),
+             torch.empty((inp.B, s_q, 128), dtype=torch.float32, device="cuda")) for _ in range(2)]
+    free_before = None
+    for call, (o, lse) in enumerate(outs):
+        o.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        torch.cuda.synchronize()
+        if call == 1:
+            free_before = torch.cuda.mem_get_info()[0]
         api.mla_decode_paged_noalloc(inp.q_abs, inp.kv_cache, inp.block_table, inp.seqlens, tm, ns, inp.scale,
                                      inp.causal, o, lse, device_status=status)
         torch.cuda.synchronize()
+        if call == 1:
+            # after the first call (which may load the module and reserve the
+            # scratch array), a call takes no device memory at all
+            assert torch.cuda.mem_get_info()[0] == free_before
         assert int(status.item()) == 0
         assert_o_close(o.cpu(), ref_o, "o_lat (no-alloc vs regular)")
         assert_lse_close(lse.cpu(), ref_lse, "lse (no-alloc vs regular)")
