@@ -17,6 +17,9 @@ Parity status per function (how each is pinned, see tests/test_oracle_pins.py):
   combine, attend_split                              - pinned (split == single pass)
   metadata                                           - pinned by invariants and a
       hand-derived example; the pages print no schedule values.
+  rope, cache_append                                 - pinned (identity at
+      position 0, exact quarter and half turns, norm preservation, relative
+      position, composition; bit-exact latent copy into the table's slot)
 """
 from __future__ import annotations
 
@@ -76,6 +79,8 @@ def _load():
         lib.orc_metadata.restype = I
         lib.orc_attend_split.argtypes = [P, P, P, I, P, I, I, I, D, I, P, I, P, P, P, P, P]
         lib.orc_num_threads.restype = I
+        lib.orc_rope.argtypes = [P, I64, I, P, D, P]
+        lib.orc_cache_append.argtypes = [P, P, I, P, I, I, D, P]
         _lib = lib
         return lib
 
@@ -213,3 +218,29 @@ def attend_split(q_abs, kv, block_table, seqlens, scale: float, causal: bool, ti
                              int(bool(causal)), _ptr(tm), tm.shape[0], _ptr(ns), _ptr(o), _ptr(lse),
                              _ptr(op), _ptr(lp))
     return o, lse, op[:P], lp[:P]
+
+
+def rope(x, pos, base: float = 10000.0) -> np.ndarray:
+    """Rotary encoding of x [..., d] at positions pos [...] (broadcast over the last dim) -> float64."""
+    x = _arr(x, np.float32)
+    d = x.shape[-1]
+    assert d % 2 == 0
+    rows = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
+    p = np.ascontiguousarray(np.broadcast_to(np.asarray(pos, np.int64), x.shape[:-1]).reshape(rows))
+    y = np.empty(x.shape, np.float64)
+    _load().orc_rope(_ptr(x), rows, d, _ptr(p), float(base), _ptr(y))
+    return y
+
+
+def cache_append(kv, kv_new, block_table, seqlens, base: float = 10000.0) -> np.ndarray:
+    """A copy of kv [num_blocks, 64, 576] (float64) with each sequence's s_q new
+    tokens kv_new [B, s_q, 576] written to their slots (latent copied, rope part
+    rotary-encoded at the token's position seqlen - s_q + s)."""
+    out = np.array(_arr(kv, np.float64), copy=True)
+    new = _arr(kv_new, np.float32)
+    bt = _arr(block_table, np.int32)
+    sl = _arr(seqlens, np.int32)
+    B, s_q, d = new.shape
+    assert d == D_QK and bt.shape[0] == B and sl.shape[0] == B and out.shape[1:] == (PAGE, D_QK)
+    _load().orc_cache_append(_ptr(new), _ptr(bt), bt.shape[1], _ptr(sl), B, s_q, float(base), _ptr(out))
+    return out

@@ -414,6 +414,55 @@ void orc_attend_split(const double* q_abs, const float* kv, const int32_t* block
     if (!lse_parts_out) free(lse_parts);
 }
 
+/*
+ * Rotary position encoding of the decoupled rope parts [V3 sec. 3.1: RoPE(q_pos, t)
+ * is a rotation that depends on the token position t; sec. 3.2: the position key
+ * is RoPE applied per token]. The pages do not print the rotation itself; this
+ * is the standard rotary encoding: the d-vector is read as d/2 adjacent pairs
+ * (x[2i], x[2i+1]), and pair i is rotated by the angle t * theta_i with
+ * theta_i = base^(-2i/d):
+ *   y[2i]   = x[2i] cos(t theta_i) - x[2i+1] sin(t theta_i)
+ *   y[2i+1] = x[2i] sin(t theta_i) + x[2i+1] cos(t theta_i)
+ * x [rows, d] float, pos [rows] -> y [rows, d] double.
+ */
+void orc_rope(const float* x, int64_t rows, int d, const int64_t* pos, double base, double* y) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int i = 0; i < d / 2; ++i) {
+            double theta = pow(base, -2.0 * i / d);
+            double a = (double)pos[r] * theta;
+            double c = cos(a), sn = sin(a);
+            double x0 = x[r * d + 2 * i], x1 = x[r * d + 2 * i + 1];
+            y[r * d + 2 * i] = x0 * c - x1 * sn;
+            y[r * d + 2 * i + 1] = x0 * sn + x1 * c;
+        }
+    }
+}
+
+/*
+ * Appending the s_q new tokens of each sequence to its paged cache [V3 sec. 4.3:
+ * only the latent is stored, kv_cache.store(c_kv); sec. 3.2: the position key
+ * is the rotary-encoded rope part]. Token s of sequence b sits at position
+ * t = seqlen_b - s_q + s (the lengths already count the new tokens); its slot is
+ * row t % 64 of block block_table[b][t / 64]. The slot receives
+ * [c_KV (512, as given) | RoPE(k_rope (64), t)]. Tokens with t < 0 are skipped.
+ * kv_new [B, s_q, 576] float (c_KV | un-rotated k_rope); kv [num_blocks, 64, 576]
+ * double, updated in place (other slots untouched).
+ */
+void orc_cache_append(const float* kv_new, const int32_t* block_table, int mbps, const int32_t* seqlens, int B,
+                      int s_q, double base, double* kv) {
+    for (int b = 0; b < B; ++b)
+        for (int s = 0; s < s_q; ++s) {
+            int64_t t = (int64_t)seqlens[b] - s_q + s;
+            if (t < 0) continue;
+            int64_t blk = block_table[(int64_t)b * mbps + t / ORC_PAGE];
+            double* slot = kv + (blk * ORC_PAGE + t % ORC_PAGE) * ORC_DQK;
+            const float* src = kv_new + ((int64_t)b * s_q + s) * ORC_DQK;
+            for (int c = 0; c < ORC_DC; ++c) slot[c] = src[c];
+            orc_rope(src + ORC_DC, 1, ORC_DR, &t, base, slot + ORC_DC);
+        }
+}
+
 /* Threads the OpenMP runtime will use (1 when built without OpenMP). */
 int orc_num_threads(void) {
 #ifdef _OPENMP
