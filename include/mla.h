@@ -194,9 +194,41 @@ int mla_out_proj(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla_bf16_t* ou
                  mla_stream_t stream);
 
 /*
- * Reads and clears the device error word of `workspace` (synchronises
- * `stream`). Returns MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_BAD_BLOCK as recorded
- * by the kernels since the last read, or MLA_ERR_CUDA if the read failed.
+ * mla_rope_append - the step before the decode: rotary position encoding of
+ * the decoupled rope parts and the append of the new tokens to the paged
+ * latent cache. Pages: [V3] sec. 3.1 (the rope query part and the position
+ * key are rotated by a position-dependent angle, apart from the latent),
+ * sec. 3.2 (the position key of token t is RoPE applied per token), sec. 4.3
+ * (only the latent is stored, page by page: kv_cache.store(c_kv)). The pages
+ * describe the rotation in words only; this is the standard rotary encoding:
+ * the 64 rope dims are 32 adjacent pairs (x[2i], x[2i+1]) and pair i turns by
+ * the angle t * theta_i, theta_i = rope_base^(-2i/64).
+ *
+ * Token s of sequence b sits at position t = cache_seqlens[b] - s_q + s
+ * (cache_seqlens already counts the s_q new tokens, as mla_decode_paged
+ * expects). For every such token with t >= 0:
+ *   q[b,s,h,128:192] <- RoPE(q[b,s,h,128:192], t) for every head h (in place;
+ *                       q [B, s_q, H, 192] bf16, the nope part is untouched);
+ *   row t % 64 of block block_table[b][t / 64] of kv_cache [num_blocks, 64, 576]
+ *                    <- [kv_new[b,s,0:512] | RoPE(kv_new[b,s,512:576], t)]
+ *                       (kv_new [B, s_q, 576] bf16: the new token's c_KV and
+ *                       its not yet rotated k_rope; the latent is copied as is).
+ * Angles are reduced in double precision; the rotation is done in fp32 and
+ * rounded to bf16 (round to nearest even). rope_base > 1 (DeepSeek-V3: 10000).
+ * A block id outside [0, num_blocks), or a position past the table row, is
+ * recorded as MLA_ERR_BAD_BLOCK in the library's own error word (read by
+ * mla_read_device_error) and that row is not written. One small launch (one
+ * CTA per new token), no host synchronisation.
+ */
+int mla_rope_append(mla_bf16_t* q, const mla_bf16_t* kv_new, const int32_t* cache_seqlens, const int32_t* block_table,
+                    int max_blocks_per_seq, mla_bf16_t* kv_cache, int num_blocks, int B, int s_q, int H,
+                    float rope_base, mla_stream_t stream);
+
+/*
+ * Reads and clears the device error word of `workspace` (may be NULL) and the
+ * library's own error word (projections, rope append); synchronises `stream`.
+ * Returns MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_BAD_BLOCK as recorded by the
+ * kernels since the last read, or MLA_ERR_CUDA if the read failed.
  */
 int mla_read_device_error(void* workspace, mla_stream_t stream);
 
@@ -264,6 +296,17 @@ int mla_decode_paged_noalloc(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache
 int mla_debug_gather(const mla_bf16_t* kv_cache, int num_blocks, const int32_t* block_table,
                      int max_blocks_per_seq, const int32_t* cache_seqlens, int B, int max_tokens,
                      mla_bf16_t* out, mla_stream_t stream);
+
+/*
+ * Failure-path check without any fault: with `enable` != 0, mla_decode_paged
+ * launches made afterwards (process-wide) never issue the value CTA's first
+ * page load, so the P.V warp's bounded wait for it runs out: the kernel
+ * records MLA_ERR_TIMEOUT, aborts both CTAs of each cluster with work, drains
+ * what is in flight, frees its tensor memory and returns (the outputs of that
+ * call are undefined). Nothing is read or written out of bounds. 0 restores
+ * normal operation.
+ */
+void mla_debug_withhold_value_load(int enable);
 
 /*
  * One-tile tcgen05 check: D[128, N] = A[128, K] * B[K, N] in fp32, the same

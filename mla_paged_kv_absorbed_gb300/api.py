@@ -75,6 +75,9 @@ def lib() -> ctypes.CDLL:
         L.mla_debug_gather.restype = I
         L.mla_debug_mma.argtypes = [P, P, I, I, I, I, P, P]
         L.mla_debug_mma.restype = I
+        L.mla_debug_withhold_value_load.argtypes = [I]
+        L.mla_rope_append.argtypes = [P, P, P, P, I, P, I, I, I, I, F, P]
+        L.mla_rope_append.restype = I
         _lib = L
         return L
 
@@ -140,6 +143,12 @@ def mla_workspace_size(B: int, s_q: int, H: int, num_parts: int) -> int:
 
 def mla_set_wait_limit_ns(ns: int):
     lib().mla_set_wait_limit_ns(int(ns))
+
+
+def mla_debug_withhold_value_load(enable: bool):
+    """Test hook: later decode launches never issue the value CTA's first page
+    load, so a bounded wait runs out (see include/mla.h)."""
+    lib().mla_debug_withhold_value_load(int(bool(enable)))
 
 
 def make_workspace(B: int, s_q: int, H: int, num_parts: int, device=None) -> torch.Tensor:
@@ -253,9 +262,30 @@ def mla_out_proj(o_lat: torch.Tensor, w_uv: torch.Tensor, out: Optional[torch.Te
     return out
 
 
-def mla_read_device_error(workspace: torch.Tensor, stream=None) -> int:
-    """Device-recorded status since the last read (synchronises the stream)."""
+def mla_read_device_error(workspace: Optional[torch.Tensor] = None, stream=None) -> int:
+    """Device-recorded status since the last read (synchronises the stream):
+    the workspace's error word (if given) and the library's own word."""
     return int(lib().mla_read_device_error(_p(workspace), _stream(stream)))
+
+
+def mla_rope_append(q: torch.Tensor, kv_new: torch.Tensor, cache_seqlens: torch.Tensor, block_table: torch.Tensor,
+                    kv_cache: torch.Tensor, rope_base: float = 10000.0, stream=None) -> None:
+    """Rotary-encodes the rope part of q [B, s_q, H, 192] in place and writes
+    each new token [c_KV | RoPE(k_rope)] from kv_new [B, s_q, 576] into its
+    cache slot (position cache_seqlens[b] - s_q + s). See include/mla.h."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(kv_new, "kv_new", torch.bfloat16, 3)
+    _need(cache_seqlens, "cache_seqlens", torch.int32, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(kv_cache, "kv_cache", torch.bfloat16, 3)
+    B, s_q, H, dq = q.shape
+    if dq != D_Q or tuple(kv_new.shape) != (B, s_q, D_QK) or tuple(kv_cache.shape[1:]) != (PAGE, D_QK):
+        raise ValueError("q must be [B, s_q, H, 192], kv_new [B, s_q, 576] and kv_cache [num_blocks, 64, 576]")
+    if cache_seqlens.shape[0] != B or block_table.shape[0] != B:
+        raise ValueError("cache_seqlens and block_table must match the batch of q")
+    _check("mla_rope_append", lib().mla_rope_append(_p(q), _p(kv_new), _p(cache_seqlens), _p(block_table),
+                                                    block_table.shape[1], _p(kv_cache), kv_cache.shape[0], B, s_q, H,
+                                                    float(rope_base), _stream(stream)))
 
 
 # -------------------------------------------------------------- test hooks --

@@ -24,6 +24,7 @@ WorkspaceLayout workspace_layout(int B, int s_q, int H, int num_parts) {
 namespace {
 
 std::atomic<long long> g_wait_ns{4000000000LL};
+std::atomic<int> g_withhold{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -188,6 +189,8 @@ size_t mla_workspace_size(int B, int s_q, int H, int num_parts) {
 
 void mla_set_wait_limit_ns(long long ns) { g_wait_ns.store(ns > 0 ? ns : 4000000000LL); }
 
+void mla_debug_withhold_value_load(int enable) { g_withhold.store(enable != 0 ? 1 : 0); }
+
 int mla_get_metadata(const int32_t* cache_seqlens, int B, int s_q, int H, int h_kv, int num_parts,
                      int32_t* tile_meta, int32_t* num_splits, mla_stream_t stream) {
     if (!cache_seqlens || !tile_meta || !num_splits || B <= 0 || num_parts <= 0 || num_parts > 65536 || h_kv != 1 ||
@@ -287,6 +290,7 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
     a.o_part = reinterpret_cast<float*>(ws + wl.o_offset);
     a.err = reinterpret_cast<int*>(ws);
     a.wait_ns = g_wait_ns.load();
+    a.withhold = g_withhold.load();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_decode(maps, a, st);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
@@ -295,15 +299,31 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
 }
 
 int mla_read_device_error(void* workspace, mla_stream_t stream) {
-    if (!workspace) return MLA_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int ws_err = 0, gemm_err = 0;
-    if (cudaMemcpyAsync(&ws_err, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        return MLA_ERR_CUDA;
+    int ws_err = 0, gemm_err = 0, rope_err = 0;
+    if (workspace != nullptr) {
+        if (cudaMemcpyAsync(&ws_err, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            return MLA_ERR_CUDA;
+        if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
+    }
     if (gemm_error_fetch(&gemm_err, st) != cudaSuccess) return MLA_ERR_CUDA;
-    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (rope_error_fetch(&rope_err, st) != cudaSuccess) return MLA_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
-    return ws_err != 0 ? ws_err : gemm_err;
+    return ws_err != 0 ? ws_err : (gemm_err != 0 ? gemm_err : rope_err);
+}
+
+int mla_rope_append(mla_bf16_t* q, const mla_bf16_t* kv_new, const int32_t* cache_seqlens, const int32_t* block_table,
+                    int max_blocks_per_seq, mla_bf16_t* kv_cache, int num_blocks, int B, int s_q, int H,
+                    float rope_base, mla_stream_t stream) {
+    if (!q || !kv_new || !cache_seqlens || !block_table || !kv_cache || B <= 0 || num_blocks <= 0 ||
+        max_blocks_per_seq <= 0 || !valid_sq(s_q) || !valid_heads(H) || !(rope_base > 1.f))
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv_new) || !aligned16(kv_cache)) return MLA_ERR_INVALID_ARG;
+    if ((int64_t)B * s_q > 0x7FFFFFFF) return MLA_ERR_INVALID_ARG;
+    int dev = check_device();
+    if (dev != MLA_OK) return dev;
+    return cuda_status(launch_rope_append(q, kv_new, cache_seqlens, block_table, max_blocks_per_seq, kv_cache,
+                                          num_blocks, B, s_q, H, (double)rope_base, static_cast<cudaStream_t>(stream)));
 }
 
 int mla_debug_gather(const mla_bf16_t* kv_cache, int num_blocks, const int32_t* block_table, int max_blocks_per_seq,

@@ -31,11 +31,15 @@
 // 8 KB boxes would stream at a fifth of the rate. The query of a new batch
 // arrives the same way (two boxes of 64 rows) and the softmax threads move it
 // into TMEM.
-// Roles (10 warps per CTA): warps 0-7 softmax (score CTA) or O rescale and
-// epilogue (value CTA), two warps per TMEM lane quadrant - on the score CTA
-// warp half h owns keys [32 h, 32 h + 32) of a page, on the value CTA O
-// columns [256 h, 256 h + 256); warp 8 TMA producer; warp 9 MMA issuer and
-// TMEM owner.
+// Roles (19 warps per CTA). Score CTA: warps 0-15 softmax in two groups of
+// eight that take alternate pages (page n goes to group n % 2), two warps of a
+// group per TMEM lane quadrant, warp half h owning keys [32 h, 32 h + 32) of a
+// page; warp 16 TMA producer; warps 17 and 18 issue the score products of the
+// even and odd pages (one issuing warp alone cannot keep the tensor pipe busy
+// with N = 64 products); warp 17 owns TMEM. Value CTA: warps 0-7 O rescale and
+// epilogue, two per lane quadrant, warp half h owning O columns
+// [256 h, 256 h + 256); warp 16 TMA producer; warp 17 P.V issuer and TMEM
+// owner; the other warps have no role.
 // Every wait is bounded; on expiry the kernel records MLA_ERR_TIMEOUT, tells
 // the peer CTA, drains its copies and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -49,10 +53,17 @@
 namespace mla {
 namespace {
 
-constexpr int kThreads = 320;
+// Warps: 0-15 softmax (score CTA; two groups of eight, one per page parity)
+// or 0-7 O rescale and epilogue (value CTA), 16 TMA producer, 17 MMA issuer
+// and TMEM owner (score CTA: even pages), 18 second score MMA issuer (odd
+// pages; idle on the value CTA).
+constexpr int kThreads = 608;
 constexpr int kRows = 128;
-constexpr int kWarpProducer = 8;
-constexpr int kWarpMma = 9;
+constexpr int kSoftmaxWarps = 16;
+constexpr int kOWarps = 8;
+constexpr int kWarpProducer = 16;
+constexpr int kWarpMma = 17;
+constexpr int kWarpMma2 = 18;
 constexpr int kChunks = kDQK / 64;  // 9 chunks of 64 dims
 
 // ---- shared memory (offsets from a 1024-byte-aligned base) ----
@@ -60,7 +71,14 @@ constexpr int kChunkBytes = kPage * 128;           // [64 rows x 64 bf16], 128-b
 constexpr int kPageBytes = kChunks * kChunkBytes;  // a page (or 64 query rows): [9 chunks][64 rows][64 dims]
 constexpr int kOffBars = 0;
 constexpr int kOffX = 1024;                        // score: row-stat exchange; value: rescale factors and 1/l
-constexpr int kOffRole = 4096;
+// score CTA exchange area (floats, from kOffX):
+constexpr int kXPair = 0;                          // [group][episode 2][half 2][128]: the pair's half-row values
+constexpr int kXRef = kXPair + 2 * 2 * 2 * kRows;  // [page parity][128]: reference max after a page
+constexpr int kXLSum = kXRef + 2 * kRows;          // [group][half][128]: a group's share of the row sum
+constexpr int kXLMax = kXLSum + 2 * 2 * kRows;     // [group][128]: the reference max that share is relative to
+constexpr int kXFloats = kXLMax + 2 * kRows;
+constexpr int kOffRole = 9216;
+static_assert(kOffX + 4 * kXFloats <= kOffRole, "exchange area");
 // score CTA
 constexpr int kRing = 3;
 constexpr int kOffRing = kOffRole;
@@ -96,6 +114,9 @@ struct Bars {
     uint64_t q_full, q_drained;
     uint64_t s_full[2], s_free[2];
     uint64_t p_free[2];  // score CTA; arrivals come from the value CTA
+    uint64_t ref_full[2][4];  // [page parity][lane quadrant]: reference max of a page published
+    uint64_t lsum_full[4];    // [lane quadrant]: the group without an item's last page published its row sums
+    uint64_t drain2;          // second score MMA warp
     // value CTA
     uint64_t p_full[2];  // own arrive + expect_tx, bytes from the score CTA
     uint64_t v_full[kVRing], v_empty[kVRing];
@@ -278,14 +299,17 @@ __device__ void score_producer(const DecodeMaps& maps, const DecodeArgs& args, B
     __syncwarp();
 }
 
-// Returns false when it gave up (timeout or abort).
-__device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uint32_t tmem, int part,
+// Score products of the pages with parity `parity` (two warps issue them, one
+// per parity, so that the tensor pipe sees two instruction streams). Returns
+// false when it gave up (timeout or abort).
+__device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uint32_t tmem, int part, int parity,
                           volatile int* abort) {
     int* err = args.err;
     const long long wait_ns = args.wait_ns;
     const int lane = threadIdx.x & 31;
     uint8_t* ring = smem + kOffRing;
     constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kPage, false, false);
+    uint64_t* drain = parity == 0 ? &bars->drain : &bars->drain2;
     PageIter pi;
     pi.init(args, part);
     bool ok = true, issued = false;
@@ -297,80 +321,102 @@ __device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
             // done reading its two ring slots
             ok = warp_wait(&bars->q_full, qi & 1, abort, err, wait_ns);
             if (!ok) break;
-            if (lane == 0) {
+            if (parity == 0 && lane == 0) {
                 mbar_arrive(&bars->ring_empty[r % kRing]);
                 mbar_arrive(&bars->ring_empty[(r + 1) % kRing]);
             }
             __syncwarp();
             r += 2;
         }
-        // S buffer `buf` was read by the softmax of page n - 2
-        if (n >= 2) ok = warp_wait(&bars->s_free[buf], ((n >> 1) - 1) & 1, abort, err, wait_ns);
-        if (ok) ok = warp_wait(&bars->ring_full[r % kRing], (r / kRing) & 1, abort, err, wait_ns);
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-            // one descriptor per page; a K-step moves its start address field
-            // (bytes / 16) by a constant
-            const uint64_t bdesc = desc_sw128(smem_u32(ring + (r % kRing) * kPageBytes), 0, 1024);
-            const uint32_t d = tmem + kTmemS + 64u * (uint32_t)buf;
+        if (buf == parity) {
+            // S buffer `buf` was read by the softmax of page n - 2
+            if (n >= 2) ok = warp_wait(&bars->s_free[buf], ((n >> 1) - 1) & 1, abort, err, wait_ns);
+            if (ok) ok = warp_wait(&bars->ring_full[r % kRing], (r / kRing) & 1, abort, err, wait_ns);
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+                // one descriptor per page; a K-step moves its start address field
+                // (bytes / 16) by a constant
+                const uint64_t bdesc = desc_sw128(smem_u32(ring + (r % kRing) * kPageBytes), 0, 1024);
+                const uint32_t d = tmem + kTmemS + 64u * (uint32_t)buf;
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
+                for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ts(d, tmem + kTmemQ + 32u * c + 8u * kk, bdesc + (uint64_t)((c * kChunkBytes + 32 * kk) >> 4),
-                                idesc_s, (c | kk) != 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ts(d, tmem + kTmemQ + 32u * c + 8u * kk,
+                                    bdesc + (uint64_t)((c * kChunkBytes + 32 * kk) >> 4), idesc_s,
+                                    (c | kk) != 0 ? 1u : 0u);
+                }
+                mma_commit(&bars->ring_empty[r % kRing]);
+                mma_commit(&bars->s_full[buf]);
             }
-            mma_commit(&bars->ring_empty[r % kRing]);
-            mma_commit(&bars->s_full[buf]);
-            if (pi.last_of_item()) mma_commit(&bars->q_drained);
+            __syncwarp();
+            issued = true;
         }
+        // both warps report when their products of the item no longer read the query
+        if (pi.last_of_item() && lane == 0) mma_commit(&bars->q_drained);
         __syncwarp();
-        issued = true;
         ++r;
     }
     // every MMA this warp issued has completed before TMEM is freed
     if (issued) {
-        if (lane == 0) mma_commit(&bars->drain);
+        if (lane == 0) mma_commit(drain);
         __syncwarp();
-        warp_wait(&bars->drain, 0, nullptr, err, kDrainNs);
+        warp_wait(drain, 0, nullptr, err, kDrainNs);
     }
     return ok;
 }
 
+// Softmax of the score CTA. Two groups of eight warps take alternate pages of
+// the part (group g the pages with n % 2 == g); in a group, the two warps of a
+// TMEM lane quadrant share its 32 rows, each taking 32 of the page's 64 keys.
+// The online softmax needs one reference max per row for the whole item (O
+// accumulates P . V with P taken relative to it), so the reference max moves
+// along the page chain: the group of page n reads the value after page n - 1
+// (published by the other group), decides whether the row max of page n moves
+// it (lazily: only by more than 2^8) and publishes the value after page n.
+// Each group keeps its own share of the row sum; at an item's end the group
+// without the last page publishes its share, and the group with it adds both
+// for 1/l and lse.
 __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem, uint32_t tmem, int part, int s,
                               uint32_t peer, volatile int* abort) {
     int* err = args.err;
     const long long wait_ns = args.wait_ns;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int quad = warp & 3, half = warp >> 2;
+    const int g = warp >> 3;  // page parity of this group
+    const int quad = warp & 3, half = (warp >> 2) & 1;
     const int row = quad * 32 + lane;
-    const int pair_bar = 1 + quad;  // named barrier of the two warps sharing these rows
+    const int pair_bar = 1 + 4 * g + quad;  // named barrier of the two warps of this group sharing these rows
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     uint8_t* ring = smem + kOffRing;
     // the value CTA's P slots, factor arrays and P barriers (same offsets there)
     const uint32_t p_remote = mapa_shared(smem_u32(smem + kOffP), peer);
     const uint32_t x_remote = mapa_shared(smem_u32(smem + kOffX), peer);
     const uint32_t pfull_remote = mapa_shared(smem_u32(&bars->p_full[0]), peer);
-    float* xch = reinterpret_cast<float*>(smem + kOffX);  // [2 episodes][2 halves][128 rows]
-    // this thread's query row inside the two 64-row query boxes
+    float* xf = reinterpret_cast<float*>(smem + kOffX);
+    float* xpair = xf + kXPair + g * (2 * 2 * kRows);  // this group's [episode][half][128]
+    float* xref = xf + kXRef;                          // [page parity][128]
+    float* xlsum = xf + kXLSum;                        // [group][half][128]
+    float* xlmax = xf + kXLMax;                        // [group][128]
+    // this thread's query row inside the two 64-row query boxes, and the query
+    // chunks this warp moves into TMEM (the four warps of a quadrant share them)
     const int qbox = quad >> 1, qrow = 32 * (quad & 1) + lane;
+    const int qpart = 2 * g + half;
     PageIter pi;
     pi.init(args, part);
-    float m = -INFINITY, l = 0.f;
+    float m_own = -INFINITY, l = 0.f;  // this thread's share of the row sum, relative to m_own
     int n_valid = 0, xe = 0, r = 0;
     bool ok = true;
     for (; pi.valid; pi.advance()) {
         // every exit goes through a pair barrier, so both warps of a pair leave together
-        const int n = pi.n, buf = n & 1, k = n & 1, qi = pi.n_items - 1;
+        const int n = pi.n, buf = n & 1, qi = pi.n_items - 1;
         const bool first = pi.first_of_item(), last = pi.last_of_item();
         if (first) {
-            m = -INFINITY;
+            m_own = -INFINITY;
             l = 0.f;
             n_valid = visible_keys(pi.it.seqlen, args.s_q, s, args.causal);
-            // the batch's query into TMEM: row -> lane, this warp's chunks
-            // (half 0: chunks 0-4, half 1: chunks 5-8), once the previous
-            // batch's last score product has stopped reading the old one
+            // the batch's query into TMEM (row -> lane), once the previous
+            // batch's last score products have stopped reading the old one
             if (ok && qi > 0) ok = warp_wait(&bars->q_drained, (qi - 1) & 1, abort, err, wait_ns);
             const int rq = r + qbox;
             if (ok) ok = warp_wait(&bars->ring_full[rq % kRing], (rq / kRing) & 1, abort, err, wait_ns);
@@ -378,9 +424,8 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
                 tc_fence_after();
                 const bool have = qrow < args.qrows;  // fewer than 64 query rows in the whole call
                 const uint8_t* src = ring + (rq % kRing) * kPageBytes + qrow * 128;
-                const int c0 = half ? 5 : 0, c1 = half ? kChunks : 5;
 #pragma unroll 1
-                for (int c = c0; c < c1; ++c) {
+                for (int c = qpart; c < kChunks; c += 4) {
                     uint32_t v[32];
 #pragma unroll
                     for (int w = 0; w < 8; ++w) {
@@ -399,9 +444,21 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
                 tc_fence_before();
                 mbar_arrive(&bars->q_full);
             }
+            // both groups pass an item start together, so neither runs an item ahead
+            if (ok) ok = warp_wait(&bars->q_full, qi & 1, abort, err, wait_ns);
             r += 2;
         }
         ++r;
+        if (buf != g) {
+            // the other group's page; at the item's last page, hand over this
+            // group's share of the row sum (complete: its last page was n - 1)
+            if (last) {
+                xlsum[(g * 2 + half) * kRows + row] = l;
+                if (half == 0) xlmax[g * kRows + row] = m_own;
+                mbar_arrive(&bars->lsum_full[quad]);
+            }
+            continue;
+        }
         float x[32];
         if (ok) ok = warp_wait(&bars->s_full[buf], (n >> 1) & 1, abort, err, wait_ns);
         if (ok) {
@@ -423,21 +480,33 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
             x[c] = c < vcount ? x[c] : -INFINITY;
             mh = fmaxf(mh, x[c]);
         }
-        float* xb = xch + (xe & 1) * (2 * kRows);
+        float* xb = xpair + (xe & 1) * (2 * kRows);
         ++xe;
         xb[half * kRows + row] = mh;
         ok = barrier_and(pair_bar, 64, ok);
         if (!ok) break;
         const float mx = fmaxf(mh, xb[(half ^ 1) * kRows + row]);
+        // the reference max before this page: none at an item's first page,
+        // else the value the other group published after page n - 1
+        float m_prev = -INFINITY;
+        if (!first) {
+            ok = warp_wait(&bars->ref_full[buf ^ 1][quad], ((n - 1) >> 1) & 1, abort, err, wait_ns);
+            m_prev = xref[(buf ^ 1) * kRows + row];
+        }
         // lazy rescale: the reference max moves only when the row max exceeds it
         // by more than 2^8; both warps of a pair take the same decision
-        const bool need = mx > m + kRescaleThreshold;
-        const float alpha = need ? fast_exp2(m - mx) : 1.f;  // 0 when m = -inf
-        if (need) {
-            l *= alpha;
-            m = mx;
+        const bool need = mx > m_prev + kRescaleThreshold;
+        const float m_new = need ? mx : m_prev;
+        const float alpha = need ? fast_exp2(m_prev - mx) : 1.f;  // 0 when m_prev = -inf
+        if (half == 0) {
+            xref[buf * kRows + row] = m_new;
+            mbar_arrive(&bars->ref_full[buf][quad]);
         }
-        const float m_use = m == -INFINITY ? 0.f : m;
+        if (m_new != m_own) {
+            if (l > 0.f) l *= fast_exp2(m_own - m_new);
+            m_own = m_new;
+        }
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
@@ -446,36 +515,41 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
             l += p0 + p1;
             pk[c] = pack_bf16x2(p0, p1);
         }
-        // slot k held page n - 2 until the value CTA released it
-        if (ok && n >= 2) ok = warp_wait(&bars->p_free[k], ((n >> 1) - 1) & 1, abort, err, wait_ns);
-        const uint32_t mbar = pfull_remote + (uint32_t)k * 8u;
+        // slot buf held page n - 2 until the value CTA released it
+        if (ok && n >= 2) ok = warp_wait(&bars->p_free[buf], ((n >> 1) - 1) & 1, abort, err, wait_ns);
+        const uint32_t mbar = pfull_remote + (uint32_t)buf * 8u;
         if (ok) {
             // row `row`, keys [32 half, 32 half + 32): 16-byte words 4 half .. 4 half + 3,
             // word w stored at position w ^ (row % 8)
-            const uint32_t dst = p_remote + (uint32_t)(k * kPSlotBytes + row * 128);
+            const uint32_t dst = p_remote + (uint32_t)(buf * kPSlotBytes + row * 128);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 st_async_u4(dst + (uint32_t)(((4 * half + q) ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1],
                             pk[4 * q + 2], pk[4 * q + 3], mbar);
             if (half == 0)
-                st_async_b32(x_remote + (uint32_t)(k * 1024 + row * 4), __float_as_uint(row < args.H ? alpha : 1.f),
+                st_async_b32(x_remote + (uint32_t)(buf * 1024 + row * 4), __float_as_uint(row < args.H ? alpha : 1.f),
                              mbar);
         }
         if (last) {
-            // the pair adds its two half sums (half 0 + half 1) for 1/l and lse
-            xb = xch + (xe & 1) * (2 * kRows);
+            // the pair adds its two half sums (half 0 + half 1), then the other
+            // group's share, moved to this reference max
+            xb = xpair + (xe & 1) * (2 * kRows);
             ++xe;
             xb[half * kRows + row] = l;
             ok = barrier_and(pair_bar, 64, ok);
             if (!ok) break;
             const float lo = xb[(half ^ 1) * kRows + row];
-            const float l_row = half == 0 ? l + lo : lo + l;
-            if (half == 0) {
+            const float l_pair = half == 0 ? l + lo : lo + l;
+            if (ok) ok = warp_wait(&bars->lsum_full[quad], qi & 1, abort, err, wait_ns);
+            const float l_oth = xlsum[((g ^ 1) * 2) * kRows + row] + xlsum[((g ^ 1) * 2 + 1) * kRows + row];
+            const float m_oth = xlmax[(g ^ 1) * kRows + row];
+            const float l_row = l_pair + (l_oth > 0.f ? l_oth * fast_exp2(m_oth - m_new) : 0.f);
+            if (ok && half == 0) {
                 const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
-                st_async_b32(x_remote + (uint32_t)(k * 1024 + 512 + row * 4), __float_as_uint(inv_l), mbar);
+                st_async_b32(x_remote + (uint32_t)(buf * 1024 + 512 + row * 4), __float_as_uint(inv_l), mbar);
                 if (row < args.H) {
                     // lse in natural log: x is in log2 units of the scaled score
-                    const float lse_v = l_row > 0.f ? (m + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
+                    const float lse_v = l_row > 0.f ? (m_new + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
                     if (pi.it.split)
                         args.lse_part[((size_t)pi.it.piece * args.s_q + s) * args.H + row] = lse_v;
                     else
@@ -483,7 +557,7 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
                 }
             }
         } else if (ok && half == 0) {
-            st_async_b32(x_remote + (uint32_t)(k * 1024 + 512 + row * 4), 0u, mbar);
+            st_async_b32(x_remote + (uint32_t)(buf * 1024 + 512 + row * 4), 0u, mbar);
         }
     }
     return ok;
@@ -497,7 +571,7 @@ __device__ void value_producer(const DecodeMaps& maps, const DecodeArgs& args, B
     uint8_t* vring = smem + kOffV;
     PageIter pi;
     pi.init(args, part);
-    bool ok = true;
+    bool ok = !args.withhold;  // test hook: issue nothing, so that the P.V warp's first wait runs out
     int v = 0;
     for (; ok && pi.valid; pi.advance()) {
         if (v >= kVRing) ok = mbar_wait(&bars->v_empty[v % kVRing], ((v / kVRing) - 1) & 1, abort, err, wait_ns);
@@ -659,25 +733,24 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
                 const int chunk = (cpr / 2) * half + cc;
                 uint8_t* dst = stage + chunk * hrows * 128 + row * 128;
                 if (!it.split) {
-                    const uint32_t col = (uint32_t)(64 * (cpr * rnd + chunk));  // absolute O column
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32(tmem + lane_base + col, v0);
-                    tmem_ld32(tmem + lane_base + col + 32, v1);
-                    tmem_wait_ld();
-                    if (row_ok) {
+                    // 64 bf16 columns = one 128-byte row, read from TMEM 32 columns
+                    // (four 16-byte words) at a time
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint32_t col = (uint32_t)(64 * (cpr * rnd + chunk) + 32 * hh);  // absolute O column
+                        uint32_t v0[32];
+                        tmem_ld32(tmem + lane_base + col, v0);
+                        tmem_wait_ld();
+                        if (row_ok) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 w0, w1;
-                            w0.x = pack_bf16x2(__uint_as_float(v0[8 * q + 0]) * inv_l, __uint_as_float(v0[8 * q + 1]) * inv_l);
-                            w0.y = pack_bf16x2(__uint_as_float(v0[8 * q + 2]) * inv_l, __uint_as_float(v0[8 * q + 3]) * inv_l);
-                            w0.z = pack_bf16x2(__uint_as_float(v0[8 * q + 4]) * inv_l, __uint_as_float(v0[8 * q + 5]) * inv_l);
-                            w0.w = pack_bf16x2(__uint_as_float(v0[8 * q + 6]) * inv_l, __uint_as_float(v0[8 * q + 7]) * inv_l);
-                            w1.x = pack_bf16x2(__uint_as_float(v1[8 * q + 0]) * inv_l, __uint_as_float(v1[8 * q + 1]) * inv_l);
-                            w1.y = pack_bf16x2(__uint_as_float(v1[8 * q + 2]) * inv_l, __uint_as_float(v1[8 * q + 3]) * inv_l);
-                            w1.z = pack_bf16x2(__uint_as_float(v1[8 * q + 4]) * inv_l, __uint_as_float(v1[8 * q + 5]) * inv_l);
-                            w1.w = pack_bf16x2(__uint_as_float(v1[8 * q + 6]) * inv_l, __uint_as_float(v1[8 * q + 7]) * inv_l);
-                            *reinterpret_cast<uint4*>(dst + ((q ^ (row & 7)) << 4)) = w0;
-                            *reinterpret_cast<uint4*>(dst + (((q + 4) ^ (row & 7)) << 4)) = w1;
+                            for (int q = 0; q < 4; ++q) {
+                                uint4 w0;
+                                w0.x = pack_bf16x2(__uint_as_float(v0[8 * q + 0]) * inv_l, __uint_as_float(v0[8 * q + 1]) * inv_l);
+                                w0.y = pack_bf16x2(__uint_as_float(v0[8 * q + 2]) * inv_l, __uint_as_float(v0[8 * q + 3]) * inv_l);
+                                w0.z = pack_bf16x2(__uint_as_float(v0[8 * q + 4]) * inv_l, __uint_as_float(v0[8 * q + 5]) * inv_l);
+                                w0.w = pack_bf16x2(__uint_as_float(v0[8 * q + 6]) * inv_l, __uint_as_float(v0[8 * q + 7]) * inv_l);
+                                *reinterpret_cast<uint4*>(dst + (((q + 4 * hh) ^ (row & 7)) << 4)) = w0;
+                            }
                         }
                     }
                 } else {
@@ -758,9 +831,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->ring_full[i], 1);
             mbar_init(&bars->ring_empty[i], 1);
         }
-        mbar_init(&bars->q_full, 256);
-        mbar_init(&bars->q_drained, 1);
+        mbar_init(&bars->q_full, 32 * kSoftmaxWarps);
+        mbar_init(&bars->q_drained, 2);
         for (int i = 0; i < 2; ++i) {
+            for (int q = 0; q < 4; ++q) mbar_init(&bars->ref_full[i][q], 32);
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->s_free[i], 256);
             mbar_init(&bars->p_free[i], 1);
@@ -774,9 +848,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bars->pv_done, 1);
         mbar_init(&bars->o_full, 1);
-        mbar_init(&bars->stage_full, 8);
+        for (int q = 0; q < 4; ++q) mbar_init(&bars->lsum_full[q], 64);
+        mbar_init(&bars->stage_full, kOWarps);
         mbar_init(&bars->stage_free, 1);
         mbar_init(&bars->drain, 1);
+        mbar_init(&bars->drain2, 1);
         bars->abort = 0;
         bars->p_consumed = 0;
         fence_mbarrier_init_cluster();
@@ -810,8 +886,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (rank == 0) {
         if (warp == kWarpProducer) {
             score_producer(maps, args, bars, smem, part, s, abort);
-        } else if (warp == kWarpMma) {
-            ok = score_mma(args, bars, smem, tmem, part, abort);
+        } else if (warp == kWarpMma || warp == kWarpMma2) {
+            ok = score_mma(args, bars, smem, tmem, part, warp == kWarpMma ? 0 : 1, abort);
         } else {
             ok = score_softmax(args, bars, smem, tmem, part, s, peer, abort);
         }
@@ -820,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((threadIdx.x & 31) == 0) value_producer(maps, args, bars, smem, part, abort);
         } else if (warp == kWarpMma) {
             ok = value_mma(args, bars, smem, tmem, part, abort);
-        } else {
+        } else if (warp < kOWarps) {
             ok = value_owarps(maps, args, bars, smem, tmem, part, s, abort);
         }
     }

@@ -63,6 +63,7 @@ struct DecodeArgs {
     float* lse_part;   // [P, s_q, H]
     int* err;
     long long wait_ns;
+    int withhold;      // test hook: the value CTA never loads its first page (its consumer's wait runs out)
 };
 cudaError_t gemm_error_fetch(int* out, cudaStream_t stream);
 int decode_max_active_clusters(int device);
@@ -82,6 +83,11 @@ struct DecodeMaps {
     CUtensorMap kv, v, q, o, op;
 };
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, cudaStream_t stream);
+
+cudaError_t launch_rope_append(void* q, const void* kv_new, const int32_t* seqlens, const int32_t* block_table,
+                               int mbps, void* kv_cache, int num_blocks, int B, int s_q, int H, double base,
+                               cudaStream_t stream);
+cudaError_t rope_error_fetch(int* out, cudaStream_t stream);
 
 cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, const float* o_part,
                            const float* lse_part, void* o_lat, float* lse, cudaStream_t stream);

@@ -80,7 +80,11 @@ def test_bad_arguments_are_rejected_on_the_host(L):
     assert L.mla_decode_paged(null, null, 1, null, 1, null, 1, 1, 128, null, null, 1, ctypes.c_float(0.1), 1,
                               null, null, null, 0, null) == 1
     assert L.mla_debug_mma(null, null, 64, 64, 1, 0, null, null) == 1
-    assert L.mla_read_device_error(null, null) == 1
+    assert L.mla_rope_append(null, null, null, null, 1, null, 1, 1, 1, 128, ctypes.c_float(10000.0), null) == 1
+    buf = ctypes.create_string_buffer(64)
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    # a rope base that is not > 1
+    assert L.mla_rope_append(p, p, p, p, 1, p, 1, 1, 1, 128, ctypes.c_float(1.0), null) == 1
 
 
 def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -75,14 +75,42 @@ def test_split_kv_and_combine(api, s_q, num_parts):
     check_decode(inp, r)
 
 
+def qabs_rounding_bound(inp, qa_exact, qa_gpu):
+    """Per query row, a bound on how far the scores (hence lse, which moves by
+    at most the largest score change) can move because the path rounds the
+    absorbed query to bf16: scale * sum_c |qa_exact - qa_gpu|[c] * max_t |kv_t[c]|
+    over the row's visible keys."""
+    kv = inp.kv_cache.float().numpy().astype(np.float64)
+    dq = np.abs(qa_exact - f32(qa_gpu).astype(np.float64))
+    B, s_q, H, _ = dq.shape
+    bound = np.zeros((B, s_q, H))
+    for b in range(B):
+        L = int(inp.seqlens[b])
+        for s in range(s_q):
+            n = max(0, min(L, L - s_q + s + 1)) if inp.causal else L
+            if n == 0:
+                continue
+            rows = [int(inp.block_table[b, t // 64]) * 64 + t % 64 for t in range(n)]
+            kmax = np.abs(kv.reshape(-1, 576)[rows]).max(0)
+            bound[b, s] = inp.scale * (dq[b, s] * kmax).sum(-1)
+    return bound
+
+
 def test_tiny_end_to_end(api):
+    """End to end from q, W_UK and W_UV: q_abs and the projected output within
+    the stated tolerances of the oracle's unrounded fp64 chain; lse within the
+    decode tolerance plus the movement the bf16 absorbed query alone allows
+    (the tolerance applies to the decode's lse, which check_decode holds to
+    1e-3 on the query the decode consumed)."""
     inp = gen.make_workload("tiny")
     r = run(api, inp)
     check_decode(inp, r)
     qa, o, lse, out = oracle_end_to_end(inp)
     assert_o_close(r["q_abs"], qa, "q_abs")
     assert_o_close(r["out"], out, "out")
-    assert_lse_close(r["lse"], lse, "lse (end to end)")
+    bound = qabs_rounding_bound(inp, qa, r["q_abs"]) + 1e-3
+    err = np.abs(f32(r["lse"]).astype(np.float64) - lse)
+    assert np.all(err <= bound), f"lse (end to end): max excess {float((err - bound).max()):.3e}"
 
 
 def test_empty_and_fully_masked_rows(api):
@@ -231,29 +259,35 @@ def test_mispaired_schedule_reports_bad_block_promptly(api):
     check_decode(inp, run(api, inp, 4))
 
 
-@pytest.mark.parametrize("limit_ns", [100, 1000])
-def test_bounded_wait_expiry_returns_timeout(api, limit_ns):
-    """With a wait limit far below the latency of a TMA load, the first
-    pipeline wait of each cluster runs out: the kernel records
-    MLA_ERR_TIMEOUT, tells the peer CTA, drains its copies and MMAs, frees its
-    tensor memory and returns. Afterwards, with the default limit restored, the
-    same call matches the oracle."""
-    inp = gen.make_workload("tiny")
-    check_decode(inp, run(api, inp))
+@pytest.mark.parametrize("name", ["tiny", "dsv3"])
+def test_bounded_wait_expiry_returns_timeout(api, name):
+    """A wait that nothing will ever satisfy runs out: with the value CTA's
+    first page load withheld (a test hook; no fault, nothing out of bounds), the
+    P.V warp's wait expires after the limit, the kernel records
+    MLA_ERR_TIMEOUT, aborts both CTAs of every cluster with work, drains its
+    copies and MMAs, frees its tensor memory and returns. Afterwards, with the
+    default limit and the hook off, the same call matches the oracle."""
+    inp = gen.make_workload(name)
     d = inp.to("cuda")
     tm, ns = api.mla_get_metadata(d.seqlens, d.s_q, d.H)
     q_abs = api.mla_absorb_q(d.q, d.w_uk)
     ws = api.make_workspace(d.B, d.s_q, d.H, tm.shape[0])
-    torch.cuda.synchronize()
-    api.mla_set_wait_limit_ns(limit_ns)
+    api.mla_decode_paged(q_abs, d.kv_cache, d.block_table, d.seqlens, tm, ns, d.scale, d.causal, workspace=ws)
+    assert api.mla_read_device_error(ws) == 0
+    api.mla_set_wait_limit_ns(20_000_000)  # 20 ms
+    api.mla_debug_withhold_value_load(True)
     try:
         t0 = time.perf_counter()
         api.mla_decode_paged(q_abs, d.kv_cache, d.block_table, d.seqlens, tm, ns, d.scale, d.causal, workspace=ws)
         status = api.mla_read_device_error(ws)
         dt = time.perf_counter() - t0
     finally:
+        api.mla_debug_withhold_value_load(False)
         api.mla_set_wait_limit_ns(0)
     assert status == api.MLA_ERR_TIMEOUT
     assert dt < 1.0, f"took {dt:.3f} s"
-    for _ in range(3):
-        check_decode(inp, run(api, inp))
+    for _ in range(2):
+        o, lse = api.mla_decode_paged(q_abs, d.kv_cache, d.block_table, d.seqlens, tm, ns, d.scale, d.causal,
+                                      workspace=ws)
+        assert api.mla_read_device_error(ws) == 0
+        check_decode(inp, {"q_abs": q_abs.cpu(), "o": o.cpu(), "lse": lse.cpu(), "status": 0})
