@@ -114,7 +114,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
         ok = __syncthreads_and(mbar_wait(full, kc & 1, nullptr, nullptr, 2000000000LL));
         tc_fence_after();
-        if (ok && threadIdx.x == 0) {
+        if (ok && warp == 0) {
+            // the whole warp runs the issue code; one elected lane issues
             const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
             if (a_tmem == 2) {
                 // the A tile goes from shared to tensor memory on the tensor pipe

@@ -34,9 +34,8 @@
 // Roles (19 warps per CTA). Score CTA: warps 0-15 softmax in two groups of
 // eight that take alternate pages (page n goes to group n % 2), two warps of a
 // group per TMEM lane quadrant, warp half h owning keys [32 h, 32 h + 32) of a
-// page; warp 16 TMA producer; warps 17 and 18 issue the score products of the
-// even and odd pages (one issuing warp alone cannot keep the tensor pipe busy
-// with N = 64 products); warp 17 owns TMEM. Value CTA: warps 0-7 O rescale and
+// page; warp 16 TMA producer; warp 17 issues the score products and owns
+// TMEM (warp 18 can take the odd pages: kScoreMmaWarps). Value CTA: warps 0-7 O rescale and
 // epilogue, two per lane quadrant, warp half h owning O columns
 // [256 h, 256 h + 256); warp 16 TMA producer; warp 17 P.V issuer and TMEM
 // owner; the other warps have no role.
@@ -59,11 +58,19 @@ namespace {
 // pages; idle on the value CTA).
 constexpr int kThreads = 608;
 constexpr int kRows = 128;
-constexpr int kSoftmaxWarps = 16;
+// Softmax groups on the score CTA: 2 (warps 0-15, alternate pages) or 1
+// (warps 0-7 take every page; 8-15 have no role).
+constexpr int kSoftmaxGroups = 2;
+constexpr int kSoftmaxWarps = 8 * kSoftmaxGroups;
 constexpr int kOWarps = 8;
 constexpr int kWarpProducer = 16;
 constexpr int kWarpMma = 17;
 constexpr int kWarpMma2 = 18;
+// Score-MMA issuing warps: 1 (warp 17 issues every page) or 2 (warps 17 and
+// 18 take the even and odd pages). Issued warp-uniformly, one warp keeps the
+// tensor pipe at its N = 64 rate (about 33 cycles a product), and one issuer
+// finishes each page's products soonest, which frees its ring slot soonest.
+constexpr int kScoreMmaWarps = 1;
 constexpr int kChunks = kDQK / 64;  // 9 chunks of 64 dims
 
 // ---- shared memory (offsets from a 1024-byte-aligned base) ----
@@ -87,12 +94,14 @@ constexpr int kSmemScore = kOffRing + kRing * kPageBytes;
 constexpr int kPSlotBytes = kRows * 128;           // P of a page: [128 rows x 64 keys] bf16
 constexpr int kVBytes = 8 * kChunkBytes;           // a page's value columns: [8 chunks][64 keys][64 dims]
 constexpr int kVRing = 2;
-constexpr int kOffP = kOffRole;
-constexpr int kOffV = kOffP + 2 * kPSlotBytes;
+constexpr int kOffXV = kOffX;                      // value: [P slot][rescale factor 128 | 1/l 128] fp32
+constexpr int kOffP = kOffRole;                    // value: two P slots
+constexpr int kOffV = kOffP + 2 * kPSlotBytes;     // value: the value ring
 constexpr int kSmemValue = kOffV + kVRing * kVBytes;
 constexpr int kSmemUsed = kSmemScore > kSmemValue ? kSmemScore : kSmemValue;
 constexpr int kSmemBytes = kSmemUsed + 1024;       // room to align the base to 1024 bytes
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(kOffP % 1024 == 0 && kOffV % 1024 == 0 && kOffRing % 1024 == 0, "swizzle atoms");
 // one P message: P (16 KB) + rescale factor and 1/l per row (fp32)
 constexpr uint32_t kPMsgBytes = kPSlotBytes + 2 * kRows * 4;
 
@@ -299,9 +308,9 @@ __device__ void score_producer(const DecodeMaps& maps, const DecodeArgs& args, B
     __syncwarp();
 }
 
-// Score products of the pages with parity `parity` (two warps issue them, one
-// per parity, so that the tensor pipe sees two instruction streams). Returns
-// false when it gave up (timeout or abort).
+// Score products of the pages with parity `parity` (0 or 1, when two warps
+// share the pages), or of every page (parity < 0). Returns false when it gave
+// up (timeout or abort).
 __device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uint32_t tmem, int part, int parity,
                           volatile int* abort) {
     int* err = args.err;
@@ -309,7 +318,7 @@ __device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
     const int lane = threadIdx.x & 31;
     uint8_t* ring = smem + kOffRing;
     constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kPage, false, false);
-    uint64_t* drain = parity == 0 ? &bars->drain : &bars->drain2;
+    uint64_t* drain = parity <= 0 ? &bars->drain : &bars->drain2;
     PageIter pi;
     pi.init(args, part);
     bool ok = true, issued = false;
@@ -321,47 +330,42 @@ __device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
             // done reading its two ring slots
             ok = warp_wait(&bars->q_full, qi & 1, abort, err, wait_ns);
             if (!ok) break;
-            if (parity == 0 && lane == 0) {
+            if (parity <= 0 && lane == 0) {
                 mbar_arrive(&bars->ring_empty[r % kRing]);
                 mbar_arrive(&bars->ring_empty[(r + 1) % kRing]);
             }
             __syncwarp();
             r += 2;
         }
-        if (buf == parity) {
+        if (parity < 0 || buf == parity) {
             // S buffer `buf` was read by the softmax of page n - 2
             if (n >= 2) ok = warp_wait(&bars->s_free[buf], ((n >> 1) - 1) & 1, abort, err, wait_ns);
             if (ok) ok = warp_wait(&bars->ring_full[r % kRing], (r / kRing) & 1, abort, err, wait_ns);
             if (!ok) break;
             tc_fence_after();
-            if (lane == 0) {
-                // one descriptor per page; a K-step moves its start address field
-                // (bytes / 16) by a constant
-                const uint64_t bdesc = desc_sw128(smem_u32(ring + (r % kRing) * kPageBytes), 0, 1024);
-                const uint32_t d = tmem + kTmemS + 64u * (uint32_t)buf;
+            // the whole warp runs the issue loop (warp-uniform operands); one
+            // elected lane issues. One descriptor per page; a K-step moves its
+            // start address field (bytes / 16) by a constant.
+            const uint64_t bdesc = desc_sw128(smem_u32(ring + (r % kRing) * kPageBytes), 0, 1024);
+            const uint32_t d = tmem + kTmemS + 64u * (uint32_t)buf;
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c) {
+            for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ts(d, tmem + kTmemQ + 32u * c + 8u * kk,
-                                    bdesc + (uint64_t)((c * kChunkBytes + 32 * kk) >> 4), idesc_s,
-                                    (c | kk) != 0 ? 1u : 0u);
-                }
-                mma_commit(&bars->ring_empty[r % kRing]);
-                mma_commit(&bars->s_full[buf]);
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ts(d, tmem + kTmemQ + 32u * c + 8u * kk, bdesc + (uint64_t)((c * kChunkBytes + 32 * kk) >> 4),
+                                idesc_s, (c | kk) != 0 ? 1u : 0u);
             }
-            __syncwarp();
+            mma_commit(&bars->ring_empty[r % kRing]);
+            mma_commit(&bars->s_full[buf]);
             issued = true;
         }
         // both warps report when their products of the item no longer read the query
-        if (pi.last_of_item() && lane == 0) mma_commit(&bars->q_drained);
-        __syncwarp();
+        if (pi.last_of_item()) mma_commit(&bars->q_drained);
         ++r;
     }
     // every MMA this warp issued has completed before TMEM is freed
     if (issued) {
-        if (lane == 0) mma_commit(drain);
-        __syncwarp();
+        mma_commit(drain);
         warp_wait(drain, 0, nullptr, err, kDrainNs);
     }
     return ok;
@@ -391,7 +395,7 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
     uint8_t* ring = smem + kOffRing;
     // the value CTA's P slots, factor arrays and P barriers (same offsets there)
     const uint32_t p_remote = mapa_shared(smem_u32(smem + kOffP), peer);
-    const uint32_t x_remote = mapa_shared(smem_u32(smem + kOffX), peer);
+    const uint32_t x_remote = mapa_shared(smem_u32(smem + kOffXV), peer);
     const uint32_t pfull_remote = mapa_shared(smem_u32(&bars->p_full[0]), peer);
     float* xf = reinterpret_cast<float*>(smem + kOffX);
     float* xpair = xf + kXPair + g * (2 * 2 * kRows);  // this group's [episode][half][128]
@@ -401,7 +405,7 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
     // this thread's query row inside the two 64-row query boxes, and the query
     // chunks this warp moves into TMEM (the four warps of a quadrant share them)
     const int qbox = quad >> 1, qrow = 32 * (quad & 1) + lane;
-    const int qpart = 2 * g + half;
+    const int qpart = kSoftmaxGroups == 2 ? 2 * g + half : half;  // the quadrant's warps split the 9 chunks
     PageIter pi;
     pi.init(args, part);
     float m_own = -INFINITY, l = 0.f;  // this thread's share of the row sum, relative to m_own
@@ -425,7 +429,7 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
                 const bool have = qrow < args.qrows;  // fewer than 64 query rows in the whole call
                 const uint8_t* src = ring + (rq % kRing) * kPageBytes + qrow * 128;
 #pragma unroll 1
-                for (int c = qpart; c < kChunks; c += 4) {
+                for (int c = qpart; c < kChunks; c += 2 * kSoftmaxGroups) {
                     uint32_t v[32];
 #pragma unroll
                     for (int w = 0; w < 8; ++w) {
@@ -449,7 +453,7 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
             r += 2;
         }
         ++r;
-        if (buf != g) {
+        if (kSoftmaxGroups == 2 && buf != g) {
             // the other group's page; at the item's last page, hand over this
             // group's share of the row sum (complete: its last page was n - 1)
             if (last) {
@@ -540,10 +544,13 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
             if (!ok) break;
             const float lo = xb[(half ^ 1) * kRows + row];
             const float l_pair = half == 0 ? l + lo : lo + l;
-            if (ok) ok = warp_wait(&bars->lsum_full[quad], qi & 1, abort, err, wait_ns);
-            const float l_oth = xlsum[((g ^ 1) * 2) * kRows + row] + xlsum[((g ^ 1) * 2 + 1) * kRows + row];
-            const float m_oth = xlmax[(g ^ 1) * kRows + row];
-            const float l_row = l_pair + (l_oth > 0.f ? l_oth * fast_exp2(m_oth - m_new) : 0.f);
+            float l_row = l_pair;
+            if (kSoftmaxGroups == 2) {
+                if (ok) ok = warp_wait(&bars->lsum_full[quad], qi & 1, abort, err, wait_ns);
+                const float l_oth = xlsum[((g ^ 1) * 2) * kRows + row] + xlsum[((g ^ 1) * 2 + 1) * kRows + row];
+                const float m_oth = xlmax[(g ^ 1) * kRows + row];
+                l_row += l_oth > 0.f ? l_oth * fast_exp2(m_oth - m_new) : 0.f;
+            }
             if (ok && half == 0) {
                 const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
                 st_async_b32(x_remote + (uint32_t)(buf * 1024 + 512 + row * 4), __float_as_uint(inv_l), mbar);
@@ -631,7 +638,8 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
             __syncwarp();
         }
         tc_fence_after();
-        if (lane == 0) {
+        {
+            // whole warp, one elected lane issues
             const uint64_t adesc = desc_sw128(smem_u32(smem + kOffP + k * kPSlotBytes), 0, 1024);
             const uint64_t vdesc = desc_sw128(smem_u32(vs), kChunkBytes, 1024);
 #pragma unroll
@@ -649,12 +657,10 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
             if (last) mma_commit(&bars->o_full);
             mma_commit_multicast(&bars->p_free[k], (uint16_t)1u);  // arrives on the score CTA (rank 0)
         }
-        __syncwarp();
         issued = true;
     }
     if (issued) {
-        if (lane == 0) mma_commit(&bars->drain);
-        __syncwarp();
+        mma_commit(&bars->drain);
         warp_wait(&bars->drain, 0, nullptr, err, kDrainNs);
     }
     if (lane == 0) bars->p_consumed = consumed;
@@ -669,7 +675,7 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
     const int quad = warp & 3, half = warp >> 2;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const float* xv = reinterpret_cast<const float*>(smem + kOffX);  // [slot][factor 128 | 1/l 128]
+    const float* xv = reinterpret_cast<const float*>(smem + kOffXV);  // [slot][factor 128 | 1/l 128]
     const uint32_t ocol = tmem + lane_base + 256u * (uint32_t)half;
     PageIter pi;
     pi.init(args, part);
@@ -832,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->ring_empty[i], 1);
         }
         mbar_init(&bars->q_full, 32 * kSoftmaxWarps);
-        mbar_init(&bars->q_drained, 2);
+        mbar_init(&bars->q_drained, kScoreMmaWarps);
         for (int i = 0; i < 2; ++i) {
             for (int q = 0; q < 4; ++q) mbar_init(&bars->ref_full[i][q], 32);
             mbar_init(&bars->s_full[i], 1);
@@ -886,9 +892,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (rank == 0) {
         if (warp == kWarpProducer) {
             score_producer(maps, args, bars, smem, part, s, abort);
-        } else if (warp == kWarpMma || warp == kWarpMma2) {
-            ok = score_mma(args, bars, smem, tmem, part, warp == kWarpMma ? 0 : 1, abort);
-        } else {
+        } else if (warp == kWarpMma) {
+            ok = score_mma(args, bars, smem, tmem, part, kScoreMmaWarps == 1 ? -1 : 0, abort);
+        } else if (warp == kWarpMma2) {
+            if (kScoreMmaWarps == 2) ok = score_mma(args, bars, smem, tmem, part, 1, abort);
+        } else if (warp < kSoftmaxWarps) {
             ok = score_softmax(args, bars, smem, tmem, part, s, peer, abort);
         }
     } else {

@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = warp_wait(&full[s], (kc / STAGES) & 1, abort, err, wait_ns);
             if (!ok) break;
             tc_fence_after();
-            if (lane == 0) {
+            {
+                // whole warp, one elected lane issues (warp-uniform operands)
                 const uint32_t a_base = smem_u32(smem + s * L::kStageBytes);
                 const uint32_t b_base = a_base + L::kABytes;
                 const uint64_t ad0 = desc_sw128(a_base, 0, 1024);
@@ -159,10 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(&empty[s]);
             }
-            __syncwarp();
         }
-        if (lane == 0) mma_commit(done);  // also covers the partial run on abort
-        __syncwarp();
+        mma_commit(done);  // also covers the partial run on abort
     }
 
     // epilogue: thread t owns tile row t (output row m0 + t). Every load and MMA
@@ -375,7 +374,8 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
             if (ok && i >= 2) ok = warp_wait(&acc_empty[ac], ((i >> 1) - 1) & 1, abort, err, wait_ns);
             if (!ok) break;
             tc_fence_after();
-            if (lane == 0) {
+            {
+                // whole warp, one elected lane issues (warp-uniform operands)
                 const uint64_t ad0 = desc_sw128(smem_u32(smem + L::kOffA + sa * L::kA), 0, 1024);
                 const uint64_t bd0 = desc_sw128(smem_u32(smem + L::kOffB + sb * L::kB), 128 * 128, 1024);  // n-chunks 128 k-rows apart
 #pragma unroll
@@ -389,12 +389,10 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
                 const bool last_of_group = (u + 1 == u1) || ((u + 1) / kAbsQuarters != x.g);
                 if (last_of_group) mma_commit(&a_empty[sa]);
             }
-            __syncwarp();
             issued = true;
         }
         if (issued) {
-            if (lane == 0) mma_commit(done);
-            __syncwarp();
+            mma_commit(done);
             warp_wait(done, 0, nullptr, err, kDrainNs);
         }
         if (!ok) *abort = 1;
