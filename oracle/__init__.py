@@ -17,6 +17,9 @@ Parity status per function (how each is pinned, see tests/test_oracle_pins.py):
   combine, attend_split                              - pinned (split == single pass)
   metadata                                           - pinned by invariants and a
       hand-derived example; the pages print no schedule values.
+  prefill_naive                                      - pinned (equals the
+      absorbed form and the fp64 numpy brute force; causal row s equals a
+      decode of the first seqlen - s_q + s + 1 keys)
   rope, cache_append                                 - pinned (identity at
       position 0, exact quarter and half turns, norm preservation, relative
       position, composition; bit-exact latent copy into the table's slot)
@@ -80,6 +83,7 @@ def _load():
         lib.orc_attend_split.argtypes = [P, P, P, I, P, I, I, I, D, I, P, I, P, P, P, P, P]
         lib.orc_num_threads.restype = I
         lib.orc_rope.argtypes = [P, I64, I, P, D, P]
+        lib.orc_prefill_naive.argtypes = [P, P, P, I, P, I, I, I, P, P, D, I, P, P]
         lib.orc_cache_append.argtypes = [P, P, I, P, I, I, D, P]
         _lib = lib
         return lib
@@ -244,3 +248,19 @@ def cache_append(kv, kv_new, block_table, seqlens, base: float = 10000.0) -> np.
     assert d == D_QK and bt.shape[0] == B and sl.shape[0] == B and out.shape[1:] == (PAGE, D_QK)
     _load().orc_cache_append(_ptr(new), _ptr(bt), bt.shape[1], _ptr(sl), B, s_q, float(base), _ptr(out))
     return out
+
+
+def prefill_naive(q, kv, block_table, seqlens, w_uk, w_uv, scale: float, causal: bool = True):
+    """Prefill, naive form (per-head K and V materialised once per token):
+    q [B, s_q, H, 192] -> (out [B, s_q, H, 128], lse [B, s_q, H]) float64."""
+    q = _arr(q, np.float32)
+    kv, bt, sl = _attend_args(kv, block_table, seqlens)
+    wk = _arr(w_uk, np.float32)
+    wv = _arr(w_uv, np.float32)
+    B, s_q, H, _ = q.shape
+    assert wk.shape == (H, D_NOPE, D_LATENT) and wv.shape == (H, D_LATENT, D_V)
+    out = np.empty((B, s_q, H, D_V), np.float64)
+    lse = np.empty((B, s_q, H), np.float64)
+    _load().orc_prefill_naive(_ptr(q), _ptr(kv), _ptr(bt), bt.shape[1], _ptr(sl), B, s_q, H, _ptr(wk), _ptr(wv),
+                              float(scale), int(bool(causal)), _ptr(out), _ptr(lse))
+    return out, lse

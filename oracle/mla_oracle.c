@@ -195,6 +195,76 @@ void orc_attend_naive(const float* q, const float* kv, const int32_t* block_tabl
 }
 
 /*
+ * Prefill in the naive (decompress) form over the paged cache [V3 sec. 2.2: the
+ * per-head key and value are up-projections of the cached latent, k = W_UK c,
+ * v = W_UV c; sec. 3.1: the rope key part is shared by the heads; sec. 4.3:
+ * the paged module decompresses K and V per head before ordinary attention].
+ * The s_q query tokens of each sequence are its last s_q positions (a whole
+ * prompt when s_q = seqlen, a prompt chunk after earlier tokens otherwise).
+ * For each (b, h) the keys and values of every cached token t < seqlen_b are
+ * materialised once:
+ *   K_t = [sum_c W_UK[h,d,c] c_t[c] (d < 128) | k_rope_t (64)],  V_t[j] = sum_c c_t[c] W_UV[h,c,j],
+ * then every query row takes a two-pass softmax over its visible keys
+ * (bottom-right causal alignment) and out = sum_t p_t V_t.
+ * q [B, s_q, H, 192] float -> out [B, s_q, H, 128], lse [B, s_q, H] double.
+ */
+void orc_prefill_naive(const float* q, const float* kv, const int32_t* block_table, int mbps,
+                       const int32_t* seqlens, int B, int s_q, int H, const float* w_uk,
+                       const float* w_uv, double scale, int causal, double* out, double* lse) {
+    #pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            const int64_t L = seqlens[b] > 0 ? seqlens[b] : 0;
+            const int32_t* trow = block_table + (int64_t)b * mbps;
+            const float* wk = w_uk + (int64_t)h * ORC_DN * ORC_DC;
+            const float* wv = w_uv + (int64_t)h * ORC_DC * ORC_DV;
+            double* K = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * ORC_DQ);
+            double* V = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * ORC_DV);
+            for (int64_t t = 0; t < L; ++t) {
+                const float* c = kv_row(kv, trow, t);
+                for (int d = 0; d < ORC_DN; ++d) {
+                    double kd = 0.0;
+                    for (int cc = 0; cc < ORC_DC; ++cc) kd += (double)wk[(int64_t)d * ORC_DC + cc] * (double)c[cc];
+                    K[t * ORC_DQ + d] = kd;
+                }
+                for (int i = 0; i < ORC_DR; ++i) K[t * ORC_DQ + ORC_DN + i] = c[ORC_DC + i];
+                for (int j = 0; j < ORC_DV; ++j) {
+                    double vj = 0.0;
+                    for (int cc = 0; cc < ORC_DC; ++cc) vj += (double)c[cc] * (double)wv[(int64_t)cc * ORC_DV + j];
+                    V[t * ORC_DV + j] = vj;
+                }
+            }
+            double* sc = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+            for (int s = 0; s < s_q; ++s) {
+                const int64_t row = ((int64_t)b * s_q + s) * H + h;
+                const float* qr = q + row * ORC_DQ;
+                double* o = out + row * ORC_DV;
+                for (int j = 0; j < ORC_DV; ++j) o[j] = 0.0;
+                const int64_t n = visible_keys(L, s_q, s, causal);
+                if (n == 0) { lse[row] = -INFINITY; continue; }
+                double mx = -INFINITY;
+                for (int64_t t = 0; t < n; ++t) {
+                    double dot = 0.0;
+                    for (int d = 0; d < ORC_DQ; ++d) dot += (double)qr[d] * K[t * ORC_DQ + d];
+                    sc[t] = scale * dot;
+                    if (sc[t] > mx) mx = sc[t];
+                }
+                double l = 0.0;
+                for (int64_t t = 0; t < n; ++t) {
+                    const double p = exp(sc[t] - mx);
+                    l += p;
+                    for (int j = 0; j < ORC_DV; ++j) o[j] += p * V[t * ORC_DV + j];
+                }
+                for (int j = 0; j < ORC_DV; ++j) o[j] /= l;
+                lse[row] = mx + log(l);
+            }
+            free(sc);
+            free(K);
+            free(V);
+        }
+}
+
+/*
  * Output up-projection [V3 sec. 2.2, W_UV side of the absorption]:
  * out[r,h,j] = sum_c o_lat[r,h,c] W_UV[h,c,j].
  * o_lat [R, H, 512] double, w_uv [H, 512, 128] float -> out [R, H, 128] double.
