@@ -225,8 +225,41 @@ int mla_rope_append(mla_bf16_t* q, const mla_bf16_t* kv_new, const int32_t* cach
                     float rope_base, mla_stream_t stream);
 
 /*
+ * mla_prefill_paged - prefill over the same paged latent cache, in the naive
+ * (decompress) form. Pages: [V3] sec. 2.2 (k = W_UK c, v = W_UV c), sec. 3.1
+ * (the rope key is shared by the heads), sec. 4.3 (the paged module
+ * decompresses K and V per head before ordinary attention); [SC] opening
+ * (prefill processes the prompt, decode one token at a time).
+ *
+ * The s_q query tokens of sequence b are its last s_q positions (a whole
+ * prompt when s_q == cache_seqlens[b], a prompt chunk after earlier tokens
+ * otherwise; cache_seqlens already counts them). For every (b, s, h):
+ *   K_t = [W_UK[h] c_t | k_rope_t] (192), V_t = W_UV[h]^T c_t (128) for t < seqlen_b,
+ *   n = causal ? seqlen_b - s_q + s + 1 : seqlen_b (clamped to [0, seqlen_b]),
+ *   out[b,s,h,:] = sum_{t<n} softmax_t(softmax_scale * q[b,s,h,:] . K_t) V_t,
+ *   lse[b,s,h] = ln sum_{t<n} exp(softmax_scale * q . K_t); n == 0 gives 0, -inf.
+ * q: bf16 [B, s_q, H, 192] = [q_nope 128 | q_rope 64] (rope already applied);
+ * kv_cache, block_table, cache_seqlens as mla_decode_paged; w_uk [H, 128, 512],
+ * w_uv [H, 512, 128] bf16; out (out): bf16 [B, s_q, H, 128] (the per-head
+ * output, already through W_UV); lse (out): fp32 [B, s_q, H].
+ * workspace: device, >= mla_prefill_workspace_size(B, H, max_blocks_per_seq)
+ * bytes, 1024-byte aligned (no zero-fill needed): holds the gathered latent and
+ * the decompressed K and V (bf16) of every sequence, padded to
+ * max_blocks_per_seq pages. Any s_q >= 1; H in {16, 32, 64, 128}.
+ * Launches a gather, two batched head GEMMs (tcgen05) and the attention
+ * kernel (one CTA per (sequence, head, 128-query tile); tcgen05 with S and O in
+ * tensor memory). A block id outside the pool is recorded as MLA_ERR_BAD_BLOCK
+ * in the library's error word and its rows read as zeros.
+ */
+size_t mla_prefill_workspace_size(int B, int H, int max_blocks_per_seq);
+int mla_prefill_paged(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int num_blocks, const int32_t* block_table,
+                      int max_blocks_per_seq, const int32_t* cache_seqlens, int B, int s_q, int H,
+                      const mla_bf16_t* w_uk, const mla_bf16_t* w_uv, float softmax_scale, int causal,
+                      mla_bf16_t* out, float* lse, void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
  * Reads and clears the device error word of `workspace` (may be NULL) and the
- * library's own error word (projections, rope append); synchronises `stream`.
+ * library's own error words (projections, rope append, prefill); synchronises `stream`.
  * Returns MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_BAD_BLOCK as recorded by the
  * kernels since the last read, or MLA_ERR_CUDA if the read failed.
  */

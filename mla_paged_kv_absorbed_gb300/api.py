@@ -76,6 +76,10 @@ def lib() -> ctypes.CDLL:
         L.mla_debug_mma.argtypes = [P, P, I, I, I, I, P, P]
         L.mla_debug_mma.restype = I
         L.mla_debug_withhold_value_load.argtypes = [I]
+        L.mla_prefill_workspace_size.argtypes = [I, I, I]
+        L.mla_prefill_workspace_size.restype = SZ
+        L.mla_prefill_paged.argtypes = [P, P, I, P, I, P, I, I, I, P, P, F, I, P, P, P, SZ, P]
+        L.mla_prefill_paged.restype = I
         L.mla_rope_append.argtypes = [P, P, P, P, I, P, I, I, I, I, F, P]
         L.mla_rope_append.restype = I
         _lib = L
@@ -358,3 +362,53 @@ def mla_decode_paged_noalloc(q_abs: torch.Tensor, kv_cache: torch.Tensor, block_
         B, s_q, H, _p(tile_meta), _p(num_splits), tile_meta.shape[0], float(softmax_scale), int(bool(causal)),
         _p(o_lat), _p(lse), _p(device_status), _stream(stream)))
     return o_lat, lse
+
+
+# ------------------------------------------------------------------ prefill --
+
+def mla_prefill_workspace_size(B: int, H: int, max_blocks_per_seq: int) -> int:
+    return int(lib().mla_prefill_workspace_size(int(B), int(H), int(max_blocks_per_seq)))
+
+
+def mla_prefill_paged(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor, cache_seqlens: torch.Tensor,
+                      w_uk: torch.Tensor, w_uv: torch.Tensor, softmax_scale: float, causal: bool = True,
+                      out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Prefill in the naive form over the paged cache: q [B, s_q, H, 192] (the
+    last s_q positions of each sequence) -> (out [B, s_q, H, 128], lse [B, s_q, H]).
+    See include/mla.h."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(kv_cache, "kv_cache", torch.bfloat16, 3)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(cache_seqlens, "cache_seqlens", torch.int32, 1)
+    _need(w_uk, "w_uk", torch.bfloat16, 3)
+    _need(w_uv, "w_uv", torch.bfloat16, 3)
+    B, s_q, H, dq = q.shape
+    if dq != D_Q or tuple(kv_cache.shape[1:]) != (PAGE, D_QK):
+        raise ValueError("q must be [B, s_q, H, 192] and kv_cache [num_blocks, 64, 576]")
+    if tuple(w_uk.shape) != (H, 128, D_LATENT) or tuple(w_uv.shape) != (H, D_LATENT, D_V):
+        raise ValueError("w_uk must be [H, 128, 512] and w_uv [H, 512, 128]")
+    if block_table.shape[0] != B or cache_seqlens.shape[0] != B:
+        raise ValueError("block_table and cache_seqlens must match the batch of q")
+    mbps = block_table.shape[1]
+    if out is None:
+        out = torch.empty((B, s_q, H, D_V), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, s_q, H), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    if tuple(out.shape) != (B, s_q, H, D_V) or tuple(lse.shape) != (B, s_q, H):
+        raise ValueError(f"out must be [{B}, {s_q}, {H}, 128] and lse [{B}, {s_q}, {H}]")
+    if workspace is None:
+        n = mla_prefill_workspace_size(B, H, mbps)
+        if n == 0:
+            raise MLAError("mla_prefill_workspace_size", MLA_ERR_INVALID_ARG)
+        workspace = torch.empty(n + 1024, dtype=torch.uint8, device=q.device)
+        off = (-workspace.data_ptr()) % 1024
+        workspace = workspace[off:off + n]
+    _need(workspace, "workspace", torch.uint8, 1)
+    _check("mla_prefill_paged", lib().mla_prefill_paged(
+        _p(q), _p(kv_cache), kv_cache.shape[0], _p(block_table), mbps, _p(cache_seqlens), B, s_q, H, _p(w_uk),
+        _p(w_uv), float(softmax_scale), int(bool(causal)), _p(out), _p(lse), _p(workspace), workspace.numel(),
+        _stream(stream)))
+    return out, lse

@@ -138,6 +138,8 @@ int head_gemm(const void* a, int a_row_elems, const void* w, int K, int N, int n
     args.out = out;
     args.out_row_elems = out_row_elems;
     args.rope_src = rope_src;
+    args.a_shared = 0;
+    args.b_kmajor = 0;
     return cuda_status(launch_head_gemm(&tm_a, &tm_b, &tm_out, args, g_wait_ns.load(), stream));
 }
 
@@ -306,10 +308,120 @@ int mla_read_device_error(void* workspace, mla_stream_t stream) {
             return MLA_ERR_CUDA;
         if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
     }
+    int prefill_err = 0;
     if (gemm_error_fetch(&gemm_err, st) != cudaSuccess) return MLA_ERR_CUDA;
     if (rope_error_fetch(&rope_err, st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (prefill_error_fetch(&prefill_err, st) != cudaSuccess) return MLA_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
-    return ws_err != 0 ? ws_err : (gemm_err != 0 ? gemm_err : rope_err);
+    return ws_err != 0 ? ws_err : (gemm_err != 0 ? gemm_err : (rope_err != 0 ? rope_err : prefill_err));
+}
+
+namespace {
+// Prefill workspace: [256-byte header] [C: R x 512] [K: H x R x 192] [V: H x R x 128]
+// bf16, R = B * max_blocks_per_seq * 64 rows, each region 1024-byte aligned.
+struct PrefillLayout {
+    size_t c, k, v, total, rows;
+};
+PrefillLayout prefill_layout(int B, int H, int mbps) {
+    auto up = [](size_t x) { return (x + 1023) & ~size_t(1023); };
+    PrefillLayout l;
+    l.rows = (size_t)B * (size_t)mbps * kPage;
+    l.c = 1024;
+    l.k = up(l.c + l.rows * kDLatent * 2);
+    l.v = up(l.k + (size_t)H * l.rows * kDQ * 2);
+    l.total = up(l.v + (size_t)H * l.rows * kDV * 2);
+    return l;
+}
+}  // namespace
+
+size_t mla_prefill_workspace_size(int B, int H, int max_blocks_per_seq) {
+    if (B <= 0 || !valid_heads(H) || max_blocks_per_seq <= 0) return 0;
+    return prefill_layout(B, H, max_blocks_per_seq).total;
+}
+
+int mla_prefill_paged(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int num_blocks, const int32_t* block_table,
+                      int max_blocks_per_seq, const int32_t* cache_seqlens, int B, int s_q, int H,
+                      const mla_bf16_t* w_uk, const mla_bf16_t* w_uv, float softmax_scale, int causal,
+                      mla_bf16_t* out, float* lse, void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+    if (!q || !kv_cache || !block_table || !cache_seqlens || !w_uk || !w_uv || !out || !lse || !workspace)
+        return MLA_ERR_INVALID_ARG;
+    if (B <= 0 || s_q <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || !valid_heads(H)) return MLA_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || (causal != 0 && causal != 1)) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 1023u) != 0)
+        return MLA_ERR_INVALID_ARG;
+    const PrefillLayout pl = prefill_layout(B, H, max_blocks_per_seq);
+    if (workspace_bytes < pl.total || (uint64_t)B * s_q > 0x7FFFFFFFull || pl.rows > 0x7FFFFFFFull)
+        return MLA_ERR_INVALID_ARG;
+    int dev = check_device();
+    if (dev != MLA_OK) return dev;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* C = ws + pl.c;
+    void* Kb = ws + pl.k;
+    void* Vb = ws + pl.v;
+    const uint64_t R = pl.rows;
+
+    // 1. the latent rows and rope keys of every sequence, contiguous (zeros past seqlen)
+    if (launch_prefill_gather(kv_cache, num_blocks, block_table, max_blocks_per_seq, cache_seqlens, B, H, C, Kb, st) !=
+        cudaSuccess)
+        return MLA_ERR_CUDA;
+
+    // 2. K_nope[h] = C . W_UK[h]^T and V[h] = C . W_UV[h] as per-head GEMMs with a shared A
+    CUtensorMap ta, tb, to;
+    const uint64_t a_dims[4] = {64, R, (uint64_t)kDLatent / 64, 1};
+    const uint64_t a_strides[3] = {(uint64_t)kDLatent * 2, 128, R * kDLatent * 2};
+    const uint32_t box128[4] = {64, 128, 2, 1};
+    if (!make_tmap(&ta, C, 4, a_dims, a_strides, box128)) return MLA_ERR_CUDA;
+    GemmArgs g;
+    g.R = (int)R;
+    g.H = H;
+    g.K = kDLatent;
+    g.N = 128;
+    g.n_cta = 128;
+    g.rope_src = nullptr;
+    g.a_shared = 1;
+    {   // W_UK[h] is [128 (n) x 512 (k)]: a K-major B operand
+        const uint64_t b_dims[4] = {64, (uint64_t)kDNope, (uint64_t)kDLatent / 64, (uint64_t)H};
+        const uint64_t b_strides[3] = {(uint64_t)kDLatent * 2, 128, (uint64_t)kDNope * kDLatent * 2};
+        const uint64_t o_dims[4] = {64, R, (uint64_t)kDQ / 64, (uint64_t)H};
+        const uint64_t o_strides[3] = {(uint64_t)kDQ * 2, 128, R * kDQ * 2};
+        if (!make_tmap(&tb, w_uk, 4, b_dims, b_strides, box128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) return MLA_ERR_CUDA;
+        if (!make_tmap(&to, Kb, 4, o_dims, o_strides, box128)) return MLA_ERR_CUDA;
+        g.out = Kb;
+        g.out_row_elems = kDQ;
+        g.b_kmajor = 1;
+        if (launch_head_gemm(&ta, &tb, &to, g, g_wait_ns.load(), st) != cudaSuccess) return MLA_ERR_CUDA;
+    }
+    {   // W_UV[h] is [512 (k) x 128 (n)]: an N-major B operand
+        const uint64_t b_dims[4] = {64, (uint64_t)kDLatent, (uint64_t)kDV / 64, (uint64_t)H};
+        const uint64_t b_strides[3] = {(uint64_t)kDV * 2, 128, (uint64_t)kDLatent * kDV * 2};
+        const uint64_t o_dims[4] = {64, R, (uint64_t)kDV / 64, (uint64_t)H};
+        const uint64_t o_strides[3] = {(uint64_t)kDV * 2, 128, R * kDV * 2};
+        if (!make_tmap(&tb, w_uv, 4, b_dims, b_strides, box128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) return MLA_ERR_CUDA;
+        if (!make_tmap(&to, Vb, 4, o_dims, o_strides, box128)) return MLA_ERR_CUDA;
+        g.out = Vb;
+        g.out_row_elems = kDV;
+        g.b_kmajor = 0;
+        if (launch_head_gemm(&ta, &tb, &to, g, g_wait_ns.load(), st) != cudaSuccess) return MLA_ERR_CUDA;
+    }
+
+    // 3. causal attention per (sequence, head, 128-query tile)
+    CUtensorMap tq, tk, tv;
+    const uint64_t q_dims[4] = {64, (uint64_t)H, (uint64_t)B * s_q, (uint64_t)kDQ / 64};
+    const uint64_t q_strides[3] = {(uint64_t)kDQ * 2, (uint64_t)H * kDQ * 2, 128};
+    const uint32_t q_box[4] = {64, 1, 128, 3};
+    if (!make_tmap(&tq, q, 4, q_dims, q_strides, q_box)) return MLA_ERR_CUDA;
+    const uint64_t k_dims[4] = {64, R, (uint64_t)kDQ / 64, (uint64_t)H};
+    const uint64_t k_strides[3] = {(uint64_t)kDQ * 2, 128, R * kDQ * 2};
+    const uint32_t k_box[4] = {64, 64, 3, 1};
+    if (!make_tmap(&tk, Kb, 4, k_dims, k_strides, k_box)) return MLA_ERR_CUDA;
+    const uint64_t v_dims[4] = {64, R, (uint64_t)kDV / 64, (uint64_t)H};
+    const uint64_t v_strides[3] = {(uint64_t)kDV * 2, 128, R * kDV * 2};
+    const uint32_t v_box[4] = {64, 64, 2, 1};
+    if (!make_tmap(&tv, Vb, 4, v_dims, v_strides, v_box)) return MLA_ERR_CUDA;
+    return cuda_status(launch_prefill_attn(&tq, &tk, &tv, cache_seqlens, B, s_q, H, max_blocks_per_seq * kPage,
+                                           softmax_scale, causal, out, lse, g_wait_ns.load(), st));
 }
 
 int mla_rope_append(mla_bf16_t* q, const mla_bf16_t* kv_new, const int32_t* cache_seqlens, const int32_t* block_table,

@@ -99,8 +99,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* a_dst = smem + s * L::kStageBytes;
             uint8_t* b_dst = a_dst + L::kABytes;
             mbar_arrive_expect_tx(&full[s], L::kStageBytes);
-            tma_load_4d(a_dst, &tm_a, &full[s], 0, m0, 2 * kc, h);
-            tma_load_4d(b_dst, &tm_b, &full[s], 0, kc * kBK, n0 / 64, h);
+            tma_load_4d(a_dst, &tm_a, &full[s], 0, m0, 2 * kc, args.a_shared ? 0 : h);
+            if (args.b_kmajor)  // [NCTA rows][2 K chunks][64] as [chunk][row][64]
+                tma_load_4d(b_dst, &tm_b, &full[s], 0, n0, 2 * kc, h);
+            else
+                tma_load_4d(b_dst, &tm_b, &full[s], 0, kc * kBK, n0 / 64, h);
             issued = kc + 1;
         }
         // never leave with a copy in flight: wait for the last load of every stage
@@ -139,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // MMA issuer
-        constexpr uint32_t idesc = idesc_bf16_f32(kBM, NCTA, false, true);
+        const uint32_t idesc = idesc_bf16_f32(kBM, NCTA, false, args.b_kmajor == 0);
         bool ok = true;
         for (int kc = 0; kc < num_k && ok; ++kc) {
             const int s = kc % STAGES;
@@ -151,11 +154,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t a_base = smem_u32(smem + s * L::kStageBytes);
                 const uint32_t b_base = a_base + L::kABytes;
                 const uint64_t ad0 = desc_sw128(a_base, 0, 1024);
-                const uint64_t bd0 = desc_sw128(b_base, kBK * 128, 1024);  // n-chunks are 128 k-rows apart
+                // N-major B: n-chunks are 128 k-rows apart, a K-step is 16 k-rows;
+                // K-major B: like A, a K-step is 32 bytes inside the 128-byte rows
+                const uint64_t bd0 = args.b_kmajor ? desc_sw128(b_base, 0, 1024) : desc_sw128(b_base, kBK * 128, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk) {
                     const uint64_t ad = ad0 + (uint64_t)(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
-                    const uint64_t bd = bd0 + (uint64_t)((kk * 2048) >> 4);
+                    const uint64_t bd = args.b_kmajor
+                                            ? bd0 + (uint64_t)(((kk >> 2) * (NCTA * 128) + (kk & 3) * 32) >> 4)
+                                            : bd0 + (uint64_t)((kk * 2048) >> 4);
                     mma_bf16_ss(tmem, ad, bd, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(&empty[s]);

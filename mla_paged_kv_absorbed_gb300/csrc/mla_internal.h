@@ -41,6 +41,8 @@ struct GemmArgs {
     void* out;        // bf16 [R, H, out_row_elems]
     int out_row_elems;
     const void* rope_src;  // absorb only: q [R, H, 192]; rope part copied to out columns 512..575
+    int a_shared;          // 1: every head reads the same A rows (the A map has one head)
+    int b_kmajor;          // 1: B is stored [N rows][K] (K contiguous) instead of [K rows][N]
 };
 cudaError_t launch_head_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const CUtensorMap* tm_out,
                              const GemmArgs& args, long long wait_ns, cudaStream_t stream);
@@ -88,6 +90,14 @@ cudaError_t launch_rope_append(void* q, const void* kv_new, const int32_t* seqle
                                int mbps, void* kv_cache, int num_blocks, int B, int s_q, int H, double base,
                                cudaStream_t stream);
 cudaError_t rope_error_fetch(int* out, cudaStream_t stream);
+
+// Prefill (naive form): gather + attention launchers (prefill.cu).
+cudaError_t launch_prefill_gather(const void* kv, int num_blocks, const int32_t* table, int mbps,
+                                  const int32_t* seqlens, int B, int H, void* C, void* Kbuf, cudaStream_t stream);
+cudaError_t launch_prefill_attn(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                                const int32_t* seqlens, int B, int s_q, int H, int Lmax, float scale, int causal,
+                                void* out, float* lse, long long wait_ns, cudaStream_t stream);
+cudaError_t prefill_error_fetch(int* out, cudaStream_t stream);
 
 cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, const float* o_part,
                            const float* lse_part, void* o_lat, float* lse, cudaStream_t stream);

@@ -1,0 +1,444 @@
+// prefill.cu - prefill over the paged latent cache in the naive (decompress)
+// form: the per-head keys and values are up-projected from the cached latent,
+// then ordinary causal attention runs per head.
+//
+// What it computes ("DeepSeek-V3 MLA deep engineering", sec. 2.2: k = W_UK c,
+// v = W_UV c; sec. 3.1: the rope key is shared by the heads; sec. 4.3: the
+// paged module decompresses K and V per head before attention; the SC11
+// article's opening: prefill processes a whole prompt, decode one token):
+// for sequence b with seqlen L and s_q query tokens (its last s_q positions),
+// head h and query s:
+//   K_t = [W_UK[h] c_t | k_rope_t] (192), V_t = W_UV[h]^T c_t (128), t < L
+//   out[b,s,h,:] = softmax_t(scale * q[b,s,h,:] . K_t) V_t over t <= L - s_q + s
+//   lse[b,s,h]   = ln sum_t exp(scale * q . K_t)
+// The naive form costs 2 * (192 + 128) flops per (query, key, head) against
+// 2 * (576 + 512) for the absorbed form, so it is the cheaper form once a
+// sequence has many query tokens; the up-projections cost 2 * 512 * 256 flops
+// per (token, head), once.
+//
+// Kernels here: the gather of the sequence's latent rows and rope keys into
+// contiguous buffers (the two up-projections then run as batched head GEMMs,
+// gemm.cu), and the attention: one CTA per (b, h, 128-query tile), 64-key
+// tiles of K and V streaming through a TMA ring, S = Q K^T and O += P V on
+// tcgen05 with S (double-buffered) and O in TMEM, one softmax thread per query
+// row (online softmax, lazy rescaling of O), P staged in shared memory.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "mla_internal.h"
+#include "ptx.cuh"
+
+namespace mla {
+
+__device__ int g_prefill_error = 0;
+
+namespace {
+
+// ------------------------------------------------------------------ gather --
+// One CTA per (b, page j): rows t = 64 j .. 64 j + 63 of sequence b. For t <
+// seqlen: C[b Lmax + t] = c_t[0:512], Kbuf[h][b Lmax + t][128:192] = k_rope_t for
+// every head; for t >= seqlen both are zero, so padding keys contribute
+// nothing finite-unsafe (their K and V rows are exact zeros after the GEMMs).
+constexpr int kGatherThreads = 256;
+
+__global__ void __launch_bounds__(kGatherThreads)
+    prefill_gather_kernel(const __nv_bfloat16* __restrict__ kv, int num_blocks, const int32_t* __restrict__ table,
+                          int mbps, const int32_t* __restrict__ seqlens, int H, size_t R, __nv_bfloat16* __restrict__ C,
+                          __nv_bfloat16* __restrict__ Kbuf) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int b = blockIdx.y, j = blockIdx.x;
+    const int L = seqlens[b];
+    if (j == 0 && threadIdx.x == 0 && L > mbps * kPage) record_error(&g_prefill_error, kErrBadBlock);
+    int blk = -1;
+    if (j * kPage < L) {
+        blk = table[(size_t)b * mbps + j];
+        if (blk < 0 || blk >= num_blocks) {
+            if (threadIdx.x == 0) record_error(&g_prefill_error, kErrBadBlock);
+            blk = -1;
+        }
+    }
+    const size_t row0 = (size_t)b * mbps * kPage + (size_t)j * kPage;
+    // latent: 64 rows x 64 words of 16 bytes
+    for (int i = threadIdx.x; i < kPage * 64; i += kGatherThreads) {
+        const int r = i >> 6, w = i & 63;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (blk >= 0 && j * kPage + r < L)
+            v = reinterpret_cast<const uint4*>(kv + ((size_t)blk * kPage + r) * kDQK)[w];
+        reinterpret_cast<uint4*>(C + (row0 + r) * kDLatent)[w] = v;
+    }
+    // rope key: 64 rows x 8 words, copied into every head's K rows
+    for (int i = threadIdx.x; i < kPage * 8 * H; i += kGatherThreads) {
+        const int w = i & 7, r = (i >> 3) & (kPage - 1), h = i >> 9;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (blk >= 0 && j * kPage + r < L)
+            v = reinterpret_cast<const uint4*>(kv + ((size_t)blk * kPage + r) * kDQK + kDLatent)[w];
+        reinterpret_cast<uint4*>(Kbuf + ((size_t)h * R + row0 + r) * kDQ + kDNope)[w] = v;
+    }
+}
+
+// --------------------------------------------------------------- attention --
+constexpr int kAThreads = 192;  // warps 0-3 softmax (one thread per row), 4 producer, 5 MMA + TMEM owner
+constexpr int kARows = 128;     // query rows per CTA
+constexpr int kAKeys = 64;      // keys per tile
+constexpr int kAStages = 3;
+constexpr int kQBytes = 3 * kARows * 128;   // [3 chunks][128 rows][64]
+constexpr int kKBytes = 3 * kAKeys * 128;   // [3 chunks][64 keys][64]
+constexpr int kVBytesA = 2 * kAKeys * 128;  // [2 chunks][64 keys][64]
+constexpr int kPBytes = kARows * 128;       // [128 rows][64 keys]
+constexpr int kAOffQ = 1024;
+constexpr int kAOffK = kAOffQ + kQBytes;
+constexpr int kAOffV = kAOffK + kAStages * kKBytes;
+constexpr int kAOffP = kAOffV + kAStages * kVBytesA;
+constexpr int kASmem = kAOffP + 2 * kPBytes + 1024;  // + alignment slack
+static_assert(kASmem <= 232448, "prefill attention shared memory");
+constexpr uint32_t kATmemS = 0;    // two S buffers of 64 columns
+constexpr uint32_t kATmemO = 128;  // O: 128 columns
+constexpr uint32_t kATmemCols = 256;
+constexpr float kARescale = 8.0f;
+
+struct ABars {
+    uint64_t q_full;
+    uint64_t kv_full[kAStages], kv_empty[kAStages];
+    uint64_t s_full[2], s_free[2];
+    uint64_t p_full[2], p_free[2];
+    uint64_t pv_done, drain;
+    uint32_t tmem_slot;
+    int abort;
+};
+static_assert(sizeof(ABars) <= 1024, "prefill barriers");
+
+struct PrefillArgs {
+    const int32_t* seqlens;
+    int s_q, H, Lmax;
+    float scale_log2;
+    int causal;
+    __nv_bfloat16* out;  // [B, s_q, H, 128]
+    float* lse;          // [B, s_q, H]
+    int* err;
+    long long wait_ns;
+};
+struct PrefillMaps {
+    CUtensorMap q, k, v;
+};
+
+__device__ __forceinline__ int visible(int L, int s_q, int s, int causal) {
+    int n = causal ? L - s_q + s + 1 : L;
+    return n < 0 ? 0 : (n > L ? L : n);
+}
+
+__global__ void __launch_bounds__(kAThreads, 1)
+    prefill_attn_kernel(const __grid_constant__ PrefillMaps maps, PrefillArgs args) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    ABars* bars = reinterpret_cast<ABars*>(smem);
+    volatile int* abort = &bars->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int q0 = qt * kARows;
+    int* err = args.err;
+    const long long wait_ns = args.wait_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->q_full, 1);
+        for (int i = 0; i < kAStages; ++i) {
+            mbar_init(&bars->kv_full[i], 1);
+            mbar_init(&bars->kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->s_full[i], 1);
+            mbar_init(&bars->s_free[i], 128);
+            mbar_init(&bars->p_full[i], 128);
+            mbar_init(&bars->p_free[i], 1);
+        }
+        mbar_init(&bars->pv_done, 1);
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbarrier_init_cluster();
+        tma_prefetch_desc(&maps.q);
+        tma_prefetch_desc(&maps.k);
+        tma_prefetch_desc(&maps.v);
+    }
+    if (warp == 5) {
+        tmem_alloc(&bars->tmem_slot, kATmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_slot;
+    griddep_wait();
+    griddep_launch_dependents();
+
+    // keys this tile needs: up to the last visible key of its last valid row
+    const int L = min(max(args.seqlens[b], 0), args.Lmax);  // longer sequences were reported by the gather
+    const int last_row = min(q0 + kARows, args.s_q) - 1;
+    const int n_max = last_row >= q0 ? visible(L, args.s_q, last_row, args.causal) : 0;
+    const int tiles = (n_max + kAKeys - 1) / kAKeys;
+    const int key_row0 = b * args.Lmax;  // first key row of this sequence in the K/V buffers
+
+    bool ok = true;
+    if (warp == 4) {
+        // producer: the query tile once, then K and V tiles through the ring
+        if (lane == 0 && tiles > 0) {
+            mbar_arrive_expect_tx(&bars->q_full, (uint32_t)kQBytes);
+            tma_load_4d(smem + kAOffQ, &maps.q, &bars->q_full, 0, h, b * args.s_q + q0, 0);
+            int issued = 0;
+            for (int j = 0; j < tiles; ++j) {
+                const int st = j % kAStages;
+                if (j >= kAStages && !mbar_wait(&bars->kv_empty[st], ((j / kAStages) - 1) & 1, abort, err, wait_ns)) break;
+                mbar_arrive_expect_tx(&bars->kv_full[st], (uint32_t)(kKBytes + kVBytesA));
+                tma_load_4d(smem + kAOffK + st * kKBytes, &maps.k, &bars->kv_full[st], 0, key_row0 + j * kAKeys, 0, h);
+                tma_load_4d(smem + kAOffV + st * kVBytesA, &maps.v, &bars->kv_full[st], 0, key_row0 + j * kAKeys, 0, h);
+                issued = j + 1;
+            }
+            // every load this thread issued has landed before the CTA may leave
+            mbar_wait(&bars->q_full, 0, nullptr, err, kDrainNs);
+            for (int j = issued - kAStages > 0 ? issued - kAStages : 0; j < issued; ++j)
+                mbar_wait(&bars->kv_full[j % kAStages], (j / kAStages) & 1, nullptr, err, kDrainNs);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // MMA issuer (whole warp; one elected lane issues)
+        const uint32_t idesc_s = idesc_bf16_f32(kARows, kAKeys, false, false);
+        const uint32_t idesc_o = idesc_bf16_f32(kARows, 128, false, true);
+        const uint64_t qdesc = desc_sw128(smem_u32(smem + kAOffQ), 0, 1024);
+        bool issued = false;
+        if (tiles > 0) ok = warp_wait(&bars->q_full, 0, abort, err, wait_ns);
+        auto issue_s = [&](int j) -> bool {
+            const int st = j % kAStages, sb = j & 1;
+            if (!warp_wait(&bars->kv_full[st], (j / kAStages) & 1, abort, err, wait_ns)) return false;
+            if (j >= 2 && !warp_wait(&bars->s_free[sb], ((j >> 1) - 1) & 1, abort, err, wait_ns)) return false;
+            tc_fence_after();
+            const uint64_t kdesc = desc_sw128(smem_u32(smem + kAOffK + st * kKBytes), 0, 1024);
+#pragma unroll
+            for (int c = 0; c < 3; ++c)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss(tmem + kATmemS + 64u * (uint32_t)sb,
+                                qdesc + (uint64_t)((c * kARows * 128 + 32 * kk) >> 4),
+                                kdesc + (uint64_t)((c * kAKeys * 128 + 32 * kk) >> 4), idesc_s, (c | kk) != 0);
+            mma_commit(&bars->s_full[sb]);
+            return true;
+        };
+        if (ok && tiles > 0) { ok = issue_s(0); issued = ok; }
+        if (ok && tiles > 1) ok = issue_s(1);
+        for (int j = 0; ok && j < tiles; ++j) {
+            const int st = j % kAStages, pb = j & 1;
+            ok = warp_wait(&bars->p_full[pb], (j >> 1) & 1, abort, err, wait_ns);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t pdesc = desc_sw128(smem_u32(smem + kAOffP + pb * kPBytes), 0, 1024);
+            const uint64_t vdesc = desc_sw128(smem_u32(smem + kAOffV + st * kVBytesA), kAKeys * 128, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kAKeys / 16; ++kk)
+                mma_bf16_ss(tmem + kATmemO, pdesc + (uint64_t)((32 * kk) >> 4), vdesc + (uint64_t)((2048 * kk) >> 4),
+                            idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&bars->kv_empty[st]);  // K(j) and V(j) read (S(j) was issued earlier)
+            mma_commit(&bars->p_free[pb]);
+            mma_commit(&bars->pv_done);
+            if (j + 2 < tiles) ok = issue_s(j + 2);
+        }
+        if (issued) {
+            mma_commit(&bars->drain);
+            warp_wait(&bars->drain, 0, nullptr, err, kDrainNs);
+        }
+    } else if (warp < 4) {
+        // softmax and epilogue: thread = query row
+        const int row = warp * 32 + lane, s = q0 + row;
+        const bool valid_row = s < args.s_q;
+        const int n_vis = valid_row ? visible(L, args.s_q, s, args.causal) : 0;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        float m = -INFINITY, l = 0.f;
+        for (int j = 0; j < tiles; ++j) {
+            const int sb = j & 1;
+            float x[64];
+            if (ok) ok = warp_wait(&bars->s_full[sb], (j >> 1) & 1, abort, err, wait_ns);
+            if (!ok) break;
+            tc_fence_after();
+            {
+                uint32_t v0[32], v1[32];
+                tmem_ld32(tmem + lane_base + kATmemS + 64u * (uint32_t)sb, v0);
+                tmem_ld32(tmem + lane_base + kATmemS + 64u * (uint32_t)sb + 32u, v1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    x[c] = __uint_as_float(v0[c]) * args.scale_log2;
+                    x[32 + c] = __uint_as_float(v1[c]) * args.scale_log2;
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars->s_free[sb]);
+            const int vcount = min(max(n_vis - j * kAKeys, 0), kAKeys);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                x[c] = c < vcount ? x[c] : -INFINITY;
+                mx = fmaxf(mx, x[c]);
+            }
+            // lazy rescale: move the reference max only when the row max grows by more than 2^8
+            const bool need = mx > m + kARescale;
+            const float alpha = need ? fast_exp2(m - mx) : 1.f;  // 0 when m = -inf
+            if (need) {
+                l *= alpha;
+                m = mx;
+            }
+            // O rows move to the new reference (warp-uniform decision) once P V of
+            // tile j - 1 has landed; S(j) completing implies P V of tile j - 2 has,
+            // so the barrier is at most one phase behind this wait
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                ok = warp_wait(&bars->pv_done, (j - 1) & 1, abort, err, wait_ns);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + kATmemO + (uint32_t)c, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                    tmem_st32(tmem + lane_base + kATmemO + (uint32_t)c, v);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+            }
+            const float m_use = m == -INFINITY ? 0.f : m;
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float p0 = fast_exp2(x[2 * c] - m_use), p1 = fast_exp2(x[2 * c + 1] - m_use);
+                l += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+            }
+            // P buffer sb held tile j - 2 until its P V finished
+            if (j >= 2) ok = warp_wait(&bars->p_free[sb], ((j >> 1) - 1) & 1, abort, err, wait_ns);
+            if (!ok) break;
+            uint8_t* prow = smem + kAOffP + sb * kPBytes + row * 128;
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                *reinterpret_cast<uint4*>(prow + ((w ^ (row & 7)) << 4)) =
+                    make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->p_full[sb]);
+        }
+        // epilogue: O / l -> out (bf16), lse. P V of the last two tiles may both be
+        // outstanding: wait for their phases in order (a parity wait must never
+        // run two phases ahead of the barrier)
+        if (ok && tiles > 1) ok = warp_wait(&bars->pv_done, (tiles - 2) & 1, abort, err, wait_ns);
+        if (ok && tiles > 0) ok = warp_wait(&bars->pv_done, (tiles - 1) & 1, abort, err, wait_ns);
+        if (ok) {
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16* dst = args.out + (((size_t)b * args.s_q + s) * args.H + h) * kDV;
+#pragma unroll 1
+            for (int c = 0; c < 128; c += 32) {
+                uint32_t v[32];
+                if (tiles > 0) {
+                    tmem_ld32(tmem + lane_base + kATmemO + (uint32_t)c, v);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
+                if (valid_row) {
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        uint4 o;
+                        o.x = pack_bf16x2(__uint_as_float(v[8 * w + 0]) * inv_l, __uint_as_float(v[8 * w + 1]) * inv_l);
+                        o.y = pack_bf16x2(__uint_as_float(v[8 * w + 2]) * inv_l, __uint_as_float(v[8 * w + 3]) * inv_l);
+                        o.z = pack_bf16x2(__uint_as_float(v[8 * w + 4]) * inv_l, __uint_as_float(v[8 * w + 5]) * inv_l);
+                        o.w = pack_bf16x2(__uint_as_float(v[8 * w + 6]) * inv_l, __uint_as_float(v[8 * w + 7]) * inv_l);
+                        reinterpret_cast<uint4*>(dst + c)[w] = o;
+                    }
+                }
+            }
+            if (valid_row)
+                args.lse[((size_t)b * args.s_q + s) * args.H + h] =
+                    l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+        }
+    }
+    if (!ok) *abort = 1;
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kATmemCols);
+    }
+}
+
+cudaError_t prepare_attn() {
+    static std::mutex mu;
+    static bool done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kASmem);
+    if (e == cudaSuccess) done[dev] = true;
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_gather(const void* kv, int num_blocks, const int32_t* table, int mbps,
+                                  const int32_t* seqlens, int B, int H, void* C, void* Kbuf, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)mbps, (unsigned)B, 1);
+    cfg.blockDim = dim3(kGatherThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const size_t R = (size_t)B * mbps * kPage;
+    return cudaLaunchKernelEx(&cfg, prefill_gather_kernel, static_cast<const __nv_bfloat16*>(kv), num_blocks, table,
+                              mbps, seqlens, H, R, static_cast<__nv_bfloat16*>(C), static_cast<__nv_bfloat16*>(Kbuf));
+}
+
+cudaError_t launch_prefill_attn(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                                const int32_t* seqlens, int B, int s_q, int H, int Lmax, float scale, int causal,
+                                void* out, float* lse, long long wait_ns, cudaStream_t stream) {
+    cudaError_t e = prepare_attn();
+    if (e != cudaSuccess) return e;
+    PrefillMaps maps;
+    maps.q = *tq;
+    maps.k = *tk;
+    maps.v = *tv;
+    PrefillArgs a;
+    a.seqlens = seqlens;
+    a.s_q = s_q;
+    a.H = H;
+    a.Lmax = Lmax;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.causal = causal;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    a.err = &g_prefill_error;
+    a.wait_ns = wait_ns;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((s_q + kARows - 1) / kARows), (unsigned)H, (unsigned)B);
+    cfg.blockDim = dim3(kAThreads, 1, 1);
+    cfg.dynamicSmemBytes = kASmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_attn_kernel, maps, a);
+}
+
+// Reads this file's error word into *out and clears it, in stream order.
+cudaError_t prefill_error_fetch(int* out, cudaStream_t stream) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_prefill_error, sizeof(int), 0, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    static const int zero = 0;
+    return cudaMemcpyToSymbolAsync(g_prefill_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, stream);
+}
+
+}  // namespace mla
