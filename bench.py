@@ -75,6 +75,10 @@ def parse():
     p.add_argument("--eager", action="store_true", help="time eager C-ABI calls instead of replaying a CUDA graph")
     p.add_argument("--no-workloads", action="store_true", help="skip the decode-only lines of the other workloads")
     p.add_argument("--decode-calls", type=int, default=400, help="decode calls per workload in `workloads`")
+    p.add_argument("--prefill-only", action="store_true",
+                   help="time only the prefill workload and print its object (a short run for a profiler)")
+    p.add_argument("--prefill-batch", type=int, default=8, help="prompts in the prefill workload")
+    p.add_argument("--prefill-calls", type=int, default=5)
     return p.parse_args()
 
 
@@ -351,6 +355,68 @@ def decode_only(torch, api, L, gen, name, rank, dev, l2, peaks, calls):
     return r
 
 
+def prefill_flops(inp):
+    """Algorithmic FLOPs of one naive-form prefill call: per visible (query row,
+    key) pair 2 x (192 + 128) (score over [k_nope | k_rope], then V), plus the
+    per-head decompression of every cached token, 2 x H x 512 x (128 + 128)."""
+    s = inp.seqlens.clamp(min=0).long()
+    if inp.causal:
+        pairs = sum(int((s - inp.s_q + q + 1).clamp(min=0).sum()) for q in range(inp.s_q))
+    else:
+        pairs = int(s.sum()) * inp.s_q
+    attn = pairs * inp.H * 2 * (192 + 128)
+    decomp = int(s.sum()) * inp.H * 2 * 512 * (128 + 128)
+    return attn, decomp
+
+
+def prefill_only(torch, api, gen, rank, dev, peaks, calls=5, batch=8):
+    """Duration of one mla_prefill_paged call (gather, two decompression GEMMs,
+    causal attention) on the prefill workload, timed with CUDA events over
+    `calls` back-to-back calls on one stream; q alone (800 MB) exceeds the L2,
+    so every call streams its inputs from HBM."""
+    inp = gen.make_workload("prefill", rep=1000 * rank, B=batch)
+    d = inp.to(dev)
+    stream = torch.cuda.Stream(dev)
+    n = api.mla_prefill_workspace_size(inp.B, inp.H, inp.max_blocks_per_seq)
+    ws = torch.empty(n + 1024, dtype=torch.uint8, device=dev)
+    off = (-ws.data_ptr()) % 1024
+    ws = ws[off:off + n]
+    out = torch.empty((inp.B, inp.s_q, inp.H, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((inp.B, inp.s_q, inp.H), dtype=torch.float32, device=dev)
+
+    def call():
+        api.mla_prefill_paged(d.q, d.kv_cache, d.block_table, d.seqlens, d.w_uk, d.w_uv, d.scale, True, out=out,
+                              lse=lse, workspace=ws, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(calls):
+            call()
+        b.record(stream)
+        b.synchronize()
+    ms = a.elapsed_time(b) / calls
+    st = api.mla_read_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error on prefill: {api.status_string(st)}")
+    attn, decomp = prefill_flops(inp)
+    tc_peak = peaks[1]
+    tflops = (attn + decomp) / (ms * 1e-3) / 1e12
+    r = {"workload": (f"prefill: B={inp.B} whole prompts of {int(inp.seqlens[0])} tokens (s_q = seqlen), H={inp.H}, "
+                      f"causal, naive form (gather, per-head K and V decompression GEMMs, flash attention)"),
+         "bound": "tensor", "avg_call_us": round(ms * 1e3, 1), "achieved": round(tflops, 1), "peak": tc_peak,
+         "unit": "TFLOP/s", "frac": round(tflops / tc_peak, 4), "algorithmic_flops_per_call": attn + decomp,
+         "attention_flops": attn, "decompression_flops": decomp, "calls": calls,
+         "binding_roofline_us": round((attn + decomp) / (tc_peak * 1e12) * 1e6, 1),
+         "l2": f"inputs larger than L2 (q {d.q.numel() * 2 / 1e6:.0f} MB)", "launches_per_call": 4}
+    del d, ws, out, lse
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return r
+
+
 def describe(inp):
     sl = inp.seqlens
     lens = f"seqlen {int(sl[0])}" if bool((sl == sl[0]).all()) else f"seqlens {int(sl.min())}..{int(sl.max())}"
@@ -374,6 +440,8 @@ def run_ours(args, world, rank, local):
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20)
     peaks = measured_peaks()
+    if args.prefill_only:
+        return prefill_only(torch, api, gen, rank, dev, peaks, args.prefill_calls, args.prefill_batch)
 
     sets, per_set = input_sets(gen, args.workload, rank, dev, l2, args.sets)
     n_sets = len(sets)
@@ -509,6 +577,7 @@ def run_ours(args, world, rank, local):
         for name in DECODE_WORKLOADS:
             if name != args.workload:
                 wl[name] = decode_only(torch, api, L, gen, name, rank, dev, l2, peaks, args.decode_calls)
+        wl["prefill"] = prefill_only(torch, api, gen, rank, dev, peaks, args.prefill_calls, args.prefill_batch)
         result["workloads"] = wl
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
         result["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0)

@@ -7,10 +7,11 @@
 // decode kernel for Hopper GPUs", usage example) but not the formula; this is
 // the standard merge of softmax pieces.
 //
-// Work units of four query rows (b, s, h .. h + 3), one warp per row, so that
-// even a few long sequences spread over many SMs; a CTA walks a contiguous
-// range of units (consecutive units mostly share their batch, so a batch that
-// was not split costs one cached read per unit). Each lane owns 16 of the 512 latent
+// One warp per query row (b, s, h). Rows are dealt to the warps of the grid
+// round-robin (row r goes to warp r mod the grid's warp count), so the rows of
+// the few split batches - contiguous in row order - spread evenly over every
+// warp instead of queueing on the handful of warps whose range holds them.
+// Each lane owns 16 of the 512 latent
 // columns as four float4 (coalesced 512-byte rows per instruction). The
 // lanes read the pieces' lse values and reduce max and sum by shuffles; the
 // pieces are then accumulated in ascending order, four at a time so that 16
@@ -26,11 +27,8 @@
 namespace mla {
 namespace {
 
-// 128 threads: with its ~110 registers a CTA still fits on an SM beside a
-// decode CTA, so the combine CTAs can wait at griddepcontrol before the
-// decode ends
 constexpr int kThreads = 128;
-constexpr int kRowsPerCta = kThreads / 32;
+constexpr int kWarpsPerCta = kThreads / 32;
 
 __device__ void combine_row(const int32_t* __restrict__ num_splits, int row, int s_q, int H,
                             const float* __restrict__ o_part, const float* __restrict__ lse_part,
@@ -109,23 +107,22 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __rest
     griddep_wait();
     griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int units = (rows + kRowsPerCta - 1) / kRowsPerCta;
-    const int per_cta = (units + (int)gridDim.x - 1) / (int)gridDim.x;
-    const int u0 = (int)blockIdx.x * per_cta, u1 = min(units, u0 + per_cta);
-    for (int base = u0; base < u1; base += 32) {
-        // the piece counts of this warp's rows in up to 32 units, read at once
-        // (lane j: unit base + j); only rows of split or empty batches have work
-        const int row_j = (base + lane) * kRowsPerCta + warp;  // ((b * s_q) + s) * H + h
+    const int stride = (int)gridDim.x * kWarpsPerCta;       // warps in the grid
+    const int gw = (int)blockIdx.x * kWarpsPerCta + warp;
+    for (long long base = gw; base < rows; base += 32LL * stride) {
+        // the piece counts of this warp's next 32 rows, read at once (lane j:
+        // row base + j * stride); only rows of split or empty batches have work
+        const long long row_j = base + (long long)lane * stride;  // ((b * s_q) + s) * H + h
         int n_j = 1;
-        if (base + lane < u1 && row_j < rows) {
-            const int b = row_j / (H * s_q);
+        if (row_j < rows) {
+            const int b = (int)(row_j / (H * s_q));
             n_j = num_splits[b + 1] - num_splits[b];
         }
         unsigned todo = __ballot_sync(0xffffffffu, n_j != 1);
         while (todo) {
             const int j = __ffs(todo) - 1;
             todo &= todo - 1;
-            combine_row(num_splits, (base + j) * kRowsPerCta + warp, s_q, H, o_part, lse_part, o_lat, lse);
+            combine_row(num_splits, (int)(base + (long long)j * stride), s_q, H, o_part, lse_part, o_lat, lse);
         }
     }
 }
@@ -136,12 +133,13 @@ cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, con
                            const float* lse_part, void* o_lat, float* lse, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     const int rows = B * s_q * H;
-    const int units = (rows + kRowsPerCta - 1) / kRowsPerCta;
+    const int ctas = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
     const int sm_count = device_sm_count();
     if (sm_count <= 0) return cudaErrorInvalidDevice;
-    // at most two CTAs per SM: enough rows in flight for a few long sequences
-    // whose pieces cover the whole part list
-    cfg.gridDim = dim3(units < 1 ? 1 : (units < 2 * sm_count ? units : 2 * sm_count), 1, 1);
+    // up to four CTAs (16 warps) per SM: each split row is a chain of two
+    // dependent memory round trips (its pieces' lse, then their partial
+    // outputs), so the rows of the whole grid are kept in flight at once
+    cfg.gridDim = dim3(ctas < 1 ? 1 : (ctas < 4 * sm_count ? ctas : 4 * sm_count), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

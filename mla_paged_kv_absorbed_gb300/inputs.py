@@ -21,6 +21,8 @@ d_c = 512, rope 64, 64-token bf16 pages, softmax scale 1/sqrt(192)):
   varlen    B=64,  s_q=1, H=128, seqlen ~ U[129, 1152]      (q_abs drawn directly)
   long      B=16,  s_q=1, H=128, seqlen ~ U[16384, 32768]   (q_abs drawn directly)
   spec      B=132, s_q=2, H=128, seqlen 4096, causal        (end to end)
+  prefill   B=8, whole prompts of 2048 tokens (s_q = seqlen = 2048), H=128,
+            causal; for the naive-form prefill over the same paged cache
 """
 from __future__ import annotations
 
@@ -45,8 +47,9 @@ WORKLOADS = {
     "varlen": dict(B=64, s_q=1, H=128, seqlens=(129, 1152), q_mode="q_abs", causal=True),
     "long": dict(B=16, s_q=1, H=128, seqlens=(16384, 32768), q_mode="q_abs", causal=True),
     "spec": dict(B=132, s_q=2, H=128, seqlens=4096, q_mode="q", causal=True),
+    "prefill": dict(B=8, s_q=2048, H=128, seqlens=2048, q_mode="q", causal=True),
 }
-WORKLOAD_ORDER = ["tiny", "dsv3", "varlen", "long", "spec"]
+WORKLOAD_ORDER = ["tiny", "dsv3", "varlen", "long", "spec", "prefill"]
 
 
 @dataclass
