@@ -23,6 +23,11 @@ Parity status per function (how each is pinned, see tests/test_oracle_pins.py):
   rope, cache_append                                 - pinned (identity at
       position 0, exact quarter and half turns, norm preservation, relative
       position, composition; bit-exact latent copy into the table's slot)
+  quantize_latent, quantize_cache, dequantize_cache,
+  attend_absorbed_q8                                 - pinned (hand-derived
+      codes and scales incl. ties and the power-of-two boundary, the record
+      bytes, round-trip bounds, lossless round trip of exactly representable
+      latents, attention over a losslessly quantised cache == bf16 attention)
 """
 from __future__ import annotations
 
@@ -85,6 +90,9 @@ def _load():
         lib.orc_rope.argtypes = [P, I64, I, P, D, P]
         lib.orc_prefill_naive.argtypes = [P, P, P, I, P, I, I, I, P, P, D, I, P, P]
         lib.orc_cache_append.argtypes = [P, P, I, P, I, I, D, P]
+        lib.orc_quantize_latent.argtypes = [P, I64, P, P]
+        lib.orc_quantize_cache.argtypes = [P, I64, P, P]
+        lib.orc_dequantize_cache.argtypes = [P, P, I64, P]
         _lib = lib
         return lib
 
@@ -264,3 +272,46 @@ def prefill_naive(q, kv, block_table, seqlens, w_uk, w_uv, scale: float, causal:
     _load().orc_prefill_naive(_ptr(q), _ptr(kv), _ptr(bt), bt.shape[1], _ptr(sl), B, s_q, H, _ptr(wk), _ptr(wv),
                               float(scale), int(bool(causal)), _ptr(out), _ptr(lse))
     return out, lse
+
+
+def quantize_latent(x):
+    """Per-token INT8 quantisation of latents x [..., 512] -> (codes int8 [..., 512],
+    scale float32 [...]), scale a power of two (see mla_oracle.c)."""
+    x = _arr(x, np.float32)
+    assert x.shape[-1] == D_LATENT
+    rows = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
+    codes = np.empty(x.shape, np.int8)
+    scale = np.empty(x.shape[:-1], np.float32)
+    _load().orc_quantize_latent(_ptr(x), rows, _ptr(codes), _ptr(scale))
+    return codes, scale
+
+
+def quantize_cache(kv):
+    """kv [..., 576] (bf16 values as float32) -> (records uint8 [..., 640], scale float32 [...]):
+    record = [512 INT8 codes | 64 bf16 rope values, little-endian]."""
+    kv = _arr(kv, np.float32)
+    assert kv.shape[-1] == D_QK
+    bits = kv.view(np.uint32)
+    assert not np.any(bits[..., D_LATENT:] & 0xFFFF), "rope values must be exact bf16"
+    tokens = int(np.prod(kv.shape[:-1]))
+    rec = np.empty(kv.shape[:-1] + (640,), np.uint8)
+    scale = np.empty(kv.shape[:-1], np.float32)
+    _load().orc_quantize_cache(_ptr(kv), tokens, _ptr(rec), _ptr(scale))
+    return rec, scale
+
+
+def dequantize_cache(rec, scale):
+    """records [..., 640] uint8 + scale [...] -> the cache they stand for, float32 [..., 576]."""
+    rec = _arr(rec, np.uint8)
+    scale = _arr(scale, np.float32)
+    assert rec.shape[-1] == 640 and rec.shape[:-1] == scale.shape
+    tokens = int(np.prod(rec.shape[:-1]))
+    kv = np.empty(rec.shape[:-1] + (D_QK,), np.float32)
+    _load().orc_dequantize_cache(_ptr(rec), _ptr(scale), tokens, _ptr(kv))
+    return kv
+
+
+def attend_absorbed_q8(q_abs, rec, scale, block_table, seqlens, softmax_scale: float, causal: bool = True):
+    """Decode over a quantised cache (records [num_blocks, 64, 640], scale [num_blocks, 64]):
+    the absorbed-form attention over the cache the records stand for."""
+    return attend_absorbed(q_abs, dequantize_cache(rec, scale), block_table, seqlens, softmax_scale, causal)

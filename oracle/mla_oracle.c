@@ -533,6 +533,91 @@ void orc_cache_append(const float* kv_new, const int32_t* block_table, int mbps,
         }
 }
 
+/*
+ * Quantised latent cache [V3 sec. 7.2: the compressed latent is stored in 8
+ * bits, c_t = Quantize(W_DKV h_t, bits = 8); DS1 sec. 3.1 names INT8 as the
+ * representative KV quantisation]. The pages fix the width and nothing else.
+ * Reading used here:
+ *  - the quantised object is the per-token latent c_t (512 dims); the
+ *    decoupled rope key is not part of c_KV and stays bf16;
+ *  - symmetric INT8 codes in [-127, 127] with one scale per token;
+ *  - the scale is the smallest power of two s with 127 s >= max_c |c_t[c]|
+ *    (so c / s is exact and every code * s is exactly representable in bf16);
+ *  - code = c / s rounded to the nearest integer, ties to even;
+ *  - a token whose latent is all zero has s = 1 and all codes 0.
+ * The smallest power of two: write amax = m 2^k with m in [0.5, 1) (frexp);
+ * 127 * 2^(k-7) >= amax iff m <= 127/128, else 2^(k-6) is the smallest (64 m <=
+ * 63.99 < 127 and 128 m > 127).
+ * x [rows, 512] float -> codes [rows, 512] int8, scale [rows] float.
+ */
+void orc_quantize_latent(const float* x, int64_t rows, int8_t* codes, float* scale) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* xr = x + r * ORC_DC;
+        double amax = 0.0;
+        for (int c = 0; c < ORC_DC; ++c) amax = fmax(amax, fabs((double)xr[c]));
+        double s = 1.0;
+        if (amax > 0.0) {
+            int k;
+            double m = frexp(amax, &k);
+            s = ldexp(1.0, m <= 127.0 / 128.0 ? k - 7 : k - 6);
+        }
+        scale[r] = (float)s;
+        for (int c = 0; c < ORC_DC; ++c) {
+            double q = nearbyint((double)xr[c] / s);  /* default rounding: to nearest, ties to even */
+            codes[r * ORC_DC + c] = (int8_t)q;
+        }
+    }
+}
+
+/*
+ * The quantised cache as stored: one 640-byte record per token,
+ *   bytes [0, 512)   the INT8 codes of c_KV (orc_quantize_latent),
+ *   bytes [512, 640) k_rope as 64 bf16 values, little-endian, unchanged,
+ * and the scales as a separate float array [tokens]. kv [tokens, 576] holds
+ * values that are exact in bf16 (the rope part is copied bit for bit).
+ */
+void orc_quantize_cache(const float* kv, int64_t tokens, uint8_t* rec, float* scale) {
+    float* lat = (float*)malloc(sizeof(float) * ORC_DC * (tokens > 0 ? tokens : 1));
+    int8_t* codes = (int8_t*)malloc(ORC_DC * (tokens > 0 ? tokens : 1));
+    for (int64_t t = 0; t < tokens; ++t)
+        for (int c = 0; c < ORC_DC; ++c) lat[t * ORC_DC + c] = kv[t * ORC_DQK + c];
+    orc_quantize_latent(lat, tokens, codes, scale);
+    for (int64_t t = 0; t < tokens; ++t) {
+        uint8_t* out = rec + t * 640;
+        memcpy(out, codes + t * ORC_DC, ORC_DC);
+        for (int d = 0; d < ORC_DR; ++d) {
+            uint32_t bits;
+            float v = kv[t * ORC_DQK + ORC_DC + d];
+            memcpy(&bits, &v, 4);
+            out[ORC_DC + 2 * d] = (uint8_t)((bits >> 16) & 0xFF);
+            out[ORC_DC + 2 * d + 1] = (uint8_t)(bits >> 24);
+        }
+    }
+    free(lat);
+    free(codes);
+}
+
+/*
+ * The cache the quantised records stand for: latent = code * scale (exact),
+ * rope = the stored bf16 values. rec [tokens, 640] bytes, scale [tokens] ->
+ * kv [tokens, 576] float. Attention over a quantised cache is attention over
+ * this cache (orc_attend_absorbed).
+ */
+void orc_dequantize_cache(const uint8_t* rec, const float* scale, int64_t tokens, float* kv) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < tokens; ++t) {
+        const uint8_t* in = rec + t * 640;
+        for (int c = 0; c < ORC_DC; ++c) kv[t * ORC_DQK + c] = (float)((double)(int8_t)in[c] * (double)scale[t]);
+        for (int d = 0; d < ORC_DR; ++d) {
+            uint32_t bits = ((uint32_t)in[ORC_DC + 2 * d] << 16) | ((uint32_t)in[ORC_DC + 2 * d + 1] << 24);
+            float v;
+            memcpy(&v, &bits, 4);
+            kv[t * ORC_DQK + ORC_DC + d] = v;
+        }
+    }
+}
+
 /* Threads the OpenMP runtime will use (1 when built without OpenMP). */
 int orc_num_threads(void) {
 #ifdef _OPENMP
