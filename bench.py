@@ -56,6 +56,7 @@ METRIC = "paged MLA decode µs/call, achieved HBM GB/s & TFLOPS vs GB300 rooflin
 UNIT = "us/call"
 WORKLOAD = "spec"
 DECODE_WORKLOADS = ["dsv3", "varlen", "long"]
+Q8_WORKLOADS = ["dsv3", "varlen", "long", "spec"]  # decode-only lines over the INT8 cache
 FLOP_PER_PAIR = 2 * (576 + 512)          # score + value MACs per visible (query row, key)
 FLOP_PROJ_PER_ROW = 2 * 128 * 512        # absorb or out-proj MACs per (b, s, h), x2 flops
 
@@ -198,7 +199,7 @@ class StepArgs:
     """Pre-marshalled C-ABI arguments of one step over one resident input set.
     Decode-only workloads (q_abs drawn directly) have no absorb or out-proj."""
 
-    def __init__(self, api, inp, num_parts, workspace, stream_ptr):
+    def __init__(self, api, inp, num_parts, workspace, stream_ptr, q8=None):
         import torch
         d = inp
         self.inp = d
@@ -222,6 +223,13 @@ class StepArgs:
                        workspace.numel(), st)
         self.proj = None if self.out is None else (P(self.o_lat.data_ptr()), P(d.w_uv.data_ptr()),
                                                    P(self.out.data_ptr()), B, s_q, H, st)
+        # INT8 cache (records, scales) of the same input set, when given
+        self.q8 = q8
+        self.decode_q8 = None if q8 is None else (
+            P(self.q_abs.data_ptr()), P(q8[0].data_ptr()), P(q8[1].data_ptr()), d.kv_cache.shape[0],
+            P(d.block_table.data_ptr()), d.block_table.shape[1], P(d.seqlens.data_ptr()), B, s_q, H,
+            P(self.tm.data_ptr()), P(self.ns.data_ptr()), num_parts, ctypes.c_float(d.scale), int(d.causal),
+            P(self.o_lat.data_ptr()), P(self.lse.data_ptr()), P(workspace.data_ptr()), workspace.numel(), st)
 
 
 def run_step(L, a: StepArgs, ev=None, meta=False):
@@ -275,13 +283,16 @@ def workload_flops(inp):
     return attn, proj
 
 
-def roofline_of(inp, dec_ms, peaks):
+Q8_TOKEN_BYTES = 640 + 4  # INT8 cache: a token's record plus its scale
+
+
+def roofline_of(inp, dec_ms, peaks, kv_bytes=None):
     """Roofline of one decode call on `inp` lasting dec_ms: the binding bound is
     the slower of the latent-cache bytes at the measured HBM copy rate and the
     attention FLOPs at the measured dense bf16 rate (burst: the call is timed
     alone); the fraction against the sustained bf16 rate is reported beside it."""
     hbm_peak, tc_peak, tc_sustained, peak_src = peaks
-    kv_bytes = inp.kv_bytes()
+    kv_bytes = inp.kv_bytes() if kv_bytes is None else kv_bytes
     attn_flops, _ = workload_flops(inp)
     gbs = kv_bytes / (dec_ms * 1e-3) / 1e9
     tflops = attn_flops / (dec_ms * 1e-3) / 1e12
@@ -311,16 +322,31 @@ def input_sets(gen, name, rank, dev, l2, n_sets=0):
     return sets, per_set
 
 
-def decode_only(torch, api, L, gen, name, rank, dev, l2, peaks, calls):
+def decode_only(torch, api, L, gen, name, rank, dev, l2, peaks, calls, q8=False):
     """Decode-call duration on workload `name` (graph of `calls` decode calls
     over rotating input sets; the absorbed query of end-to-end workloads is
-    made once per set beforehand) and its roofline."""
-    sets, per_set = input_sets(gen, name, rank, dev, l2)
+    made once per set beforehand) and its roofline. q8: the same workload with
+    its cache quantised to the INT8 format (mla_quantize_cache, before timing)
+    and decoded by mla_decode_paged_q8."""
+    n_sets = 0
+    if q8:
+        probe = gen.make_workload(name, rep=1000 * rank)
+        q_bytes = probe.B * probe.s_q * probe.H * 576 * 2
+        per = int(probe.seqlens.clamp(min=0).sum()) * Q8_TOKEN_BYTES + q_bytes
+        n_sets = max(2, math.ceil(2.0 * l2 / per) + 1)
+        del probe
+    sets, per_set = input_sets(gen, name, rank, dev, l2, n_sets)
     B, s_q, H = sets[0].B, sets[0].s_q, sets[0].H
     num_parts = api.mla_default_num_parts(dev.index, s_q)
     ws = api.make_workspace(B, s_q, H, num_parts, dev)
     stream = torch.cuda.Stream(dev)
-    steps = [StepArgs(api, s, num_parts, ws, stream.cuda_stream) for s in sets]
+    q8c = [api.mla_quantize_cache(s.kv_cache) for s in sets] if q8 else [None] * len(sets)
+    torch.cuda.synchronize()
+    steps = [StepArgs(api, s, num_parts, ws, stream.cuda_stream, q) for s, q in zip(sets, q8c)]
+    call = L.mla_decode_paged_q8 if q8 else L.mla_decode_paged
+
+    def args_of(a):
+        return a.decode_q8 if q8 else a.decode
     rc = 0
     with torch.cuda.stream(stream):
         for a in steps:
@@ -328,7 +354,7 @@ def decode_only(torch, api, L, gen, name, rank, dev, l2, peaks, calls):
             if a.absorb is not None:
                 rc |= L.mla_absorb_q(*a.absorb)
         for i in range(3 * len(steps)):
-            rc |= L.mla_decode_paged(*steps[i % len(steps)].decode)
+            rc |= call(*args_of(steps[i % len(steps)]))
         stream.synchronize()
     if rc != 0 or api.mla_read_device_error(ws) != 0:
         raise RuntimeError(f"decode failed on {name}")
@@ -336,7 +362,7 @@ def decode_only(torch, api, L, gen, name, rank, dev, l2, peaks, calls):
     def body():
         r = 0
         for i in range(calls):
-            r |= L.mla_decode_paged(*steps[i % len(steps)].decode)
+            r |= call(*args_of(steps[i % len(steps)]))
         return r
     g = capture(torch, stream, body)
     if g is None:
@@ -345,11 +371,16 @@ def decode_only(torch, api, L, gen, name, rank, dev, l2, peaks, calls):
     st = api.mla_read_device_error(ws)
     if st != 0:
         raise RuntimeError(f"device error on {name}: {api.status_string(st)}")
-    r = roofline_of(sets[0], ms, peaks)
+    kvb = int(sets[0].seqlens.clamp(min=0).sum()) * Q8_TOKEN_BYTES if q8 else None
+    r = roofline_of(sets[0], ms, peaks, kvb)
+    if q8:
+        q_bytes = B * s_q * H * 576 * 2
+        per_set = kvb + q_bytes
+        r.update({"cache": "INT8 records (512 codes + 64 bf16 rope) + fp32 scale per token, 644 bytes"})
     r.update({"workload": describe(sets[0]), "num_parts": num_parts, "calls": calls,
               "l2": f"rotate {len(sets)} input sets, {len(sets) * per_set / 1e6:.0f} MB > 2 x L2",
-              "traffic": recorded_traffic(name)})
-    del g, steps, sets, ws
+              "traffic": None if q8 else recorded_traffic(name)})
+    del g, steps, sets, ws, q8c
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return r
@@ -577,6 +608,8 @@ def run_ours(args, world, rank, local):
         for name in DECODE_WORKLOADS:
             if name != args.workload:
                 wl[name] = decode_only(torch, api, L, gen, name, rank, dev, l2, peaks, args.decode_calls)
+        for name in Q8_WORKLOADS:
+            wl[name + "_int8"] = decode_only(torch, api, L, gen, name, rank, dev, l2, peaks, args.decode_calls, q8=True)
         wl["prefill"] = prefill_only(torch, api, gen, rank, dev, peaks, args.prefill_calls, args.prefill_batch)
         result["workloads"] = wl
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:

@@ -225,6 +225,55 @@ int mla_rope_append(mla_bf16_t* q, const mla_bf16_t* kv_new, const int32_t* cach
                     float rope_base, mla_stream_t stream);
 
 /*
+ * INT8 latent cache. Pages: [V3] sec. 7.2 (the compressed latent is stored in
+ * 8 bits, c_t = Quantize(W_DKV h_t, bits = 8)); [DS1] sec. 3.1 (INT8 as the
+ * representative KV quantisation). The pages fix only the width; this library
+ * reads it as:
+ *   kv8      uint8 [num_blocks, 64, 640]: per token a 640-byte record, bytes
+ *            0..511 the INT8 codes of c_KV, bytes 512..639 k_rope as 64 bf16
+ *            values (the decoupled rope key is not part of c_KV), unchanged;
+ *   kv_scale fp32 [num_blocks, 64]: one scale per token, the smallest power of
+ *            two s with 127 s >= max_c |c_KV[c]| (s = 1 for an all-zero latent);
+ *   code = c_KV / s rounded to nearest, ties to even, in [-127, 127].
+ * The token stands for [code * s | k_rope]; with a power-of-two s every code * s
+ * is exact in bf16, so the decode over kv8 equals the bf16 decode over the
+ * cache of those values (bit for bit, same schedule). Latent values are
+ * finite; their maximum is at least 2^-119 or all of them are zero.
+ */
+
+/*
+ * mla_quantize_cache - bf16 cache rows -> INT8 records and scales.
+ * kv: bf16 [tokens, 576] (e.g. a whole [num_blocks, 64, 576] cache); kv8 (out):
+ * uint8 [tokens, 640]; kv_scale (out): fp32 [tokens]. All 16-byte aligned.
+ * One warp per token, one launch.
+ */
+int mla_quantize_cache(const mla_bf16_t* kv, long long tokens, uint8_t* kv8, float* kv_scale, mla_stream_t stream);
+
+/*
+ * mla_rope_append_q8 - mla_rope_append into an INT8 cache: the same rotation
+ * of q's rope parts, and the new token's slot receives its record (codes of
+ * kv_new[b,s,0:512] under its scale, then RoPE(kv_new[b,s,512:576], t) in bf16)
+ * and its scale. Same arguments and errors as mla_rope_append, with kv8 uint8
+ * [num_blocks, 64, 640] and kv_scale fp32 [num_blocks, 64] in place of kv_cache.
+ */
+int mla_rope_append_q8(mla_bf16_t* q, const mla_bf16_t* kv_new, const int32_t* cache_seqlens,
+                       const int32_t* block_table, int max_blocks_per_seq, uint8_t* kv8, float* kv_scale,
+                       int num_blocks, int B, int s_q, int H, float rope_base, mla_stream_t stream);
+
+/*
+ * mla_decode_paged_q8 - mla_decode_paged over an INT8 cache (kv8, kv_scale as
+ * above; both 16-byte aligned). Same arguments, outputs, workspace and errors
+ * as mla_decode_paged. Each CTA loads a page's 32 KB of codes (plus, on the
+ * score side, its 8 KB of rope keys and 256 bytes of scales) instead of 72 KB
+ * and expands it to bf16 in shared memory before the tensor-core products.
+ */
+int mla_decode_paged_q8(const mla_bf16_t* q_abs, const uint8_t* kv8, const float* kv_scale, int num_blocks,
+                        const int32_t* block_table, int max_blocks_per_seq, const int32_t* cache_seqlens, int B,
+                        int s_q, int H, const int32_t* tile_meta, const int32_t* num_splits, int num_parts,
+                        float softmax_scale, int causal, mla_bf16_t* o_lat, float* lse, void* workspace,
+                        size_t workspace_bytes, mla_stream_t stream);
+
+/*
  * mla_prefill_paged - prefill over the same paged latent cache, in the naive
  * (decompress) form. Pages: [V3] sec. 2.2 (k = W_UK c, v = W_UV c), sec. 3.1
  * (the rope key is shared by the heads), sec. 4.3 (the paged module

@@ -29,6 +29,7 @@ PAGE = 64
 D_QK = 576
 D_LATENT = 512
 D_Q = 192
+Q8_RECORD = 640  # bytes per token of the INT8 cache: 512 codes + 64 bf16 rope values
 D_V = 128
 
 _lock = threading.Lock()
@@ -82,6 +83,12 @@ def lib() -> ctypes.CDLL:
         L.mla_prefill_paged.restype = I
         L.mla_rope_append.argtypes = [P, P, P, P, I, P, I, I, I, I, F, P]
         L.mla_rope_append.restype = I
+        L.mla_quantize_cache.argtypes = [P, LL, P, P, P]
+        L.mla_quantize_cache.restype = I
+        L.mla_rope_append_q8.argtypes = [P, P, P, P, I, P, P, I, I, I, I, F, P]
+        L.mla_rope_append_q8.restype = I
+        L.mla_decode_paged_q8.argtypes = [P, P, P, I, P, I, P, I, I, I, P, P, I, F, I, P, P, P, SZ, P]
+        L.mla_decode_paged_q8.restype = I
         _lib = L
         return L
 
@@ -201,18 +208,26 @@ def mla_absorb_q(q: torch.Tensor, w_uk: torch.Tensor, q_abs: Optional[torch.Tens
     return q_abs
 
 
-def _check_decode_inputs(q_abs, kv_cache, block_table, cache_seqlens, tile_meta, num_splits):
-    """dtype, device, contiguity and shape checks shared by both decode entry
+def _check_decode_inputs(q_abs, kv_cache, block_table, cache_seqlens, tile_meta, num_splits, kv_scale=None):
+    """dtype, device, contiguity and shape checks shared by the decode entry
     points (the C ABI sees only pointers, so a shape mismatch would make the
-    kernels read or write out of bounds). Returns (B, s_q, H)."""
+    kernels read or write out of bounds). kv_scale given: kv_cache is the INT8
+    cache (uint8 [num_blocks, 64, 640], scales fp32 [num_blocks, 64]).
+    Returns (B, s_q, H)."""
     _need(q_abs, "q_abs", torch.bfloat16, 4)
-    _need(kv_cache, "kv_cache", torch.bfloat16, 3)
+    if kv_scale is None:
+        _need(kv_cache, "kv_cache", torch.bfloat16, 3)
+    else:
+        _need(kv_cache, "kv8", torch.uint8, 3)
+        _need(kv_scale, "kv_scale", torch.float32, 2)
+        if tuple(kv_cache.shape[1:]) != (PAGE, Q8_RECORD) or tuple(kv_scale.shape) != (kv_cache.shape[0], PAGE):
+            raise ValueError("kv8 must be [num_blocks, 64, 640] and kv_scale [num_blocks, 64]")
     _need(block_table, "block_table", torch.int32, 2)
     _need(cache_seqlens, "cache_seqlens", torch.int32, 1)
     _need(tile_meta, "tile_meta", torch.int32, 2)
     _need(num_splits, "num_splits", torch.int32, 1)
     B, s_q, H, d = q_abs.shape
-    if d != D_QK or tuple(kv_cache.shape[1:]) != (PAGE, D_QK):
+    if d != D_QK or (kv_scale is None and tuple(kv_cache.shape[1:]) != (PAGE, D_QK)):
         raise ValueError("q_abs must be [B, s_q, H, 576] and kv_cache [num_blocks, 64, 576]")
     if block_table.shape[0] != B or cache_seqlens.shape[0] != B or num_splits.shape[0] != B + 1:
         raise ValueError("block_table, cache_seqlens and num_splits must match the batch of q_abs")
@@ -248,6 +263,72 @@ def mla_decode_paged(q_abs: torch.Tensor, kv_cache: torch.Tensor, block_table: t
         B, s_q, H, _p(tile_meta), _p(num_splits), num_parts, float(softmax_scale), int(bool(causal)),
         _p(o_lat), _p(lse), _p(workspace), workspace.numel(), _stream(stream)))
     return o_lat, lse
+
+
+def mla_decode_paged_q8(q_abs: torch.Tensor, kv8: torch.Tensor, kv_scale: torch.Tensor, block_table: torch.Tensor,
+                        cache_seqlens: torch.Tensor, tile_meta: torch.Tensor, num_splits: torch.Tensor,
+                        softmax_scale: float, causal: bool = True, o_lat: Optional[torch.Tensor] = None,
+                        lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                        stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """mla_decode_paged over the INT8 cache (kv8 uint8 [num_blocks, 64, 640],
+    kv_scale fp32 [num_blocks, 64]). See include/mla.h."""
+    B, s_q, H = _check_decode_inputs(q_abs, kv8, block_table, cache_seqlens, tile_meta, num_splits, kv_scale)
+    num_parts = tile_meta.shape[0]
+    if o_lat is None:
+        o_lat = torch.empty((B, s_q, H, D_LATENT), dtype=torch.bfloat16, device=q_abs.device)
+    if lse is None:
+        lse = torch.empty((B, s_q, H), dtype=torch.float32, device=q_abs.device)
+    if workspace is None:
+        workspace = make_workspace(B, s_q, H, num_parts, q_abs.device)
+    _check_decode_outputs(o_lat, lse, B, s_q, H)
+    _need(workspace, "workspace", torch.uint8, 1)
+    _check("mla_decode_paged_q8", lib().mla_decode_paged_q8(
+        _p(q_abs), _p(kv8), _p(kv_scale), kv8.shape[0], _p(block_table), block_table.shape[1], _p(cache_seqlens),
+        B, s_q, H, _p(tile_meta), _p(num_splits), num_parts, float(softmax_scale), int(bool(causal)),
+        _p(o_lat), _p(lse), _p(workspace), workspace.numel(), _stream(stream)))
+    return o_lat, lse
+
+
+def mla_quantize_cache(kv: torch.Tensor, kv8: Optional[torch.Tensor] = None, kv_scale: Optional[torch.Tensor] = None,
+                       stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """bf16 cache rows kv [..., 576] -> (kv8 uint8 [..., 640], kv_scale fp32 [...]). See include/mla.h."""
+    _need(kv, "kv", torch.bfloat16)
+    if kv.shape[-1] != D_QK:
+        raise ValueError("kv must be [..., 576]")
+    lead = tuple(kv.shape[:-1])
+    tokens = kv.numel() // D_QK
+    if kv8 is None:
+        kv8 = torch.empty(lead + (Q8_RECORD,), dtype=torch.uint8, device=kv.device)
+    if kv_scale is None:
+        kv_scale = torch.empty(lead, dtype=torch.float32, device=kv.device)
+    _need(kv8, "kv8", torch.uint8)
+    _need(kv_scale, "kv_scale", torch.float32)
+    if kv8.numel() != tokens * Q8_RECORD or kv_scale.numel() != tokens:
+        raise ValueError("kv8 must hold 640 bytes and kv_scale one float per row of kv")
+    _check("mla_quantize_cache", lib().mla_quantize_cache(_p(kv), tokens, _p(kv8), _p(kv_scale), _stream(stream)))
+    return kv8, kv_scale
+
+
+def mla_rope_append_q8(q: torch.Tensor, kv_new: torch.Tensor, cache_seqlens: torch.Tensor, block_table: torch.Tensor,
+                       kv8: torch.Tensor, kv_scale: torch.Tensor, rope_base: float = 10000.0, stream=None):
+    """mla_rope_append into the INT8 cache (q's rope parts rotated in place; the
+    new tokens' records and scales written). See include/mla.h."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(kv_new, "kv_new", torch.bfloat16, 3)
+    _need(cache_seqlens, "cache_seqlens", torch.int32, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(kv8, "kv8", torch.uint8, 3)
+    _need(kv_scale, "kv_scale", torch.float32, 2)
+    B, s_q, H, dq = q.shape
+    if dq != D_Q or tuple(kv_new.shape) != (B, s_q, D_QK) or tuple(kv8.shape[1:]) != (PAGE, Q8_RECORD):
+        raise ValueError("q must be [B, s_q, H, 192], kv_new [B, s_q, 576] and kv8 [num_blocks, 64, 640]")
+    if tuple(kv_scale.shape) != (kv8.shape[0], PAGE):
+        raise ValueError("kv_scale must be [num_blocks, 64]")
+    if block_table.shape[0] != B or cache_seqlens.shape[0] != B:
+        raise ValueError("block_table and cache_seqlens must match the batch of q")
+    _check("mla_rope_append_q8", lib().mla_rope_append_q8(
+        _p(q), _p(kv_new), _p(cache_seqlens), _p(block_table), block_table.shape[1], _p(kv8), _p(kv_scale),
+        kv8.shape[0], B, s_q, H, float(rope_base), _stream(stream)))
 
 
 def mla_out_proj(o_lat: torch.Tensor, w_uv: torch.Tensor, out: Optional[torch.Tensor] = None,

@@ -8,6 +8,7 @@
 
 #include "mla.h"
 #include "mla_internal.h"
+#include "quant.cuh"
 
 namespace mla {
 
@@ -224,18 +225,26 @@ int mla_out_proj(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla_bf16_t* ou
                      static_cast<cudaStream_t>(stream));
 }
 
-int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int num_blocks, const int32_t* block_table,
-                     int max_blocks_per_seq, const int32_t* cache_seqlens, int B, int s_q, int H,
-                     const int32_t* tile_meta, const int32_t* num_splits, int num_parts, float softmax_scale,
-                     int causal, mla_bf16_t* o_lat, float* lse, void* workspace, size_t workspace_bytes,
-                     mla_stream_t stream) {
-    if (!q_abs || !kv_cache || !block_table || !cache_seqlens || !tile_meta || !num_splits || !o_lat || !lse ||
-        !workspace)
+}  // extern "C"
+
+namespace mla {
+namespace {
+// The decode over either cache format: the bf16 cache (kv_cache, kv8 = NULL)
+// or the INT8 records with their scales (kv8 and kv_scale, kv_cache = NULL).
+int decode_impl(const mla_bf16_t* q_abs, const void* kv_cache, const void* kv8, const float* kv_scale, int num_blocks,
+                const int32_t* block_table, int max_blocks_per_seq, const int32_t* cache_seqlens, int B, int s_q,
+                int H, const int32_t* tile_meta, const int32_t* num_splits, int num_parts, float softmax_scale,
+                int causal, mla_bf16_t* o_lat, float* lse, void* workspace, size_t workspace_bytes,
+                mla_stream_t stream) {
+    const bool q8 = kv8 != nullptr;
+    if (!q_abs || (q8 ? (!kv_scale || kv_cache) : !kv_cache) || !block_table || !cache_seqlens || !tile_meta ||
+        !num_splits || !o_lat || !lse || !workspace)
         return MLA_ERR_INVALID_ARG;
+    if (q8 && (!aligned16(kv8) || !aligned16(kv_scale))) return MLA_ERR_INVALID_ARG;
     if (B <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || num_parts <= 0 || !valid_sq(s_q) || !valid_heads(H))
         return MLA_ERR_INVALID_ARG;
     if (!(softmax_scale > 0.f) || (causal != 0 && causal != 1)) return MLA_ERR_INVALID_ARG;
-    if (!aligned16(q_abs) || !aligned16(kv_cache) || !aligned16(o_lat) || !aligned16(lse) ||
+    if (!aligned16(q_abs) || (!q8 && !aligned16(kv_cache)) || !aligned16(o_lat) || !aligned16(lse) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return MLA_ERR_INVALID_ARG;
     if ((uint64_t)num_blocks * kPage > 0xFFFFFFFFull) return MLA_ERR_INVALID_ARG;
@@ -245,10 +254,29 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
     if (dev != MLA_OK) return dev;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    DecodeMaps maps;
-    // [dims, keys, chunk] views: one box per page (or per 64 query rows)
-    if (!make_kv_page_map(&maps.kv, kv_cache, num_blocks, kDQK / 64)) return MLA_ERR_CUDA;
-    if (!make_kv_page_map(&maps.v, kv_cache, num_blocks, kDLatent / 64)) return MLA_ERR_CUDA;
+    DecodeMaps maps = {};
+    if (q8) {
+        // the records as {128 code bytes, num_blocks * 64 keys, 4 planes}, strides
+        // {640, 128}: one box is a page's 32 KB of codes as four [64 keys][128 B]
+        // planes; the rope keys (bytes 512-639 of each record) as bf16 {64, keys}
+        const uint64_t keys = (uint64_t)num_blocks * kPage;
+        const uint64_t c_dims[3] = {128, keys, 4};
+        const uint64_t c_strides[2] = {(uint64_t)kQ8Record, 128};
+        const uint32_t c_box[3] = {128, (uint32_t)kPage, 4};
+        if (!make_tmap(&maps.kv8, kv8, 3, c_dims, c_strides, c_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_DATA_TYPE_UINT8))
+            return MLA_ERR_CUDA;
+        const uint64_t r_dims[2] = {(uint64_t)kDRope, keys};
+        const uint64_t r_strides[1] = {(uint64_t)kQ8Record};
+        const uint32_t r_box[2] = {(uint32_t)kDRope, (uint32_t)kPage};
+        if (!make_tmap(&maps.rope, static_cast<const uint8_t*>(kv8) + kDLatent, 2, r_dims, r_strides, r_box,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+            return MLA_ERR_CUDA;
+    } else {
+        // [dims, keys, chunk] views: one box per page (or per 64 query rows)
+        if (!make_kv_page_map(&maps.kv, kv_cache, num_blocks, kDQK / 64)) return MLA_ERR_CUDA;
+        if (!make_kv_page_map(&maps.v, kv_cache, num_blocks, kDLatent / 64)) return MLA_ERR_CUDA;
+    }
     const uint64_t rows = (uint64_t)B * s_q;
     const uint64_t qrows_total = rows * (uint64_t)H;
     const uint32_t qrows = (uint32_t)(qrows_total < 64 ? qrows_total : 64);
@@ -271,7 +299,7 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
                    CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
         return MLA_ERR_CUDA;
 
-    DecodeArgs a;
+    DecodeArgs a = {};
     a.q_abs = q_abs;
     a.block_table = block_table;
     a.mbps = max_blocks_per_seq;
@@ -293,12 +321,49 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
     a.err = reinterpret_cast<int*>(ws);
     a.wait_ns = g_wait_ns.load();
     a.withhold = g_withhold.load();
+    a.kv_scale = q8 ? kv_scale : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_decode(maps, a, st);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     e = launch_combine(num_splits, B, s_q, H, a.o_part, a.lse_part, o_lat, lse, st);
     return cuda_status(e);
 }
+}  // namespace
+}  // namespace mla
+
+extern "C" {
+
+int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int num_blocks, const int32_t* block_table,
+                     int max_blocks_per_seq, const int32_t* cache_seqlens, int B, int s_q, int H,
+                     const int32_t* tile_meta, const int32_t* num_splits, int num_parts, float softmax_scale,
+                     int causal, mla_bf16_t* o_lat, float* lse, void* workspace, size_t workspace_bytes,
+                     mla_stream_t stream) {
+    if (!kv_cache) return MLA_ERR_INVALID_ARG;
+    return mla::decode_impl(q_abs, kv_cache, nullptr, nullptr, num_blocks, block_table, max_blocks_per_seq,
+                            cache_seqlens, B, s_q, H, tile_meta, num_splits, num_parts, softmax_scale, causal, o_lat,
+                            lse, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_paged_q8(const mla_bf16_t* q_abs, const uint8_t* kv8, const float* kv_scale, int num_blocks,
+                        const int32_t* block_table, int max_blocks_per_seq, const int32_t* cache_seqlens, int B,
+                        int s_q, int H, const int32_t* tile_meta, const int32_t* num_splits, int num_parts,
+                        float softmax_scale, int causal, mla_bf16_t* o_lat, float* lse, void* workspace,
+                        size_t workspace_bytes, mla_stream_t stream) {
+    if (!kv8 || !kv_scale) return MLA_ERR_INVALID_ARG;
+    return mla::decode_impl(q_abs, nullptr, kv8, kv_scale, num_blocks, block_table, max_blocks_per_seq, cache_seqlens,
+                            B, s_q, H, tile_meta, num_splits, num_parts, softmax_scale, causal, o_lat, lse, workspace,
+                            workspace_bytes, stream);
+}
+
+int mla_quantize_cache(const mla_bf16_t* kv, long long tokens, uint8_t* kv8, float* kv_scale, mla_stream_t stream) {
+    if (!kv || !kv8 || !kv_scale || tokens <= 0) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(kv) || !aligned16(kv8) || !aligned16(kv_scale)) return MLA_ERR_INVALID_ARG;
+    int dev = check_device();
+    if (dev != MLA_OK) return dev;
+    return cuda_status(launch_quantize(kv, tokens, kv8, kv_scale, static_cast<cudaStream_t>(stream)));
+}
+
+
 
 int mla_read_device_error(void* workspace, mla_stream_t stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -435,7 +500,23 @@ int mla_rope_append(mla_bf16_t* q, const mla_bf16_t* kv_new, const int32_t* cach
     int dev = check_device();
     if (dev != MLA_OK) return dev;
     return cuda_status(launch_rope_append(q, kv_new, cache_seqlens, block_table, max_blocks_per_seq, kv_cache,
-                                          num_blocks, B, s_q, H, (double)rope_base, static_cast<cudaStream_t>(stream)));
+                                          nullptr, nullptr, num_blocks, B, s_q, H, (double)rope_base,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int mla_rope_append_q8(mla_bf16_t* q, const mla_bf16_t* kv_new, const int32_t* cache_seqlens,
+                       const int32_t* block_table, int max_blocks_per_seq, uint8_t* kv8, float* kv_scale,
+                       int num_blocks, int B, int s_q, int H, float rope_base, mla_stream_t stream) {
+    if (!q || !kv_new || !cache_seqlens || !block_table || !kv8 || !kv_scale || B <= 0 || num_blocks <= 0 ||
+        max_blocks_per_seq <= 0 || !valid_sq(s_q) || !valid_heads(H) || !(rope_base > 1.f))
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv_new) || !aligned16(kv8)) return MLA_ERR_INVALID_ARG;
+    if ((int64_t)B * s_q > 0x7FFFFFFF) return MLA_ERR_INVALID_ARG;
+    int dev = check_device();
+    if (dev != MLA_OK) return dev;
+    return cuda_status(launch_rope_append(q, kv_new, cache_seqlens, block_table, max_blocks_per_seq, nullptr, kv8,
+                                          kv_scale, num_blocks, B, s_q, H, (double)rope_base,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 int mla_debug_gather(const mla_bf16_t* kv_cache, int num_blocks, const int32_t* block_table, int max_blocks_per_seq,

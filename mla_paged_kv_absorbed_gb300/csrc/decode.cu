@@ -48,6 +48,7 @@
 
 #include "mla_internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace mla {
 namespace {
@@ -84,8 +85,11 @@ constexpr int kXRef = kXPair + 2 * 2 * 2 * kRows;  // [page parity][128]: refere
 constexpr int kXLSum = kXRef + 2 * kRows;          // [group][half][128]: a group's share of the row sum
 constexpr int kXLMax = kXLSum + 2 * 2 * kRows;     // [group][128]: the reference max that share is relative to
 constexpr int kXFloats = kXLMax + 2 * kRows;
-constexpr int kOffRole = 9216;
-static_assert(kOffX + 4 * kXFloats <= kOffRole, "exchange area");
+static_assert(kOffX + 4 * kXFloats <= 9216, "exchange area");
+// INT8 cache: the per-token scales of the page in each ring (or value) slot, 64 floats a slot
+constexpr int kOffScale = 9216;
+constexpr int kScaleBytes = kPage * 4;
+constexpr int kOffRole = 10240;
 // score CTA
 constexpr int kRing = 3;
 constexpr int kOffRing = kOffRole;
@@ -102,6 +106,13 @@ constexpr int kSmemUsed = kSmemScore > kSmemValue ? kSmemScore : kSmemValue;
 constexpr int kSmemBytes = kSmemUsed + 1024;       // room to align the base to 1024 bytes
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kOffP % 1024 == 0 && kOffV % 1024 == 0 && kOffRing % 1024 == 0, "swizzle atoms");
+static_assert(kOffScale + kRing * kScaleBytes <= kOffRole && kOffScale + kVRing * kScaleBytes <= kOffRole, "scales");
+// INT8 cache, in a page slot: the codes arrive as four planes [64 keys x 128 B]
+// (128-byte swizzle) at kQ8Planes and are expanded in place into the bf16
+// chunks 0-7; the score slot's rope key lands directly in chunk 8.
+constexpr int kQ8Planes = 4 * kChunkBytes;             // byte offset of the code planes in a slot
+constexpr uint32_t kQ8PageBytes = 4 * kChunkBytes + kChunkBytes + kScaleBytes;  // score slot: codes + rope + scales
+constexpr uint32_t kQ8VBytes = 4 * kChunkBytes + kScaleBytes;                   // value slot: codes + scales
 // one P message: P (16 KB) + rescale factor and 1/l per row (fp32)
 constexpr uint32_t kPMsgBytes = kPSlotBytes + 2 * kRows * 4;
 
@@ -126,6 +137,7 @@ struct Bars {
     uint64_t ref_full[2][4];  // [page parity][lane quadrant]: reference max of a page published
     uint64_t lsum_full[4];    // [lane quadrant]: the group without an item's last page published its row sums
     uint64_t drain2;          // second score MMA warp
+    uint64_t deq_full[2];     // INT8 cache: [page parity] the page is expanded to bf16 in its ring slot
     // value CTA
     uint64_t p_full[2];  // own arrive + expect_tx, bytes from the score CTA
     uint64_t v_full[kVRing], v_empty[kVRing];
@@ -134,6 +146,7 @@ struct Bars {
     uint64_t o_free[2];
     uint64_t stage_full, stage_free;  // epilogue rounds: eight warps staged / staging read by the store
     uint64_t drain;
+    uint64_t vdeq_full[kVRing];     // INT8 cache: the value slot is expanded to bf16
     uint32_t tmem_slot;
     int abort;
     int p_consumed;  // value CTA: P messages its MMA warp has taken (their successors are armed)
@@ -240,10 +253,49 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int slots, int issued
         mbar_wait(&full[r % slots], (r / slots) & 1, nullptr, err, kDrainNs);
 }
 
+// ============================================================= INT8 cache ==
+// Writes the 16 values of code unit u (plane p, key k) as bf16 into the page's
+// chunk 2p + u / 4 (128-byte swizzle), or zeros for a key past the valid ones.
+__device__ __forceinline__ void q8_store_unit(uint8_t* slot, int p, int k, int u, uint4 codes, float sc, bool live) {
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+    if (live) q8_dequant16(codes, sc, lo, hi);
+    uint8_t* row = slot + (2 * p + (u >> 2)) * kChunkBytes + k * 128;
+    const int w0 = 2 * (u & 3);
+    *reinterpret_cast<uint4*>(row + ((w0 ^ (k & 7)) << 4)) = lo;
+    *reinterpret_cast<uint4*>(row + (((w0 + 1) ^ (k & 7)) << 4)) = hi;
+}
+
+// Expands one page slot in place from INT8 codes to the bf16 page the MMAs read
+// (the codes stand for code * scale, exactly representable in bf16). Code
+// plane p (dims [128 p, 128 p + 128), [64 keys][128 B], 128-byte swizzle) sits at
+// slot + kQ8Planes + 8 KB p and becomes bf16 chunks 2p and 2p + 1 at slot +
+// 16 KB p; keys at or past `valid` become zeros. Eight warps share a page, warp
+// w8 taking keys [8 w8, 8 w8 + 8) of every plane (8 units of 16 codes per lane).
+// Row k of output chunk 4 + p is row k of code plane p, so a warp only
+// overwrites code rows of its own keys: it loads all of its codes first, and
+// needs no other warp.
+__device__ __forceinline__ void q8_expand_warp(uint8_t* slot, const float* sc, int valid, int w8, int lane) {
+    const int kr = lane >> 3, u = lane & 7;
+    uint4 c[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int p = i >> 1, k = 8 * w8 + 4 * (i & 1) + kr;
+        c[i] = *reinterpret_cast<const uint4*>(slot + kQ8Planes + p * kChunkBytes + k * 128 + ((u ^ (k & 7)) << 4));
+    }
+    const float s0 = sc[8 * w8 + kr], s1 = sc[8 * w8 + 4 + kr];
+    __syncwarp();  // every lane's codes are in registers before any lane overwrites code rows
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int p = i >> 1, k = 8 * w8 + 4 * (i & 1) + kr;
+        q8_store_unit(slot, p, k, u, c[i], (i & 1) ? s1 : s0, k < valid);
+    }
+}
+
 // ============================================================== score CTA ==
 // Ring positions: every batch first takes two positions for its query (rows
 // 0-63 and 64-127), then one per page; producer, MMA warp and softmax warps
 // count them the same way.
+template <bool kQ8>
 __device__ void score_producer(const DecodeMaps& maps, const DecodeArgs& args, Bars* bars, uint8_t* smem, int part,
                                int s, volatile int* abort) {
     // the whole warp runs this loop (warp-uniform waits); lane 0 issues the loads
@@ -297,8 +349,18 @@ __device__ void score_producer(const DecodeMaps& maps, const DecodeArgs& args, B
         if (lane == 0) {
             const int blk = checked_block(args, pi.it.b, pi.j, err, abort);
             uint64_t* bar = &bars->ring_full[r % kRing];
-            mbar_arrive_expect_tx(bar, (uint32_t)kPageBytes);
-            tma_load_3d(ring + (r % kRing) * kPageBytes, &maps.kv, bar, 0, blk * kPage, 0);
+            uint8_t* slot = ring + (r % kRing) * kPageBytes;
+            if (kQ8) {
+                // codes (four planes), the bf16 rope key straight into chunk 8, the scales
+                mbar_arrive_expect_tx(bar, kQ8PageBytes);
+                tma_load_3d(slot + kQ8Planes, &maps.kv8, bar, 0, blk * kPage, 0);
+                tma_load_2d(slot + 8 * kChunkBytes, &maps.rope, bar, 0, blk * kPage);
+                bulk_load(smem + kOffScale + (r % kRing) * kScaleBytes, args.kv_scale + (size_t)blk * kPage,
+                          kScaleBytes, bar);
+            } else {
+                mbar_arrive_expect_tx(bar, (uint32_t)kPageBytes);
+                tma_load_3d(slot, &maps.kv, bar, 0, blk * kPage, 0);
+            }
         }
         __syncwarp();
         ++r;
@@ -311,6 +373,7 @@ __device__ void score_producer(const DecodeMaps& maps, const DecodeArgs& args, B
 // Score products of the pages with parity `parity` (0 or 1, when two warps
 // share the pages), or of every page (parity < 0). Returns false when it gave
 // up (timeout or abort).
+template <bool kQ8>
 __device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uint32_t tmem, int part, int parity,
                           volatile int* abort) {
     int* err = args.err;
@@ -340,7 +403,10 @@ __device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
         if (parity < 0 || buf == parity) {
             // S buffer `buf` was read by the softmax of page n - 2
             if (n >= 2) ok = warp_wait(&bars->s_free[buf], ((n >> 1) - 1) & 1, abort, err, wait_ns);
-            if (ok) ok = warp_wait(&bars->ring_full[r % kRing], (r / kRing) & 1, abort, err, wait_ns);
+            // the page has landed (INT8 cache: and its softmax group has expanded it)
+            if (ok)
+                ok = kQ8 ? warp_wait(&bars->deq_full[n & 1], (n >> 1) & 1, abort, err, wait_ns)
+                         : warp_wait(&bars->ring_full[r % kRing], (r / kRing) & 1, abort, err, wait_ns);
             if (!ok) break;
             tc_fence_after();
             // the whole warp runs the issue loop (warp-uniform operands); one
@@ -382,8 +448,10 @@ __device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
 // Each group keeps its own share of the row sum; at an item's end the group
 // without the last page publishes its share, and the group with it adds both
 // for 1/l and lse.
+template <bool kQ8>
 __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem, uint32_t tmem, int part, int s,
                               uint32_t peer, volatile int* abort) {
+    static_assert(!kQ8 || kSoftmaxGroups == 2, "the INT8 expansion is done by the group that owns the page");
     int* err = args.err;
     const long long wait_ns = args.wait_ns;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -406,6 +474,7 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
     // chunks this warp moves into TMEM (the four warps of a quadrant share them)
     const int qbox = quad >> 1, qrow = 32 * (quad & 1) + lane;
     const int qpart = kSoftmaxGroups == 2 ? 2 * g + half : half;  // the quadrant's warps split the 9 chunks
+    const float* scales = reinterpret_cast<const float*>(smem + kOffScale);
     PageIter pi;
     pi.init(args, part);
     float m_own = -INFINITY, l = 0.f;  // this thread's share of the row sum, relative to m_own
@@ -462,6 +531,19 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
                 mbar_arrive(&bars->lsum_full[quad]);
             }
             continue;
+        }
+        if (kQ8) {
+            // this group's page: expand its codes in the ring slot before its
+            // score products can be issued (slot of ring position r - 1)
+            const int rp = r - 1, slot = rp % kRing;
+            if (ok) ok = warp_wait(&bars->ring_full[slot], (rp / kRing) & 1, abort, err, wait_ns);
+            if (ok) {
+                const int valid = min(kPage, pi.it.seqlen - pi.j * kPage);
+                q8_expand_warp(ring + slot * kPageBytes, scales + slot * kPage, valid, warp & 7, lane);
+                fence_proxy_async_smem();  // the tensor pipe reads the expanded page next
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->deq_full[g]);
+            }
         }
         float x[32];
         if (ok) ok = warp_wait(&bars->s_full[buf], (n >> 1) & 1, abort, err, wait_ns);
@@ -571,6 +653,7 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
 }
 
 // ============================================================== value CTA ==
+template <bool kQ8>
 __device__ void value_producer(const DecodeMaps& maps, const DecodeArgs& args, Bars* bars, uint8_t* smem, int part,
                                volatile int* abort) {
     int* err = args.err;
@@ -585,13 +668,21 @@ __device__ void value_producer(const DecodeMaps& maps, const DecodeArgs& args, B
         if (!ok) break;
         const int blk = checked_block(args, pi.it.b, pi.j, err, abort);
         uint64_t* bar = &bars->v_full[v % kVRing];
-        mbar_arrive_expect_tx(bar, (uint32_t)kVBytes);
-        tma_load_3d(vring + (v % kVRing) * kVBytes, &maps.v, bar, 0, blk * kPage, 0);
+        if (kQ8) {
+            mbar_arrive_expect_tx(bar, kQ8VBytes);
+            tma_load_3d(vring + (v % kVRing) * kVBytes + kQ8Planes, &maps.kv8, bar, 0, blk * kPage, 0);
+            bulk_load(smem + kOffScale + (v % kVRing) * kScaleBytes, args.kv_scale + (size_t)blk * kPage, kScaleBytes,
+                      bar);
+        } else {
+            mbar_arrive_expect_tx(bar, (uint32_t)kVBytes);
+            tma_load_3d(vring + (v % kVRing) * kVBytes, &maps.v, bar, 0, blk * kPage, 0);
+        }
         ++v;
     }
     drain_ring(bars->v_full, kVRing, v, err);
 }
 
+template <bool kQ8>
 __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uint32_t tmem, int part,
                           volatile int* abort) {
     int* err = args.err;
@@ -622,11 +713,13 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
         // a batch's first product overwrites O: its previous epilogue must have read it
         if (ok && first && qi > 0) ok = warp_wait(&bars->o_free[0], (qi - 1) & 1, abort, err, wait_ns);
         if (ok && first && qi > 0) ok = warp_wait(&bars->o_free[1], (qi - 1) & 1, abort, err, wait_ns);
-        if (ok) ok = warp_wait(&bars->v_full[n % kVRing], (n / kVRing) & 1, abort, err, wait_ns);
+        if (ok)
+            ok = kQ8 ? warp_wait(&bars->vdeq_full[n % kVRing], (n / kVRing) & 1, abort, err, wait_ns)
+                     : warp_wait(&bars->v_full[n % kVRing], (n / kVRing) & 1, abort, err, wait_ns);
         if (!ok) break;
         uint8_t* vs = vring + (n % kVRing) * kVBytes;
         const int tail = pi.j == pi.it.nblk - 1 ? pi.it.seqlen - pi.j * kPage : kPage;
-        if (tail < kPage) {
+        if (!kQ8 && tail < kPage) {  // (the INT8 expansion writes those rows as zeros)
             // rows past seqlen hold arbitrary bytes: zero them so that
             // 0-probability keys cannot inject NaN/Inf into P.V
             const int per_chunk = (kPage - tail) * 8;  // 16-byte words
@@ -664,6 +757,30 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
         warp_wait(&bars->drain, 0, nullptr, err, kDrainNs);
     }
     if (lane == 0) bars->p_consumed = consumed;
+    return ok;
+}
+
+// INT8 cache: warps 8-15 of the value CTA expand each value slot's codes to
+// bf16 (rows past the sequence as zeros) before its P.V products.
+__device__ bool value_expand(const DecodeArgs& args, Bars* bars, uint8_t* smem, int part, volatile int* abort) {
+    int* err = args.err;
+    const long long wait_ns = args.wait_ns;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* vring = smem + kOffV;
+    const float* scales = reinterpret_cast<const float*>(smem + kOffScale);
+    PageIter pi;
+    pi.init(args, part);
+    bool ok = true;
+    for (; ok && pi.valid; pi.advance()) {
+        const int n = pi.n, slot = n % kVRing;
+        ok = warp_wait(&bars->v_full[slot], (n / kVRing) & 1, abort, err, wait_ns);
+        if (!ok) break;
+        const int valid = min(kPage, pi.it.seqlen - pi.j * kPage);
+        q8_expand_warp(vring + slot * kVBytes, scales + slot * kPage, valid, warp - 8, lane);
+        fence_proxy_async_smem();  // the tensor pipe reads the expanded values next
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->vdeq_full[slot]);
+    }
     return ok;
 }
 
@@ -816,6 +933,7 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
     return ok;
 }
 
+template <bool kQ8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeMaps maps, DecodeArgs args) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -859,14 +977,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->stage_free, 1);
         mbar_init(&bars->drain, 1);
         mbar_init(&bars->drain2, 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&bars->deq_full[i], 8);
+        for (int i = 0; i < kVRing; ++i) mbar_init(&bars->vdeq_full[i], 8);
         bars->abort = 0;
         bars->p_consumed = 0;
         fence_mbarrier_init_cluster();
         if (rank == 0) {
-            tma_prefetch_desc(&maps.kv);
+            if (kQ8) {
+                tma_prefetch_desc(&maps.kv8);
+                tma_prefetch_desc(&maps.rope);
+            } else {
+                tma_prefetch_desc(&maps.kv);
+            }
             tma_prefetch_desc(&maps.q);
         } else {
-            tma_prefetch_desc(&maps.v);
+            tma_prefetch_desc(kQ8 ? &maps.kv8 : &maps.v);
             tma_prefetch_desc(&maps.o);
             tma_prefetch_desc(&maps.op);
             // the first two P messages may arrive as soon as the cluster is up
@@ -891,21 +1016,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     if (rank == 0) {
         if (warp == kWarpProducer) {
-            score_producer(maps, args, bars, smem, part, s, abort);
+            score_producer<kQ8>(maps, args, bars, smem, part, s, abort);
         } else if (warp == kWarpMma) {
-            ok = score_mma(args, bars, smem, tmem, part, kScoreMmaWarps == 1 ? -1 : 0, abort);
+            ok = score_mma<kQ8>(args, bars, smem, tmem, part, kScoreMmaWarps == 1 ? -1 : 0, abort);
         } else if (warp == kWarpMma2) {
-            if (kScoreMmaWarps == 2) ok = score_mma(args, bars, smem, tmem, part, 1, abort);
+            if (kScoreMmaWarps == 2) ok = score_mma<kQ8>(args, bars, smem, tmem, part, 1, abort);
         } else if (warp < kSoftmaxWarps) {
-            ok = score_softmax(args, bars, smem, tmem, part, s, peer, abort);
+            ok = score_softmax<kQ8>(args, bars, smem, tmem, part, s, peer, abort);
         }
     } else {
         if (warp == kWarpProducer) {
-            if ((threadIdx.x & 31) == 0) value_producer(maps, args, bars, smem, part, abort);
+            if ((threadIdx.x & 31) == 0) value_producer<kQ8>(maps, args, bars, smem, part, abort);
         } else if (warp == kWarpMma) {
-            ok = value_mma(args, bars, smem, tmem, part, abort);
+            ok = value_mma<kQ8>(args, bars, smem, tmem, part, abort);
         } else if (warp < kOWarps) {
             ok = value_owarps(maps, args, bars, smem, tmem, part, s, abort);
+        } else if (kQ8 && warp < 16) {
+            ok = value_expand(args, bars, smem, part, abort);
         }
     }
     // a role that gave up tells the peer, whose waits then end promptly
@@ -931,6 +1058,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Sets the kernel's shared-memory attribute once per device (thread-safe).
+template <bool kQ8>
 cudaError_t prepare_kernel() {
     static std::mutex mu;
     static bool done[64] = {};
@@ -940,7 +1068,7 @@ cudaError_t prepare_kernel() {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(mu);
     if (done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(decode_kernel<kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess) done[dev] = true;
     return e;
 }
@@ -965,20 +1093,23 @@ cudaLaunchConfig_t make_config(int clusters, cudaStream_t stream, cudaLaunchAttr
 }  // namespace
 
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, cudaStream_t stream) {
-    cudaError_t e = prepare_kernel();
+    const bool q8 = args.kv_scale != nullptr;
+    cudaError_t e = q8 ? prepare_kernel<true>() : prepare_kernel<false>();
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = make_config(args.num_parts * args.s_q, stream, attr, true);
-    return cudaLaunchKernelEx(&cfg, decode_kernel, maps, args);
+    if (q8) return cudaLaunchKernelEx(&cfg, decode_kernel<true>, maps, args);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<false>, maps, args);
 }
 
 // Clusters of the decode kernel that can be resident at once on the current device.
 int decode_max_active_clusters(int /*device*/) {
-    if (prepare_kernel() != cudaSuccess) return 0;
+    // both cache formats use the same threads and shared memory
+    if (prepare_kernel<false>() != cudaSuccess) return 0;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = make_config(1024, nullptr, attr, false);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_kernel, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<false>, &cfg) != cudaSuccess) return 0;
     return n;
 }
 

@@ -66,6 +66,7 @@ struct DecodeArgs {
     int* err;
     long long wait_ns;
     int withhold;      // test hook: the value CTA never loads its first page (its consumer's wait runs out)
+    const float* kv_scale;  // INT8 cache: per-token scales [num_blocks * 64]; nullptr for the bf16 cache
 };
 cudaError_t gemm_error_fetch(int* out, cudaStream_t stream);
 int decode_max_active_clusters(int device);
@@ -83,12 +84,14 @@ int decode_max_active_clusters(int device);
 //      box {32, min(H, 128), 4, 1} (store)
 struct DecodeMaps {
     CUtensorMap kv, v, q, o, op;
+    CUtensorMap kv8, rope;  // INT8 cache only
 };
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, cudaStream_t stream);
 
 cudaError_t launch_rope_append(void* q, const void* kv_new, const int32_t* seqlens, const int32_t* block_table,
-                               int mbps, void* kv_cache, int num_blocks, int B, int s_q, int H, double base,
-                               cudaStream_t stream);
+                               int mbps, void* kv_cache, void* kv8, float* kv_scale, int num_blocks, int B, int s_q,
+                               int H, double base, cudaStream_t stream);
+cudaError_t launch_quantize(const void* kv, long long rows, void* rec, float* scale, cudaStream_t stream);
 cudaError_t rope_error_fetch(int* out, cudaStream_t stream);
 
 // Prefill (naive form): gather + attention launchers (prefill.cu).

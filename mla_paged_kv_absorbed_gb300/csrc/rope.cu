@@ -20,10 +20,15 @@
 // float angle would lose about a milli-radian), then every head's rope part and
 // the new cache row are rotated in fp32 and rounded to bf16. All accesses are
 // 16-byte words; the latent is copied unchanged.
+//
+// With an INT8 cache (quant.cuh) the slot is the token's 640-byte record: the
+// latent's INT8 codes under its power-of-two scale (written to the scale
+// array), then the rotated rope key in bf16.
 #include <cuda_bf16.h>
 
 #include "mla_internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace mla {
 
@@ -46,11 +51,14 @@ __device__ __forceinline__ uint4 rotate_word(uint4 v, const float2* cs, int w) {
                       rotate_pair(v.w, d.x, d.y));
 }
 
+template <bool kQ8>
 __global__ void __launch_bounds__(kRopeThreads)
     rope_append_kernel(__nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kv_new,
                        const int32_t* __restrict__ seqlens, const int32_t* __restrict__ block_table, int mbps,
-                       __nv_bfloat16* __restrict__ kv_cache, int num_blocks, int s_q, int H, double base) {
+                       __nv_bfloat16* __restrict__ kv_cache, uint8_t* __restrict__ kv8, float* __restrict__ kv_scale,
+                       int num_blocks, int s_q, int H, double base) {
     __shared__ float2 cs[kPairs];
+    __shared__ float red[2];
     griddep_wait();
     griddep_launch_dependents();
     const int row = blockIdx.x;  // b * s_q + s
@@ -80,20 +88,57 @@ __global__ void __launch_bounds__(kRopeThreads)
         return;
     }
     const uint4* src = reinterpret_cast<const uint4*>(kv_new + (size_t)row * kDQK);
-    uint4* dst = reinterpret_cast<uint4*>(kv_cache + ((size_t)blk * kPage + t % kPage) * kDQK);
+    const size_t slot = (size_t)blk * kPage + t % kPage;
+    if (!kQ8) {
+        uint4* dst = reinterpret_cast<uint4*>(kv_cache + slot * kDQK);
+        if (threadIdx.x < kDLatent / 8) {
+            dst[threadIdx.x] = src[threadIdx.x];
+        } else if (threadIdx.x < kDLatent / 8 + 8) {
+            const int w = threadIdx.x - kDLatent / 8;
+            dst[kDLatent / 8 + w] = rotate_word(src[kDLatent / 8 + w], cs, w);
+        }
+        return;
+    }
+    // INT8 record: threads 0-63 hold one latent word (8 values) each; the row
+    // maximum over the two warps, then the codes; threads 64-71 rotate the rope words
+    uint8_t* rec = kv8 + slot * kQ8Record;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    float m = 0.f;
     if (threadIdx.x < kDLatent / 8) {
-        dst[threadIdx.x] = src[threadIdx.x];
+        v = src[threadIdx.x];
+        const uint32_t* u = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(u[i] << 16)), fabsf(__uint_as_float(u[i] & 0xFFFF0000u))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (threadIdx.x < kDLatent / 8 && (threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < kDLatent / 8) {
+        const float sc = q8_scale(fmaxf(red[0], red[1]));
+        const float inv = 1.f / sc;  // exact: a power of two
+        const uint32_t* u = reinterpret_cast<const uint32_t*>(&v);
+        uint32_t c[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            c[2 * i] = q8_code(__uint_as_float(u[i] << 16), inv);
+            c[2 * i + 1] = q8_code(__uint_as_float(u[i] & 0xFFFF0000u), inv);
+        }
+        reinterpret_cast<uint2*>(rec)[threadIdx.x] =
+            make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24), c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+        if (threadIdx.x == 0) kv_scale[slot] = sc;
     } else if (threadIdx.x < kDLatent / 8 + 8) {
         const int w = threadIdx.x - kDLatent / 8;
-        dst[kDLatent / 8 + w] = rotate_word(src[kDLatent / 8 + w], cs, w);
+        reinterpret_cast<uint4*>(rec + kDLatent)[w] = rotate_word(src[kDLatent / 8 + w], cs, w);
     }
 }
 
 }  // namespace
 
 cudaError_t launch_rope_append(void* q, const void* kv_new, const int32_t* seqlens, const int32_t* block_table,
-                               int mbps, void* kv_cache, int num_blocks, int B, int s_q, int H, double base,
-                               cudaStream_t stream) {
+                               int mbps, void* kv_cache, void* kv8, float* kv_scale, int num_blocks, int B, int s_q,
+                               int H, double base, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(B * s_q), 1, 1);
     cfg.blockDim = dim3(kRopeThreads, 1, 1);
@@ -103,9 +148,15 @@ cudaError_t launch_rope_append(void* q, const void* kv_new, const int32_t* seqle
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, rope_append_kernel, static_cast<__nv_bfloat16*>(q),
+    if (kv8 != nullptr)
+        return cudaLaunchKernelEx(&cfg, rope_append_kernel<true>, static_cast<__nv_bfloat16*>(q),
+                                  static_cast<const __nv_bfloat16*>(kv_new), seqlens, block_table, mbps,
+                                  static_cast<__nv_bfloat16*>(nullptr), static_cast<uint8_t*>(kv8), kv_scale,
+                                  num_blocks, s_q, H, base);
+    return cudaLaunchKernelEx(&cfg, rope_append_kernel<false>, static_cast<__nv_bfloat16*>(q),
                               static_cast<const __nv_bfloat16*>(kv_new), seqlens, block_table, mbps,
-                              static_cast<__nv_bfloat16*>(kv_cache), num_blocks, s_q, H, base);
+                              static_cast<__nv_bfloat16*>(kv_cache), static_cast<uint8_t*>(nullptr),
+                              static_cast<float*>(nullptr), num_blocks, s_q, H, base);
 }
 
 // Reads this file's error word into *out and clears it, in stream order.

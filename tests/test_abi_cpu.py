@@ -85,6 +85,21 @@ def test_bad_arguments_are_rejected_on_the_host(L):
     p = ctypes.cast(buf, ctypes.c_void_p)
     # a rope base that is not > 1
     assert L.mla_rope_append(p, p, p, p, 1, p, 1, 1, 1, 128, ctypes.c_float(1.0), null) == 1
+    # INT8 cache entry points: missing records or scales, empty or unaligned inputs
+    assert L.mla_decode_paged_q8(p, null, p, 1, p, 1, p, 1, 1, 128, p, p, 1, ctypes.c_float(0.1), 1,
+                                 p, p, p, 1 << 20, null) == 1
+    assert L.mla_decode_paged_q8(p, p, null, 1, p, 1, p, 1, 1, 128, p, p, 1, ctypes.c_float(0.1), 1,
+                                 p, p, p, 1 << 20, null) == 1
+    assert L.mla_quantize_cache(p, ctypes.c_longlong(0), p, p, null) == 1
+    assert L.mla_quantize_cache(null, ctypes.c_longlong(4), p, p, null) == 1
+    odd = ctypes.c_void_p(buf_addr(buf) + 4)
+    assert L.mla_quantize_cache(odd, ctypes.c_longlong(4), p, p, null) == 1
+    assert L.mla_rope_append_q8(p, p, p, p, 1, null, p, 1, 1, 1, 128, ctypes.c_float(10000.0), null) == 1
+    assert L.mla_rope_append_q8(p, p, p, p, 1, p, null, 1, 1, 1, 128, ctypes.c_float(10000.0), null) == 1
+
+
+def buf_addr(buf):
+    return ctypes.addressof(buf) + ((16 - ctypes.addressof(buf) % 16) % 16)
 
 
 def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
