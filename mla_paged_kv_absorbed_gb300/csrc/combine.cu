@@ -40,6 +40,24 @@ __device__ void combine_row(const int32_t* __restrict__ num_splits, int row, int
     const int first = num_splits[b];
     const int n = num_splits[b + 1] - first;
     if (n == 1) return;
+    // the first four pieces' lse and partial rows are requested first, with the
+    // reduction's loads right after, so the common case (two to four pieces) costs
+    // one memory round trip: none of these addresses depends on a loaded value
+    float l4[4];
+    float4 v4[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        l4[j] = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v4[j][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < n) {
+            const size_t prow = ((size_t)(first + j) * s_q + s) * H + h;
+            l4[j] = lse_part[prow];
+            const float4* src = reinterpret_cast<const float4*>(o_part + prow * kDLatent);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v4[j][k] = src[lane + 32 * k];
+        }
+    }
     // lse of piece i of this row
     auto lse_of = [&](int i) { return lse_part[((size_t)(first + i) * s_q + s) * H + h]; };
     float L = -INFINITY;
@@ -56,7 +74,19 @@ __device__ void combine_row(const int32_t* __restrict__ num_splits, int row, int
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         total = L + logf(sum);
-        for (int i0 = 0; i0 < n; i0 += 4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float w = j < n ? expf(l4[j] - total) : 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                acc[k].x += w * v4[j][k].x;
+                acc[k].y += w * v4[j][k].y;
+                acc[k].z += w * v4[j][k].z;
+                acc[k].w += w * v4[j][k].w;
+            }
+        }
+        // pieces 4, 5, ... (long sequences), four at a time, in ascending order
+        for (int i0 = 4; i0 < n; i0 += 4) {
             float4 v[4][4];
             float w[4];
 #pragma unroll

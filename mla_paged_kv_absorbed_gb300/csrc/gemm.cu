@@ -228,6 +228,220 @@ cudaError_t launch_variant(const CUtensorMap* tm_a, const CUtensorMap* tm_b, con
 }
 
 // ---------------------------------------------------------------------------
+// wres_gemm_kernel: the K = 512, N = 128 head GEMMs (the out-projection and the
+// prefill's two decompression GEMMs) with the head's weight resident. One CTA
+// per (head, group of 128-row tiles) loads W[h] (512 x 128 bf16 = 128 KB, four
+// 128-deep K-stages, the same boxes as head_gemm_kernel) once, then streams its
+// tiles' A rows through a two-slot ring of 32 KB K-stages. The accumulator is
+// double-buffered in TMEM (2 x 128 columns), so the products of tile t + 1 run
+// while four epilogue warps move tile t through a 32 KB staging buffer to a TMA
+// store. Against one CTA per (head, tile), the weight is read once per CTA
+// instead of once per tile, and a few tiles per head (B * s_q = 264 rows: 3
+// tiles) run in one wave instead of 2.5.
+// Warps: 0 TMA producer, 1 MMA issuer and TMEM owner, 2-5 epilogue (warp w
+// reads TMEM lane quadrant w % 4, one thread per tile row).
+constexpr int kWrThreads = 192;
+constexpr int kWrStages = 4;           // K = 512 as four stages of 128
+constexpr int kWrStageBytes = 32768;   // [2 chunks][128 rows][64] bf16
+constexpr int kWrRing = 2;
+constexpr int kWrOffA = kWrStages * kWrStageBytes;          // after the weight
+constexpr int kWrOffStage = kWrOffA + kWrRing * kWrStageBytes;
+constexpr int kWrOffBar = kWrOffStage + kWrStageBytes;
+constexpr int kWrBytes = kWrOffBar + 256 + 1024;            // + barriers + alignment slack
+static_assert(kWrBytes <= 232448, "shared memory per CTA");
+
+struct WrBars {
+    uint64_t w_full, a_full[kWrRing], a_empty[kWrRing], acc_full[2], acc_free[2], drain;
+    uint32_t tmem_slot;
+    int abort;
+};
+static_assert(sizeof(WrBars) <= 256, "barrier block");
+
+__global__ void __launch_bounds__(kWrThreads, 1)
+    wres_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                     const __grid_constant__ CUtensorMap tm_out, GemmArgs args, int tiles_per_cta, long long wait_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    WrBars* bars = reinterpret_cast<WrBars*>(smem + kWrOffBar);
+    volatile int* abort = &bars->abort;
+    int* err = &g_gemm_error;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x;
+    const int mtiles = (args.R + kBM - 1) / kBM;
+    const int t0 = (int)blockIdx.y * tiles_per_cta;
+    const int ntiles = max(0, min(mtiles, t0 + tiles_per_cta) - t0);
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->w_full, 1);
+        for (int i = 0; i < kWrRing; ++i) {
+            mbar_init(&bars->a_full[i], 1);
+            mbar_init(&bars->a_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->acc_full[i], 1);
+            mbar_init(&bars->acc_free[i], 4);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbarrier_init_cluster();
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+        tma_prefetch_desc(&tm_out);
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_slot, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_slot;
+    griddep_wait();
+    griddep_launch_dependents();
+
+    if (warp == 0) {
+        if (lane == 0 && ntiles > 0) {
+            mbar_arrive_expect_tx(&bars->w_full, kWrStages * kWrStageBytes);
+            for (int kc = 0; kc < kWrStages; ++kc) {
+                uint8_t* dst = smem + kc * kWrStageBytes;
+                if (args.b_kmajor)  // [2 K chunks][128 n rows][64]
+                    tma_load_4d(dst, &tm_b, &bars->w_full, 0, 0, 2 * kc, h);
+                else                // [2 n chunks][128 k rows][64]
+                    tma_load_4d(dst, &tm_b, &bars->w_full, 0, kc * kBK, 0, h);
+            }
+            int q = 0;
+            bool ok = true;
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int m0 = (t0 + t) * kBM;
+                for (int kc = 0; kc < kWrStages; ++kc, ++q) {
+                    const int slot = q % kWrRing;
+                    if (q >= kWrRing) ok = mbar_wait(&bars->a_empty[slot], ((q / kWrRing) - 1) & 1, abort, err, wait_ns);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&bars->a_full[slot], kWrStageBytes);
+                    tma_load_4d(smem + kWrOffA + slot * kWrStageBytes, &tm_a, &bars->a_full[slot], 0, m0, 2 * kc,
+                                args.a_shared ? 0 : h);
+                }
+            }
+            // never leave with a copy in flight
+            mbar_wait(&bars->w_full, 0, nullptr, err, kDrainNs);
+            for (int r = q - kWrRing > 0 ? q - kWrRing : 0; r < q; ++r)
+                mbar_wait(&bars->a_full[r % kWrRing], (r / kWrRing) & 1, nullptr, err, kDrainNs);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        const uint32_t idesc = idesc_bf16_f32(kBM, 128, false, args.b_kmajor == 0);
+        bool ok = ntiles > 0 && warp_wait(&bars->w_full, 0, abort, err, wait_ns);
+        bool issued = false;
+        int q = 0;
+        for (int t = 0; t < ntiles && ok; ++t) {
+            const int buf = t & 1;
+            // the epilogue has read this buffer's tile t - 2
+            if (t >= 2) ok = warp_wait(&bars->acc_free[buf], ((t >> 1) - 1) & 1, abort, err, wait_ns);
+            for (int kc = 0; kc < kWrStages && ok; ++kc, ++q) {
+                const int slot = q % kWrRing;
+                ok = warp_wait(&bars->a_full[slot], (q / kWrRing) & 1, abort, err, wait_ns);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t a_base = smem_u32(smem + kWrOffA + slot * kWrStageBytes);
+                const uint32_t b_base = smem_u32(smem + kc * kWrStageBytes);
+                const uint64_t ad0 = desc_sw128(a_base, 0, 1024);
+                const uint64_t bd0 = args.b_kmajor ? desc_sw128(b_base, 0, 1024) : desc_sw128(b_base, kBK * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    const uint64_t ad = ad0 + (uint64_t)(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+                    const uint64_t bd = args.b_kmajor ? bd0 + (uint64_t)(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4)
+                                                      : bd0 + (uint64_t)((kk * 2048) >> 4);
+                    mma_bf16_ss(tmem + 128u * (uint32_t)buf, ad, bd, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&bars->a_empty[slot]);
+                issued = true;
+            }
+            if (ok) mma_commit(&bars->acc_full[buf]);
+        }
+        // every product has completed before TMEM is freed
+        if (issued) {
+            mma_commit(&bars->drain);
+            warp_wait(&bars->drain, 0, nullptr, err, kDrainNs);
+        }
+    } else {
+        // epilogue: TMEM -> bf16 -> staging ([2 chunks][128 rows][128 B], swizzled) -> TMA store
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        uint8_t* stage = smem + kWrOffStage;
+        const bool leader = threadIdx.x == 64;
+        bool stored = false, ok = true;
+        for (int t = 0; t < ntiles && ok; ++t) {
+            const int buf = t & 1;
+            ok = warp_wait(&bars->acc_full[buf], (t >> 1) & 1, abort, err, wait_ns);
+            // the staging buffer is free once the previous tile's store has read it
+            if (leader && stored) bulk_wait_group_read0();
+            ok = barrier_and(1, 128, ok);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + 128u * (uint32_t)buf + (uint32_t)(c * 32), v);
+                tmem_wait_ld();
+                uint8_t* box = stage + (c >> 1) * (kBM * 128) + row * 128;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int gidx = (c & 1) * 4 + i;
+                    *reinterpret_cast<uint4*>(box + ((gidx ^ (row & 7)) * 16)) =
+                        make_uint4(pack_bf16x2(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1])),
+                                   pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                                   pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                                   pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+                }
+            }
+            // TMEM buffer read: the products of tile t + 2 may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->acc_free[buf]);
+            fence_proxy_async_smem();
+            ok = barrier_and(1, 128, ok);
+            if (ok && leader) {
+                tma_store_4d(&tm_out, stage, 0, (t0 + t) * kBM, 0, h);
+                bulk_commit_group();
+                stored = true;
+            }
+        }
+        if (leader && stored) bulk_wait_group0();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+cudaError_t launch_wres(const CUtensorMap* tm_a, const CUtensorMap* tm_b, const CUtensorMap* tm_out,
+                        const GemmArgs& args, long long wait_ns, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(wres_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWrBytes);
+    if (e != cudaSuccess) return e;
+    const int sm_count = device_sm_count();
+    if (sm_count <= 0) return cudaErrorInvalidDevice;
+    const int mtiles = (args.R + kBM - 1) / kBM;
+    // one CTA per SM: as many row-tile groups per head as the SMs beyond one
+    // per head allow (1 at 128 heads), each group one contiguous run of tiles
+    const int groups = max(1, min(mtiles, sm_count / args.H));
+    const int per = (mtiles + groups - 1) / groups;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)args.H, (unsigned)((mtiles + per - 1) / per), 1);
+    cfg.blockDim = dim3(kWrThreads, 1, 1);
+    cfg.dynamicSmemBytes = kWrBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, wres_gemm_kernel, *tm_a, *tm_b, *tm_out, args, per, wait_ns);
+}
+
+// ---------------------------------------------------------------------------
 // absorb_kernel: the absorb projection (K = 128) as a persistent kernel. Work
 // units are (head, 128-row tile, 128-column quarter of the 512 outputs); each
 // CTA (one per SM) walks a contiguous range of them, so it keeps the head's
@@ -524,6 +738,8 @@ cudaError_t launch_head_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b, c
     // K = 512 through three stages, one CTA per head and row tile
     if (args.K == 128 && args.N == kAbsN * kAbsQuarters && args.n_cta == kAbsN)
         return launch_absorb(tm_a, tm_b, tm_out, args, wait_ns, stream);
+    if (args.K == kWrStages * kBK && args.N == 128 && args.n_cta == 128 && args.rope_src == nullptr)
+        return launch_wres(tm_a, tm_b, tm_out, args, wait_ns, stream);
     if (args.n_cta == 128) return launch_variant<128, 3>(tm_a, tm_b, tm_out, args, wait_ns, stream);
     return cudaErrorInvalidValue;
 }

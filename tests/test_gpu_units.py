@@ -94,7 +94,11 @@ def test_absorb_q(api, B, s_q, H):
     assert torch.equal(q_abs[..., 512:].view(torch.int16), inp.q[..., 128:].view(torch.int16))
 
 
-@pytest.mark.parametrize("B,s_q,H", [(2, 1, 16), (128, 1, 128), (132, 2, 128), (5, 1, 64)])
+# rows per head: 1 tile (2, 128, 5), 3 tiles (264), 9 tiles looped in one CTA
+# per head (1100), five 1-tile groups (600 rows, 16 heads), uneven groups of
+# 2, 2, 1 tiles (600 rows, 32 heads)
+@pytest.mark.parametrize("B,s_q,H", [(2, 1, 16), (128, 1, 128), (132, 2, 128), (5, 1, 64), (1100, 1, 128),
+                                     (600, 1, 16), (300, 2, 32)])
 def test_out_proj(api, B, s_q, H):
     g = torch.Generator().manual_seed(B * 7 + H)
     o = (torch.randn(B, s_q, H, 512, generator=g) * 0.2).to(torch.bfloat16)
