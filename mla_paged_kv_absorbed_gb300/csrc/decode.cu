@@ -99,13 +99,17 @@ constexpr int kPSlotBytes = kRows * 128;           // P of a page: [128 rows x 6
 constexpr int kVBytes = 8 * kChunkBytes;           // a page's value columns: [8 chunks][64 keys][64 dims]
 constexpr int kVRing = 2;
 constexpr int kOffXV = kOffX;                      // value: [P slot][rescale factor 128 | 1/l 128] fp32
-constexpr int kOffP = kOffRole;                    // value: two P slots
-constexpr int kOffV = kOffP + 2 * kPSlotBytes;     // value: the value ring
+constexpr int kOffP = kOffRole;                    // value: kPSlots P slots
+// P slots: page n's message goes to slot n % kPSlots. Two: a third let the
+// softmax run further ahead but made the long multi-token workload 12 % slower.
+constexpr int kPSlots = 2;
+constexpr int kOffV = kOffP + kPSlots * kPSlotBytes;  // value: the value ring
 constexpr int kSmemValue = kOffV + kVRing * kVBytes;
 constexpr int kSmemUsed = kSmemScore > kSmemValue ? kSmemScore : kSmemValue;
 constexpr int kSmemBytes = kSmemUsed + 1024;       // room to align the base to 1024 bytes
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kOffP % 1024 == 0 && kOffV % 1024 == 0 && kOffRing % 1024 == 0, "swizzle atoms");
+static_assert(kOffXV + kPSlots * 1024 <= kOffScale, "value factor slots");
 static_assert(kOffScale + kRing * kScaleBytes <= kOffRole && kOffScale + kVRing * kScaleBytes <= kOffRole, "scales");
 // INT8 cache, in a page slot: the codes arrive as four planes [64 keys x 128 B]
 // (128-byte swizzle) at kQ8Planes and are expanded in place into the bf16
@@ -118,7 +122,11 @@ constexpr uint32_t kPMsgBytes = kPSlotBytes + 2 * kRows * 4;
 
 // ---- tensor memory ----
 constexpr uint32_t kTmemQ = 0;       // score CTA: the 576 query dims as bf16 pairs (288 columns)
-constexpr uint32_t kTmemS = 288;     // score CTA: two S buffers of 64 columns
+constexpr uint32_t kTmemS = 288;     // score CTA: kSBufs S buffers of 64 columns
+// S buffers: page n's scores go to buffer n % kSBufs. With three, the score
+// products can run two pages ahead of the softmax that frees a buffer.
+constexpr int kSBufs = 3;
+static_assert(kTmemS + 64 * kSBufs <= 512, "TMEM columns");
 constexpr uint32_t kTmemCols = 512;  // value CTA: O, all columns
 
 // After an abort the value CTA waits this long for P messages that may still
@@ -132,17 +140,17 @@ struct Bars {
     // score CTA
     uint64_t ring_full[kRing], ring_empty[kRing];
     uint64_t q_full, q_drained;
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_free[2];  // score CTA; arrivals come from the value CTA
+    uint64_t s_full[kSBufs], s_free[kSBufs];
+    uint64_t p_free[kPSlots];  // score CTA; arrivals come from the value CTA
     uint64_t ref_full[2][4];  // [page parity][lane quadrant]: reference max of a page published
     uint64_t lsum_full[4];    // [lane quadrant]: the group without an item's last page published its row sums
     uint64_t drain2;          // second score MMA warp
     uint64_t deq_full[2];     // INT8 cache: [page parity] the page is expanded to bf16 in its ring slot
     // value CTA
-    uint64_t p_full[2];  // own arrive + expect_tx, bytes from the score CTA
+    uint64_t p_full[kPSlots];  // own arrive + expect_tx, bytes from the score CTA
     uint64_t v_full[kVRing], v_empty[kVRing];
     uint64_t pv_done, o_full;
-    uint64_t o_ack[2];   // per P slot: the O warps may run one page ahead, never two on one slot
+    uint64_t o_ack[kPSlots];  // per P slot: the O warps have read the slot's factors
     uint64_t o_free[2];
     uint64_t stage_full, stage_free;  // epilogue rounds: eight warps staged / staging read by the store
     uint64_t drain;
@@ -402,7 +410,8 @@ __device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
         }
         if (parity < 0 || buf == parity) {
             // S buffer `buf` was read by the softmax of page n - 2
-            if (n >= 2) ok = warp_wait(&bars->s_free[buf], ((n >> 1) - 1) & 1, abort, err, wait_ns);
+            const int sb = n % kSBufs;
+            if (n >= kSBufs) ok = warp_wait(&bars->s_free[sb], ((n / kSBufs) - 1) & 1, abort, err, wait_ns);
             // the page has landed (INT8 cache: and its softmax group has expanded it)
             if (ok)
                 ok = kQ8 ? warp_wait(&bars->deq_full[n & 1], (n >> 1) & 1, abort, err, wait_ns)
@@ -413,7 +422,7 @@ __device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
             // elected lane issues. One descriptor per page; a K-step moves its
             // start address field (bytes / 16) by a constant.
             const uint64_t bdesc = desc_sw128(smem_u32(ring + (r % kRing) * kPageBytes), 0, 1024);
-            const uint32_t d = tmem + kTmemS + 64u * (uint32_t)buf;
+            const uint32_t d = tmem + kTmemS + 64u * (uint32_t)sb;
 #pragma unroll
             for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
@@ -422,7 +431,7 @@ __device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
                                 idesc_s, (c | kk) != 0 ? 1u : 0u);
             }
             mma_commit(&bars->ring_empty[r % kRing]);
-            mma_commit(&bars->s_full[buf]);
+            mma_commit(&bars->s_full[sb]);
             issued = true;
         }
         // both warps report when their products of the item no longer read the query
@@ -546,16 +555,17 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
             }
         }
         float x[32];
-        if (ok) ok = warp_wait(&bars->s_full[buf], (n >> 1) & 1, abort, err, wait_ns);
+        const int sb = n % kSBufs;
+        if (ok) ok = warp_wait(&bars->s_full[sb], (n / kSBufs) & 1, abort, err, wait_ns);
         if (ok) {
             tc_fence_after();
             uint32_t v[32];
-            tmem_ld32(tmem + lane_base + kTmemS + 64u * (uint32_t)buf + 32u * (uint32_t)half, v);
+            tmem_ld32(tmem + lane_base + kTmemS + 64u * (uint32_t)sb + 32u * (uint32_t)half, v);
             tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]) * args.scale_log2;
             tc_fence_before();
-            mbar_arrive(&bars->s_free[buf]);
+            mbar_arrive(&bars->s_free[sb]);
         }
         // keys of this half; columns past the visible keys are masked by
         // selection, so whatever the tail rows of the page hold never leaks
@@ -602,18 +612,19 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
             pk[c] = pack_bf16x2(p0, p1);
         }
         // slot buf held page n - 2 until the value CTA released it
-        if (ok && n >= 2) ok = warp_wait(&bars->p_free[buf], ((n >> 1) - 1) & 1, abort, err, wait_ns);
-        const uint32_t mbar = pfull_remote + (uint32_t)buf * 8u;
+        const int pb = n % kPSlots;  // P slot of this page
+        if (ok && n >= kPSlots) ok = warp_wait(&bars->p_free[pb], ((n / kPSlots) - 1) & 1, abort, err, wait_ns);
+        const uint32_t mbar = pfull_remote + (uint32_t)pb * 8u;
         if (ok) {
             // row `row`, keys [32 half, 32 half + 32): 16-byte words 4 half .. 4 half + 3,
             // word w stored at position w ^ (row % 8)
-            const uint32_t dst = p_remote + (uint32_t)(buf * kPSlotBytes + row * 128);
+            const uint32_t dst = p_remote + (uint32_t)(pb * kPSlotBytes + row * 128);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 st_async_u4(dst + (uint32_t)(((4 * half + q) ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1],
                             pk[4 * q + 2], pk[4 * q + 3], mbar);
             if (half == 0)
-                st_async_b32(x_remote + (uint32_t)(buf * 1024 + row * 4), __float_as_uint(row < args.H ? alpha : 1.f),
+                st_async_b32(x_remote + (uint32_t)(pb * 1024 + row * 4), __float_as_uint(row < args.H ? alpha : 1.f),
                              mbar);
         }
         if (last) {
@@ -635,7 +646,7 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
             }
             if (ok && half == 0) {
                 const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
-                st_async_b32(x_remote + (uint32_t)(buf * 1024 + 512 + row * 4), __float_as_uint(inv_l), mbar);
+                st_async_b32(x_remote + (uint32_t)(pb * 1024 + 512 + row * 4), __float_as_uint(inv_l), mbar);
                 if (row < args.H) {
                     // lse in natural log: x is in log2 units of the scaled score
                     const float lse_v = l_row > 0.f ? (m_new + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
@@ -646,7 +657,7 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
                 }
             }
         } else if (ok && half == 0) {
-            st_async_b32(x_remote + (uint32_t)(buf * 1024 + 512 + row * 4), 0u, mbar);
+            st_async_b32(x_remote + (uint32_t)(pb * 1024 + 512 + row * 4), 0u, mbar);
         }
     }
     return ok;
@@ -695,21 +706,21 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
     bool ok = true, issued = false;
     int consumed = 0;
     for (; ok && pi.valid; pi.advance()) {
-        const int n = pi.n, k = n & 1, qi = pi.n_items - 1;
+        const int n = pi.n, k = n % kPSlots, qi = pi.n_items - 1;
         const bool first = pi.first_of_item(), last = pi.last_of_item();
-        ok = warp_wait<true>(&bars->p_full[k], (n >> 1) & 1, abort, err, wait_ns);
+        ok = warp_wait<true>(&bars->p_full[k], (n / kPSlots) & 1, abort, err, wait_ns);
         if (!ok) break;
         consumed = n + 1;
         if (lane == 0) {
             // P was written by the peer's generic stores: make it visible to the
-            // tensor pipe, then arm the slot for page n + 2 (its bytes can only
-            // come after this page has released the slot)
+            // tensor pipe, then arm the slot for page n + kPSlots (its bytes can
+            // only come after this page has released the slot)
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&bars->p_full[k], kPMsgBytes);
         }
         __syncwarp();
         // the O warps have read this message's factors (and rescaled O if asked)
-        ok = warp_wait(&bars->o_ack[k], (n >> 1) & 1, abort, err, wait_ns);
+        ok = warp_wait(&bars->o_ack[k], (n / kPSlots) & 1, abort, err, wait_ns);
         // a batch's first product overwrites O: its previous epilogue must have read it
         if (ok && first && qi > 0) ok = warp_wait(&bars->o_free[0], (qi - 1) & 1, abort, err, wait_ns);
         if (ok && first && qi > 0) ok = warp_wait(&bars->o_free[1], (qi - 1) & 1, abort, err, wait_ns);
@@ -800,9 +811,9 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
     bool stored = false;
     int erounds = 0;  // epilogue rounds so far (phase of stage_full / stage_free)
     for (; ok && pi.valid; pi.advance()) {
-        const int n = pi.n, k = n & 1, qi = pi.n_items - 1;
+        const int n = pi.n, k = n % kPSlots, qi = pi.n_items - 1;
         const bool first = pi.first_of_item(), last = pi.last_of_item();
-        ok = warp_wait<true>(&bars->p_full[k], (n >> 1) & 1, abort, err, wait_ns);
+        ok = warp_wait<true>(&bars->p_full[k], (n / kPSlots) & 1, abort, err, wait_ns);
         if (!ok) break;
         const float inv_l = xv[k * 256 + 128 + row];
         if (!first) {
@@ -957,13 +968,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bars->q_full, 32 * kSoftmaxWarps);
         mbar_init(&bars->q_drained, kScoreMmaWarps);
-        for (int i = 0; i < 2; ++i) {
-            for (int q = 0; q < 4; ++q) mbar_init(&bars->ref_full[i][q], 32);
+        for (int i = 0; i < kSBufs; ++i) {
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->s_free[i], 256);
+        }
+        for (int i = 0; i < kPSlots; ++i) {
             mbar_init(&bars->p_free[i], 1);
             mbar_init(&bars->p_full[i], 1);
             mbar_init(&bars->o_ack[i], 8);
+        }
+        for (int i = 0; i < 2; ++i) {
+            for (int q = 0; q < 4; ++q) mbar_init(&bars->ref_full[i][q], 32);
             mbar_init(&bars->o_free[i], 4);
         }
         for (int i = 0; i < kVRing; ++i) {
@@ -994,9 +1009,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(kQ8 ? &maps.kv8 : &maps.v);
             tma_prefetch_desc(&maps.o);
             tma_prefetch_desc(&maps.op);
-            // the first two P messages may arrive as soon as the cluster is up
-            mbar_arrive_expect_tx(&bars->p_full[0], kPMsgBytes);
-            mbar_arrive_expect_tx(&bars->p_full[1], kPMsgBytes);
+            // the first kPSlots P messages may arrive as soon as the cluster is up
+            for (int i = 0; i < kPSlots; ++i) mbar_arrive_expect_tx(&bars->p_full[i], kPMsgBytes);
         }
     }
     if (warp == kWarpMma) {
@@ -1044,11 +1058,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // it has finished its last page: leave together
     cluster_sync_all();
     if (rank == 1 && warp == kWarpMma && (threadIdx.x & 31) == 0 && *abort) {
-        // The score CTA has stopped sending, but the st.async stores of the two
-        // armed P messages (pages c and c + 1) may still be landing in this
+        // The score CTA has stopped sending, but the st.async stores of the
+        // armed P messages (pages c .. c + kPSlots - 1) may still be landing in this
         // CTA's shared memory: wait for their phases, briefly, before leaving.
         const int c = bars->p_consumed;
-        for (int n = c; n < c + 2; ++n) mbar_wait(&bars->p_full[n & 1], (n >> 1) & 1, nullptr, nullptr, kPDrainNs);
+        for (int n = c; n < c + kPSlots; ++n)
+            mbar_wait(&bars->p_full[n % kPSlots], (n / kPSlots) & 1, nullptr, nullptr, kPDrainNs);
     }
     if (warp == kWarpMma) {
         __syncwarp();
