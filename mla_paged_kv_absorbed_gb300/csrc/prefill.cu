@@ -20,8 +20,8 @@
 // contiguous buffers (the two up-projections then run as batched head GEMMs,
 // gemm.cu), and the attention: one CTA per (b, h, 128-query tile), 64-key
 // tiles of K and V streaming through a TMA ring, S = Q K^T and O += P V on
-// tcgen05 with S (double-buffered) and O in TMEM, one softmax thread per query
-// row (online softmax, lazy rescaling of O), P staged in shared memory.
+// tcgen05 with S (double-buffered), P and O in TMEM, two softmax threads per
+// query row (online softmax, lazy rescaling of O).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -80,21 +80,35 @@ __global__ void __launch_bounds__(kGatherThreads)
 }
 
 // --------------------------------------------------------------- attention --
-constexpr int kAThreads = 192;  // warps 0-3 softmax (one thread per row), 4 producer, 5 MMA + TMEM owner
+// One CTA per (b, h, 128-query tile). Warps 0-7 run the softmax and the
+// epilogue, two per TMEM lane quadrant: warp w owns rows 32 (w % 4) .. + 31 and
+// keys [32 (w / 4), + 32) of every 64-key tile, and the two warps of a quadrant
+// exchange their half-row maxima (and, at the end, their half sums) through
+// shared memory. Warp 8 is the TMA producer, warp 9 issues the products and
+// owns TMEM. S = Q K^T goes to one of two TMEM buffers; the softmax writes P
+// (bf16 pairs) back over the first 32 columns of the same buffer, and O += P V
+// takes P as the A operand straight from TMEM. The tensor pipe runs a CTA's
+// products in issue order, so S of tile j + 2 (issued after P V of tile j)
+// never overwrites P before it has been read, and P is written only after both
+// halves of a row have read their scores (the max exchange orders them).
+constexpr int kAThreads = 320;
+constexpr int kAWarpProducer = 8;
+constexpr int kAWarpMma = 9;
 constexpr int kARows = 128;     // query rows per CTA
 constexpr int kAKeys = 64;      // keys per tile
-constexpr int kAStages = 3;
+constexpr int kAStages = 4;
 constexpr int kQBytes = 3 * kARows * 128;   // [3 chunks][128 rows][64]
 constexpr int kKBytes = 3 * kAKeys * 128;   // [3 chunks][64 keys][64]
 constexpr int kVBytesA = 2 * kAKeys * 128;  // [2 chunks][64 keys][64]
-constexpr int kPBytes = kARows * 128;       // [128 rows][64 keys]
-constexpr int kAOffQ = 1024;
+constexpr int kAOffX = 1024;                // [2 episodes][2 halves][128 rows] floats
+constexpr int kAOffQ = 4096;
 constexpr int kAOffK = kAOffQ + kQBytes;
 constexpr int kAOffV = kAOffK + kAStages * kKBytes;
-constexpr int kAOffP = kAOffV + kAStages * kVBytesA;
-constexpr int kASmem = kAOffP + 2 * kPBytes + 1024;  // + alignment slack
+constexpr int kASmem = kAOffV + kAStages * kVBytesA + 1024;  // + alignment slack
 static_assert(kASmem <= 232448, "prefill attention shared memory");
-constexpr uint32_t kATmemS = 0;    // two S buffers of 64 columns
+static_assert(kAOffX + 2 * 2 * kARows * 4 <= kAOffQ, "exchange area");
+static_assert(kAOffQ % 1024 == 0 && kAOffK % 1024 == 0 && kAOffV % 1024 == 0, "swizzle atoms");
+constexpr uint32_t kATmemS = 0;    // two S buffers of 64 columns (P over the first 32 of each)
 constexpr uint32_t kATmemO = 128;  // O: 128 columns
 constexpr uint32_t kATmemCols = 256;
 constexpr float kARescale = 8.0f;
@@ -102,13 +116,12 @@ constexpr float kARescale = 8.0f;
 struct ABars {
     uint64_t q_full;
     uint64_t kv_full[kAStages], kv_empty[kAStages];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_full[2], p_free[2];
+    uint64_t s_full[2], p_full[2];
     uint64_t pv_done, drain;
     uint32_t tmem_slot;
     int abort;
 };
-static_assert(sizeof(ABars) <= 1024, "prefill barriers");
+static_assert(sizeof(ABars) <= kAOffX, "prefill barriers");
 
 struct PrefillArgs {
     const int32_t* seqlens;
@@ -149,9 +162,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->s_free[i], 128);
-            mbar_init(&bars->p_full[i], 128);
-            mbar_init(&bars->p_free[i], 1);
+            mbar_init(&bars->p_full[i], 256);
         }
         mbar_init(&bars->pv_done, 1);
         mbar_init(&bars->drain, 1);
@@ -161,7 +172,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
         tma_prefetch_desc(&maps.k);
         tma_prefetch_desc(&maps.v);
     }
-    if (warp == 5) {
+    if (warp == kAWarpMma) {
         tmem_alloc(&bars->tmem_slot, kATmemCols);
         tmem_relinquish();
     }
@@ -180,7 +191,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
     const int key_row0 = b * args.Lmax;  // first key row of this sequence in the K/V buffers
 
     bool ok = true;
-    if (warp == 4) {
+    if (warp == kAWarpProducer) {
         // producer: the query tile once, then K and V tiles through the ring
         if (lane == 0 && tiles > 0) {
             mbar_arrive_expect_tx(&bars->q_full, (uint32_t)kQBytes);
@@ -200,7 +211,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 mbar_wait(&bars->kv_full[j % kAStages], (j / kAStages) & 1, nullptr, err, kDrainNs);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == kAWarpMma) {
         // MMA issuer (whole warp; one elected lane issues)
         const uint32_t idesc_s = idesc_bf16_f32(kARows, kAKeys, false, false);
         const uint32_t idesc_o = idesc_bf16_f32(kARows, 128, false, true);
@@ -210,7 +221,6 @@ __global__ void __launch_bounds__(kAThreads, 1)
         auto issue_s = [&](int j) -> bool {
             const int st = j % kAStages, sb = j & 1;
             if (!warp_wait(&bars->kv_full[st], (j / kAStages) & 1, abort, err, wait_ns)) return false;
-            if (j >= 2 && !warp_wait(&bars->s_free[sb], ((j >> 1) - 1) & 1, abort, err, wait_ns)) return false;
             tc_fence_after();
             const uint64_t kdesc = desc_sw128(smem_u32(smem + kAOffK + st * kKBytes), 0, 1024);
 #pragma unroll
@@ -223,21 +233,22 @@ __global__ void __launch_bounds__(kAThreads, 1)
             mma_commit(&bars->s_full[sb]);
             return true;
         };
-        if (ok && tiles > 0) { ok = issue_s(0); issued = ok; }
+        if (ok && tiles > 0) {
+            ok = issue_s(0);
+            issued = true;
+        }
         if (ok && tiles > 1) ok = issue_s(1);
         for (int j = 0; ok && j < tiles; ++j) {
-            const int st = j % kAStages, pb = j & 1;
-            ok = warp_wait(&bars->p_full[pb], (j >> 1) & 1, abort, err, wait_ns);
+            const int st = j % kAStages, sb = j & 1;
+            ok = warp_wait(&bars->p_full[sb], (j >> 1) & 1, abort, err, wait_ns);
             if (!ok) break;
             tc_fence_after();
-            const uint64_t pdesc = desc_sw128(smem_u32(smem + kAOffP + pb * kPBytes), 0, 1024);
             const uint64_t vdesc = desc_sw128(smem_u32(smem + kAOffV + st * kVBytesA), kAKeys * 128, 1024);
 #pragma unroll
             for (int kk = 0; kk < kAKeys / 16; ++kk)
-                mma_bf16_ss(tmem + kATmemO, pdesc + (uint64_t)((32 * kk) >> 4), vdesc + (uint64_t)((2048 * kk) >> 4),
-                            idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                mma_bf16_ts(tmem + kATmemO, tmem + kATmemS + 64u * (uint32_t)sb + 8u * (uint32_t)kk,
+                            vdesc + (uint64_t)((2048 * kk) >> 4), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&bars->kv_empty[st]);  // K(j) and V(j) read (S(j) was issued earlier)
-            mma_commit(&bars->p_free[pb]);
             mma_commit(&bars->pv_done);
             if (j + 2 < tiles) ok = issue_s(j + 2);
         }
@@ -245,82 +256,88 @@ __global__ void __launch_bounds__(kAThreads, 1)
             mma_commit(&bars->drain);
             warp_wait(&bars->drain, 0, nullptr, err, kDrainNs);
         }
-    } else if (warp < 4) {
-        // softmax and epilogue: thread = query row
-        const int row = warp * 32 + lane, s = q0 + row;
+    } else if (warp < 8) {
+        // softmax and epilogue: thread = (query row, half of each key tile)
+        const int quad = warp & 3, half = warp >> 2;
+        const int row = quad * 32 + lane, s = q0 + row;
         const bool valid_row = s < args.s_q;
         const int n_vis = valid_row ? visible(L, args.s_q, s, args.causal) : 0;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        float m = -INFINITY, l = 0.f;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const int pair_bar = 1 + quad;  // named barrier of this quadrant's two warps
+        float* xch = reinterpret_cast<float*>(smem + kAOffX);
+        int xe = 0;
+        float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum, relative to m
         for (int j = 0; j < tiles; ++j) {
             const int sb = j & 1;
-            float x[64];
+            const uint32_t sbuf = tmem + lane_base + kATmemS + 64u * (uint32_t)sb;
+            float x[32];
             if (ok) ok = warp_wait(&bars->s_full[sb], (j >> 1) & 1, abort, err, wait_ns);
-            if (!ok) break;
-            tc_fence_after();
-            {
-                uint32_t v0[32], v1[32];
-                tmem_ld32(tmem + lane_base + kATmemS + 64u * (uint32_t)sb, v0);
-                tmem_ld32(tmem + lane_base + kATmemS + 64u * (uint32_t)sb + 32u, v1);
+            if (ok) {
+                tc_fence_after();
+                uint32_t v[32];
+                tmem_ld32(sbuf + 32u * (uint32_t)half, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    x[c] = __uint_as_float(v0[c]) * args.scale_log2;
-                    x[32 + c] = __uint_as_float(v1[c]) * args.scale_log2;
-                }
+                for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]) * args.scale_log2;
             }
-            tc_fence_before();
-            mbar_arrive(&bars->s_free[sb]);
-            const int vcount = min(max(n_vis - j * kAKeys, 0), kAKeys);
-            float mx = -INFINITY;
+            const int vcount = min(max(n_vis - j * kAKeys - 32 * half, 0), 32);
+            float mh = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
+            for (int c = 0; c < 32; ++c) {
                 x[c] = c < vcount ? x[c] : -INFINITY;
-                mx = fmaxf(mx, x[c]);
+                mh = fmaxf(mh, x[c]);
             }
-            // lazy rescale: move the reference max only when the row max grows by more than 2^8
+            // both halves of the row have read their scores after this barrier
+            float* xb = xch + (xe & 1) * (2 * kARows);
+            ++xe;
+            xb[half * kARows + row] = mh;
+            ok = barrier_and(pair_bar, 64, ok);
+            if (!ok) break;
+            const float mx = fmaxf(mh, xb[(half ^ 1) * kARows + row]);
+            // lazy rescale: move the reference max only when the row max grows by
+            // more than 2^8 (both halves take the same decision)
             const bool need = mx > m + kARescale;
             const float alpha = need ? fast_exp2(m - mx) : 1.f;  // 0 when m = -inf
             if (need) {
                 l *= alpha;
                 m = mx;
             }
-            // O rows move to the new reference (warp-uniform decision) once P V of
-            // tile j - 1 has landed; S(j) completing implies P V of tile j - 2 has,
-            // so the barrier is at most one phase behind this wait
+            // this half's O columns move to the new reference (warp-uniform
+            // decision) once P V of tile j - 1 has landed; S(j) completing
+            // implies P V of tile j - 2 has, so the barrier is at most one
+            // phase behind this wait
+            // (both warps of the pair see the same maxima, so they take this branch together)
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 ok = warp_wait(&bars->pv_done, (j - 1) & 1, abort, err, wait_ns);
-                if (!ok) break;
-                tc_fence_after();
+                if (ok) {
+                    tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < 128; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + kATmemO + (uint32_t)c, v);
-                    tmem_wait_ld();
+                    for (int c = 0; c < 64; c += 32) {
+                        uint32_t v[32];
+                        const uint32_t oc = tmem + lane_base + kATmemO + 64u * (uint32_t)half + (uint32_t)c;
+                        tmem_ld32(oc, v);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st32(tmem + lane_base + kATmemO + (uint32_t)c, v);
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                        tmem_st32(oc, v);
+                    }
+                    tmem_wait_st();
                 }
-                tmem_wait_st();
-                tc_fence_before();
+                ok = barrier_and(pair_bar, 64, ok);  // the pair leaves together
+                if (!ok) break;
             }
             const float m_use = m == -INFINITY ? 0.f : m;
-            uint32_t pk[32];
+            uint32_t pk[16];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
+            for (int c = 0; c < 16; ++c) {
                 const float p0 = fast_exp2(x[2 * c] - m_use), p1 = fast_exp2(x[2 * c + 1] - m_use);
                 l += p0 + p1;
                 pk[c] = pack_bf16x2(p0, p1);
             }
-            // P buffer sb held tile j - 2 until its P V finished
-            if (j >= 2) ok = warp_wait(&bars->p_free[sb], ((j >> 1) - 1) & 1, abort, err, wait_ns);
-            if (!ok) break;
-            uint8_t* prow = smem + kAOffP + sb * kPBytes + row * 128;
-#pragma unroll
-            for (int w = 0; w < 8; ++w)
-                *reinterpret_cast<uint4*>(prow + ((w ^ (row & 7)) << 4)) =
-                    make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
-            fence_proxy_async_smem();
+            // P of keys [32 half, 32 half + 32) as bf16 pairs in columns [16 half, 16 half + 16)
+            tmem_st16(sbuf + 16u * (uint32_t)half, pk);
+            tmem_wait_st();
+            tc_fence_before();
             mbar_arrive(&bars->p_full[sb]);
         }
         // epilogue: O / l -> out (bf16), lse. P V of the last two tiles may both be
@@ -328,15 +345,20 @@ __global__ void __launch_bounds__(kAThreads, 1)
         // run two phases ahead of the barrier)
         if (ok && tiles > 1) ok = warp_wait(&bars->pv_done, (tiles - 2) & 1, abort, err, wait_ns);
         if (ok && tiles > 0) ok = warp_wait(&bars->pv_done, (tiles - 1) & 1, abort, err, wait_ns);
+        // the row sum: this half's share plus the other's (both relative to m)
+        float* xb = xch + (xe & 1) * (2 * kARows);
+        xb[half * kARows + row] = l;
+        ok = barrier_and(pair_bar, 64, ok);
         if (ok) {
+            const float l_row = half == 0 ? l + xb[kARows + row] : xb[row] + l;
             tc_fence_after();
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16* dst = args.out + (((size_t)b * args.s_q + s) * args.H + h) * kDV;
+            const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
+            __nv_bfloat16* dst = args.out + (((size_t)b * args.s_q + s) * args.H + h) * kDV + 64 * half;
 #pragma unroll 1
-            for (int c = 0; c < 128; c += 32) {
+            for (int c = 0; c < 64; c += 32) {
                 uint32_t v[32];
                 if (tiles > 0) {
-                    tmem_ld32(tmem + lane_base + kATmemO + (uint32_t)c, v);
+                    tmem_ld32(tmem + lane_base + kATmemO + 64u * (uint32_t)half + (uint32_t)c, v);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
@@ -354,15 +376,15 @@ __global__ void __launch_bounds__(kAThreads, 1)
                     }
                 }
             }
-            if (valid_row)
+            if (valid_row && half == 0)
                 args.lse[((size_t)b * args.s_q + s) * args.H + h] =
-                    l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+                    l_row > 0.f ? (m + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
         }
     }
     if (!ok) *abort = 1;
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kAWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kATmemCols);
     }
