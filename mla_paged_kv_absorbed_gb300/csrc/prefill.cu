@@ -18,10 +18,10 @@
 //
 // Kernels here: the gather of the sequence's latent rows and rope keys into
 // contiguous buffers (the two up-projections then run as batched head GEMMs,
-// gemm.cu), and the attention: one CTA per (b, h, 128-query tile), 64-key
-// tiles of K and V streaming through a TMA ring, S = Q K^T and O += P V on
-// tcgen05 with S (double-buffered), P and O in TMEM, two softmax threads per
-// query row (online softmax, lazy rescaling of O).
+// gemm.cu), and the attention: one CTA per (b, h, two 128-query tiles),
+// 64-key tiles of K and V streaming through a TMA ring and shared by both query
+// tiles, S = Q K^T and O += P V on tcgen05 with S (double-buffered), P and O in
+// TMEM, two softmax threads per query row (online softmax, lazy rescaling of O).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -80,44 +80,50 @@ __global__ void __launch_bounds__(kGatherThreads)
 }
 
 // --------------------------------------------------------------- attention --
-// One CTA per (b, h, 128-query tile). Warps 0-7 run the softmax and the
-// epilogue, two per TMEM lane quadrant: warp w owns rows 32 (w % 4) .. + 31 and
-// keys [32 (w / 4), + 32) of every 64-key tile, and the two warps of a quadrant
-// exchange their half-row maxima (and, at the end, their half sums) through
-// shared memory. Warp 8 is the TMA producer, warp 9 issues the products and
-// owns TMEM. S = Q K^T goes to one of two TMEM buffers; the softmax writes P
-// (bf16 pairs) back over the first 32 columns of the same buffer, and O += P V
-// takes P as the A operand straight from TMEM. The tensor pipe runs a CTA's
-// products in issue order, so S of tile j + 2 (issued after P V of tile j)
-// never overwrites P before it has been read, and P is written only after both
-// halves of a row have read their scores (the max exchange orders them).
-constexpr int kAThreads = 320;
-constexpr int kAWarpProducer = 8;
-constexpr int kAWarpMma = 9;
-constexpr int kARows = 128;     // query rows per CTA
+// One CTA per (b, h, block of 256 query rows) = two 128-row query tiles (t = 0,
+// 1) that share every 64-key tile of K and V, so each K/V byte loaded feeds
+// twice the products. Warps 8t .. 8t + 7 run tile t's softmax and epilogue,
+// two per TMEM lane quadrant: warp w owns rows 32 (w % 4) .. + 31 of its tile
+// and keys [32 ((w / 4) % 2), + 32) of every key tile, and the two warps of a
+// quadrant exchange their half-row maxima (and, at the end, their half sums)
+// through shared memory. Warp 16 is the TMA producer, warp 17 issues the
+// products and owns TMEM (all 512 columns: per tile two 64-column S buffers
+// and a 128-column O). S_t = Q_t K^T goes to one of tile t's S buffers; the
+// softmax writes P (bf16 pairs) back over the first 32 columns of the same
+// buffer, and O_t += P V takes P as the A operand straight from TMEM. The
+// tensor pipe runs a CTA's products in issue order, so S_t of key tile j + 2
+// (issued after P V of tile j) never overwrites P before it has been read, and
+// P is written only after both halves of a row have read their scores.
+constexpr int kATiles = 2;
+constexpr int kAThreads = 576;
+constexpr int kAWarpProducer = 16;
+constexpr int kAWarpMma = 17;
+constexpr int kARows = 128;     // query rows per tile
 constexpr int kAKeys = 64;      // keys per tile
-constexpr int kAStages = 4;
+constexpr int kAStages = 3;
 constexpr int kQBytes = 3 * kARows * 128;   // [3 chunks][128 rows][64]
 constexpr int kKBytes = 3 * kAKeys * 128;   // [3 chunks][64 keys][64]
 constexpr int kVBytesA = 2 * kAKeys * 128;  // [2 chunks][64 keys][64]
-constexpr int kAOffX = 1024;                // [2 episodes][2 halves][128 rows] floats
-constexpr int kAOffQ = 4096;
-constexpr int kAOffK = kAOffQ + kQBytes;
+constexpr int kAXBytes = 2 * 2 * kARows * 4;  // per tile: [2 episodes][2 halves][128 rows] floats
+constexpr int kAOffX = 1024;
+constexpr int kAOffQ = 6144;
+constexpr int kAOffK = kAOffQ + kATiles * kQBytes;
 constexpr int kAOffV = kAOffK + kAStages * kKBytes;
 constexpr int kASmem = kAOffV + kAStages * kVBytesA + 1024;  // + alignment slack
 static_assert(kASmem <= 232448, "prefill attention shared memory");
-static_assert(kAOffX + 2 * 2 * kARows * 4 <= kAOffQ, "exchange area");
+static_assert(kAOffX + kATiles * kAXBytes <= kAOffQ, "exchange area");
 static_assert(kAOffQ % 1024 == 0 && kAOffK % 1024 == 0 && kAOffV % 1024 == 0, "swizzle atoms");
-constexpr uint32_t kATmemS = 0;    // two S buffers of 64 columns (P over the first 32 of each)
-constexpr uint32_t kATmemO = 128;  // O: 128 columns
-constexpr uint32_t kATmemCols = 256;
+constexpr uint32_t kATmemCols = 512;
+// tile t: S buffers at 128 t and 128 t + 64 (P over the first 32 of each), O at 256 + 128 t
+__device__ __forceinline__ uint32_t tmem_s(int t, int sb) { return (uint32_t)(128 * t + 64 * sb); }
+__device__ __forceinline__ uint32_t tmem_o(int t) { return (uint32_t)(256 + 128 * t); }
 constexpr float kARescale = 8.0f;
 
 struct ABars {
     uint64_t q_full;
     uint64_t kv_full[kAStages], kv_empty[kAStages];
-    uint64_t s_full[2], p_full[2];
-    uint64_t pv_done, drain;
+    uint64_t s_full[kATiles][2], p_full[kATiles][2];
+    uint64_t pv_done[kATiles], drain;
     uint32_t tmem_slot;
     int abort;
 };
@@ -142,6 +148,15 @@ __device__ __forceinline__ int visible(int L, int s_q, int s, int causal) {
     return n < 0 ? 0 : (n > L ? L : n);
 }
 
+// Key tiles query tile t (rows q0 + 128 t ..) needs: up to the last visible key
+// of its last valid row (0 when it has no valid row).
+__device__ __forceinline__ int tile_count(int L, const PrefillArgs& args, int q0, int t) {
+    const int first = q0 + kARows * t;
+    const int last_row = min(first + kARows, args.s_q) - 1;
+    const int n_max = last_row >= first ? visible(L, args.s_q, last_row, args.causal) : 0;
+    return (n_max + kAKeys - 1) / kAKeys;
+}
+
 __global__ void __launch_bounds__(kAThreads, 1)
     prefill_attn_kernel(const __grid_constant__ PrefillMaps maps, PrefillArgs args) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -149,8 +164,8 @@ __global__ void __launch_bounds__(kAThreads, 1)
     ABars* bars = reinterpret_cast<ABars*>(smem);
     volatile int* abort = &bars->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int q0 = qt * kARows;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int q0 = blockIdx.x * (kATiles * kARows);
     int* err = args.err;
     const long long wait_ns = args.wait_ns;
 
@@ -160,11 +175,13 @@ __global__ void __launch_bounds__(kAThreads, 1)
             mbar_init(&bars->kv_full[i], 1);
             mbar_init(&bars->kv_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->p_full[i], 256);
+        for (int t = 0; t < kATiles; ++t) {
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&bars->s_full[t][i], 1);
+                mbar_init(&bars->p_full[t][i], 256);
+            }
+            mbar_init(&bars->pv_done[t], 1);
         }
-        mbar_init(&bars->pv_done, 1);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_mbarrier_init_cluster();
@@ -183,19 +200,21 @@ __global__ void __launch_bounds__(kAThreads, 1)
     griddep_wait();
     griddep_launch_dependents();
 
-    // keys this tile needs: up to the last visible key of its last valid row
     const int L = min(max(args.seqlens[b], 0), args.Lmax);  // longer sequences were reported by the gather
-    const int last_row = min(q0 + kARows, args.s_q) - 1;
-    const int n_max = last_row >= q0 ? visible(L, args.s_q, last_row, args.causal) : 0;
-    const int tiles = (n_max + kAKeys - 1) / kAKeys;
+    int tiles_t[kATiles];
+#pragma unroll
+    for (int t = 0; t < kATiles; ++t) tiles_t[t] = tile_count(L, args, q0, t);
+    const int tiles = max(tiles_t[0], tiles_t[1]);  // key tiles the block loads (causal: tile 1's count)
     const int key_row0 = b * args.Lmax;  // first key row of this sequence in the K/V buffers
 
     bool ok = true;
     if (warp == kAWarpProducer) {
-        // producer: the query tile once, then K and V tiles through the ring
+        // producer: both query tiles once, then K and V tiles through the ring
         if (lane == 0 && tiles > 0) {
-            mbar_arrive_expect_tx(&bars->q_full, (uint32_t)kQBytes);
-            tma_load_4d(smem + kAOffQ, &maps.q, &bars->q_full, 0, h, b * args.s_q + q0, 0);
+            mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kATiles * kQBytes));
+            for (int t = 0; t < kATiles; ++t)
+                tma_load_4d(smem + kAOffQ + t * kQBytes, &maps.q, &bars->q_full, 0, h, b * args.s_q + q0 + kARows * t,
+                            0);
             int issued = 0;
             for (int j = 0; j < tiles; ++j) {
                 const int st = j % kAStages;
@@ -215,63 +234,79 @@ __global__ void __launch_bounds__(kAThreads, 1)
         // MMA issuer (whole warp; one elected lane issues)
         const uint32_t idesc_s = idesc_bf16_f32(kARows, kAKeys, false, false);
         const uint32_t idesc_o = idesc_bf16_f32(kARows, 128, false, true);
-        const uint64_t qdesc = desc_sw128(smem_u32(smem + kAOffQ), 0, 1024);
         bool issued = false;
         if (tiles > 0) ok = warp_wait(&bars->q_full, 0, abort, err, wait_ns);
-        auto issue_s = [&](int j) -> bool {
+        // K(j) has landed once kv_full was seen for it; S products of both tiles
+        auto issue_s = [&](int t, int j) {
             const int st = j % kAStages, sb = j & 1;
-            if (!warp_wait(&bars->kv_full[st], (j / kAStages) & 1, abort, err, wait_ns)) return false;
-            tc_fence_after();
+            const uint64_t qdesc = desc_sw128(smem_u32(smem + kAOffQ + t * kQBytes), 0, 1024);
             const uint64_t kdesc = desc_sw128(smem_u32(smem + kAOffK + st * kKBytes), 0, 1024);
 #pragma unroll
             for (int c = 0; c < 3; ++c)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(tmem + kATmemS + 64u * (uint32_t)sb,
-                                qdesc + (uint64_t)((c * kARows * 128 + 32 * kk) >> 4),
+                    mma_bf16_ss(tmem + tmem_s(t, sb), qdesc + (uint64_t)((c * kARows * 128 + 32 * kk) >> 4),
                                 kdesc + (uint64_t)((c * kAKeys * 128 + 32 * kk) >> 4), idesc_s, (c | kk) != 0);
-            mma_commit(&bars->s_full[sb]);
+            mma_commit(&bars->s_full[t][sb]);
+        };
+        auto load_ready = [&](int j) -> bool {
+            if (!warp_wait(&bars->kv_full[j % kAStages], (j / kAStages) & 1, abort, err, wait_ns)) return false;
+            tc_fence_after();
             return true;
         };
-        if (ok && tiles > 0) {
-            ok = issue_s(0);
+        for (int j = 0; ok && j < 2 && j < tiles; ++j) {
+            ok = load_ready(j);
+            if (!ok) break;
             issued = true;
+            for (int t = 0; t < kATiles; ++t)
+                if (j < tiles_t[t]) issue_s(t, j);
         }
-        if (ok && tiles > 1) ok = issue_s(1);
         for (int j = 0; ok && j < tiles; ++j) {
             const int st = j % kAStages, sb = j & 1;
-            ok = warp_wait(&bars->p_full[sb], (j >> 1) & 1, abort, err, wait_ns);
-            if (!ok) break;
-            tc_fence_after();
             const uint64_t vdesc = desc_sw128(smem_u32(smem + kAOffV + st * kVBytesA), kAKeys * 128, 1024);
+            for (int t = 0; ok && t < kATiles; ++t) {
+                if (j >= tiles_t[t]) continue;
+                ok = warp_wait(&bars->p_full[t][sb], (j >> 1) & 1, abort, err, wait_ns);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < kAKeys / 16; ++kk)
-                mma_bf16_ts(tmem + kATmemO, tmem + kATmemS + 64u * (uint32_t)sb + 8u * (uint32_t)kk,
-                            vdesc + (uint64_t)((2048 * kk) >> 4), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&bars->kv_empty[st]);  // K(j) and V(j) read (S(j) was issued earlier)
-            mma_commit(&bars->pv_done);
-            if (j + 2 < tiles) ok = issue_s(j + 2);
+                for (int kk = 0; kk < kAKeys / 16; ++kk)
+                    mma_bf16_ts(tmem + tmem_o(t), tmem + tmem_s(t, sb) + 8u * (uint32_t)kk,
+                                vdesc + (uint64_t)((2048 * kk) >> 4), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bars->pv_done[t]);
+            }
+            if (!ok) break;
+            mma_commit(&bars->kv_empty[st]);  // K(j) and V(j) read by every product of tile j
+            if (j + 2 < tiles) {
+                ok = load_ready(j + 2);
+                if (!ok) break;
+                for (int t = 0; t < kATiles; ++t)
+                    if (j + 2 < tiles_t[t]) issue_s(t, j + 2);
+            }
         }
         if (issued) {
             mma_commit(&bars->drain);
             warp_wait(&bars->drain, 0, nullptr, err, kDrainNs);
         }
-    } else if (warp < 8) {
-        // softmax and epilogue: thread = (query row, half of each key tile)
-        const int quad = warp & 3, half = warp >> 2;
-        const int row = quad * 32 + lane, s = q0 + row;
+    } else if (warp < 8 * kATiles) {
+        // softmax and epilogue of query tile t: thread = (query row, half of each key tile)
+        const int t = warp >> 3;
+        const int quad = warp & 3, half = (warp >> 2) & 1;
+        const int row = quad * 32 + lane, s = q0 + kARows * t + row;
         const bool valid_row = s < args.s_q;
         const int n_vis = valid_row ? visible(L, args.s_q, s, args.causal) : 0;
+        const int tiles_my = tiles_t[t];
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const int pair_bar = 1 + quad;  // named barrier of this quadrant's two warps
-        float* xch = reinterpret_cast<float*>(smem + kAOffX);
+        const uint32_t ocol = tmem + lane_base + tmem_o(t) + 64u * (uint32_t)half;  // this half's 64 O columns
+        const int pair_bar = 1 + 4 * t + quad;  // named barrier of this quadrant's two warps
+        float* xch = reinterpret_cast<float*>(smem + kAOffX + t * kAXBytes);
         int xe = 0;
         float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum, relative to m
-        for (int j = 0; j < tiles; ++j) {
+        for (int j = 0; j < tiles_my; ++j) {
             const int sb = j & 1;
-            const uint32_t sbuf = tmem + lane_base + kATmemS + 64u * (uint32_t)sb;
+            const uint32_t sbuf = tmem + lane_base + tmem_s(t, sb);
             float x[32];
-            if (ok) ok = warp_wait(&bars->s_full[sb], (j >> 1) & 1, abort, err, wait_ns);
+            if (ok) ok = warp_wait(&bars->s_full[t][sb], (j >> 1) & 1, abort, err, wait_ns);
             if (ok) {
                 tc_fence_after();
                 uint32_t v[32];
@@ -303,23 +338,22 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 m = mx;
             }
             // this half's O columns move to the new reference (warp-uniform
-            // decision) once P V of tile j - 1 has landed; S(j) completing
-            // implies P V of tile j - 2 has, so the barrier is at most one
-            // phase behind this wait
-            // (both warps of the pair see the same maxima, so they take this branch together)
+            // decision) once P V of key tile j - 1 has landed; S(j) completing
+            // implies P V of tile j - 2 has, so the barrier is at most one phase
+            // behind this wait. Both warps of the pair see the same maxima, so
+            // they take this branch together.
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                ok = warp_wait(&bars->pv_done, (j - 1) & 1, abort, err, wait_ns);
+                ok = warp_wait(&bars->pv_done[t], (j - 1) & 1, abort, err, wait_ns);
                 if (ok) {
                     tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < 64; c += 32) {
                         uint32_t v[32];
-                        const uint32_t oc = tmem + lane_base + kATmemO + 64u * (uint32_t)half + (uint32_t)c;
-                        tmem_ld32(oc, v);
+                        tmem_ld32(ocol + (uint32_t)c, v);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                        tmem_st32(oc, v);
+                        tmem_st32(ocol + (uint32_t)c, v);
                     }
                     tmem_wait_st();
                 }
@@ -338,13 +372,13 @@ __global__ void __launch_bounds__(kAThreads, 1)
             tmem_st16(sbuf + 16u * (uint32_t)half, pk);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&bars->p_full[sb]);
+            mbar_arrive(&bars->p_full[t][sb]);
         }
-        // epilogue: O / l -> out (bf16), lse. P V of the last two tiles may both be
-        // outstanding: wait for their phases in order (a parity wait must never
-        // run two phases ahead of the barrier)
-        if (ok && tiles > 1) ok = warp_wait(&bars->pv_done, (tiles - 2) & 1, abort, err, wait_ns);
-        if (ok && tiles > 0) ok = warp_wait(&bars->pv_done, (tiles - 1) & 1, abort, err, wait_ns);
+        // epilogue: O / l -> out (bf16), lse. P V of the last two key tiles may
+        // both be outstanding: wait for their phases in order (a parity wait
+        // must never run two phases ahead of the barrier)
+        if (ok && tiles_my > 1) ok = warp_wait(&bars->pv_done[t], (tiles_my - 2) & 1, abort, err, wait_ns);
+        if (ok && tiles_my > 0) ok = warp_wait(&bars->pv_done[t], (tiles_my - 1) & 1, abort, err, wait_ns);
         // the row sum: this half's share plus the other's (both relative to m)
         float* xb = xch + (xe & 1) * (2 * kARows);
         xb[half * kARows + row] = l;
@@ -357,8 +391,8 @@ __global__ void __launch_bounds__(kAThreads, 1)
 #pragma unroll 1
             for (int c = 0; c < 64; c += 32) {
                 uint32_t v[32];
-                if (tiles > 0) {
-                    tmem_ld32(tmem + lane_base + kATmemO + 64u * (uint32_t)half + (uint32_t)c, v);
+                if (tiles_my > 0) {
+                    tmem_ld32(ocol + (uint32_t)c, v);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
@@ -443,7 +477,7 @@ cudaError_t launch_prefill_attn(const CUtensorMap* tq, const CUtensorMap* tk, co
     a.err = &g_prefill_error;
     a.wait_ns = wait_ns;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((s_q + kARows - 1) / kARows), (unsigned)H, (unsigned)B);
+    cfg.gridDim = dim3((unsigned)((s_q + kATiles * kARows - 1) / (kATiles * kARows)), (unsigned)H, (unsigned)B);
     cfg.blockDim = dim3(kAThreads, 1, 1);
     cfg.dynamicSmemBytes = kASmem;
     cfg.stream = stream;
