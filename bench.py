@@ -80,6 +80,8 @@ def parse():
                    help="time only the prefill workload and print its object (a short run for a profiler)")
     p.add_argument("--prefill-batch", type=int, default=8, help="prompts in the prefill workload")
     p.add_argument("--prefill-calls", type=int, default=5)
+    p.add_argument("--int8", action="store_true",
+                   help="with --profile: the step decodes over the INT8 cache (mla_decode_paged_q8)")
     return p.parse_args()
 
 
@@ -238,7 +240,7 @@ def run_step(L, a: StepArgs, ev=None, meta=False):
         rc |= L.mla_absorb_q(*a.absorb)
     if ev is not None:
         ev[0].record()
-    rc |= L.mla_decode_paged(*a.decode)
+    rc |= L.mla_decode_paged_q8(*a.decode_q8) if a.decode_q8 is not None else L.mla_decode_paged(*a.decode)
     if ev is not None:
         ev[1].record()
     if a.proj is not None:
@@ -480,7 +482,10 @@ def run_ours(args, world, rank, local):
     num_parts = api.mla_default_num_parts(local, s_q)
     ws = api.make_workspace(B, s_q, H, num_parts, dev)
     stream = torch.cuda.current_stream(dev)
-    steps = [StepArgs(api, s, num_parts, ws, stream.cuda_stream) for s in sets]
+    if args.int8 and not args.profile:
+        raise SystemExit("--int8 is a profiling option: use it with --profile")
+    q8c = [api.mla_quantize_cache(s.kv_cache) for s in sets] if args.int8 else [None] * n_sets
+    steps = [StepArgs(api, s, num_parts, ws, stream.cuda_stream, q) for s, q in zip(sets, q8c)]
     launches_per_step = sum(x is not None for x in (steps[0].absorb, steps[0].proj)) + 2  # + decode, combine
 
     # the schedule of each input set (fixed lengths), then warm-up and a

@@ -295,10 +295,12 @@ int mla_decode_paged_q8(const mla_bf16_t* q_abs, const uint8_t* kv8, const float
  * bytes, 1024-byte aligned (no zero-fill needed): holds the gathered latent and
  * the decompressed K and V (bf16) of every sequence, padded to
  * max_blocks_per_seq pages. Any s_q >= 1; H in {16, 32, 64, 128}.
- * Launches a gather, two batched head GEMMs (tcgen05) and the attention
- * kernel (one CTA per (sequence, head, 128-query tile); tcgen05 with S and O in
- * tensor memory). A block id outside the pool is recorded as MLA_ERR_BAD_BLOCK
- * in the library's error word and its rows read as zeros.
+ * Launches a gather, two batched head GEMMs (tcgen05, the head's weight resident
+ * per CTA) and the attention kernel (one CTA per (sequence, head, 256 query
+ * rows) as two 128-row tiles sharing each K/V tile; tcgen05 with S, P and O in
+ * tensor memory). A block id outside the pool, or a sequence longer than its
+ * table row, is recorded as MLA_ERR_BAD_BLOCK in the library's error word and
+ * those rows read as zeros.
  */
 size_t mla_prefill_workspace_size(int B, int H, int max_blocks_per_seq);
 int mla_prefill_paged(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int num_blocks, const int32_t* block_table,
