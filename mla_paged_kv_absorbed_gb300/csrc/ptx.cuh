@@ -226,6 +226,26 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 
 // The mbarrier gets one arrival when every tcgen05 op the elected lane issued
 // before the commit has completed (all lanes call it).
+// Four TS products that accumulate into the same D, issued under one
+// elect.sync: the A operands are a0 + {0, 8, 16, 24} TMEM columns (four 16-deep
+// K-steps of a 64-wide chunk) and the B descriptors b0 + {0, 2, 4, 6} (32 bytes
+// apart); only the first product may start a fresh accumulation (accumulate = 0).
+__device__ __forceinline__ void mma_bf16_ts4(uint32_t d_tmem, uint32_t a0, uint64_t b0, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, 0, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, t;\n\t}" ::"r"(d_tmem),
+        "r"(a0), "l"(b0), "r"(idesc), "r"(accumulate), "r"(a0 + 8u), "l"(b0 + 2ull), "r"(a0 + 16u), "l"(b0 + 4ull),
+        "r"(a0 + 24u), "l"(b0 + 6ull)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
