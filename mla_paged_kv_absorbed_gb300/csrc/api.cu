@@ -418,6 +418,7 @@ int mla_prefill_paged(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int num_b
     const PrefillLayout pl = prefill_layout(B, H, max_blocks_per_seq);
     if (workspace_bytes < pl.total || (uint64_t)B * s_q > 0x7FFFFFFFull || pl.rows > 0x7FFFFFFFull)
         return MLA_ERR_INVALID_ARG;
+    if (B > 65535) return MLA_ERR_INVALID_ARG;  // attention grid (query blocks, H, B)
     int dev = check_device();
     if (dev != MLA_OK) return dev;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -164,6 +164,9 @@ __global__ void __launch_bounds__(kAThreads, 1)
     ABars* bars = reinterpret_cast<ABars*>(smem);
     volatile int* abort = &bars->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // grid (query blocks, H, B), launched x fastest: the blocks of one (sequence,
+    // head) run side by side and share its K and V in L2 (launching the longest
+    // blocks of every head first measured slower: their K/V outgrew the L2)
     const int h = blockIdx.y, b = blockIdx.z;
     const int q0 = blockIdx.x * (kATiles * kARows);
     int* err = args.err;
