@@ -304,6 +304,10 @@ __global__ void __launch_bounds__(kAThreads, 1)
         const int pair_bar = 1 + 4 * t + quad;  // named barrier of this quadrant's two warps
         float* xch = reinterpret_cast<float*>(smem + kAOffX + t * kAXBytes);
         int xe = 0;
+        // scores stay unscaled (x = q . k, m their running max); the scale goes
+        // into the exponent's FMA: p = 2^(x s - m s), s = softmax scale * log2(e)
+        const float sc = args.scale_log2;
+        const float thr = kARescale / sc;  // the lazy-rescale margin in unscaled units
         float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum, relative to m
         for (int j = 0; j < tiles_my; ++j) {
             const int sb = j & 1;
@@ -316,15 +320,18 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 tmem_ld32(sbuf + 32u * (uint32_t)half, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]) * args.scale_log2;
+                for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]);
             }
+            // keys past the visible ones are masked by selection (only the tiles
+            // on the diagonal and past the sequence have any)
             const int vcount = min(max(n_vis - j * kAKeys - 32 * half, 0), 32);
+            if (vcount < 32) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) x[c] = c < vcount ? x[c] : -INFINITY;
+            }
             float mh = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                x[c] = c < vcount ? x[c] : -INFINITY;
-                mh = fmaxf(mh, x[c]);
-            }
+            for (int c = 0; c < 32; ++c) mh = fmaxf(mh, x[c]);
             // both halves of the row have read their scores after this barrier
             float* xb = xch + (xe & 1) * (2 * kARows);
             ++xe;
@@ -334,8 +341,8 @@ __global__ void __launch_bounds__(kAThreads, 1)
             const float mx = fmaxf(mh, xb[(half ^ 1) * kARows + row]);
             // lazy rescale: move the reference max only when the row max grows by
             // more than 2^8 (both halves take the same decision)
-            const bool need = mx > m + kARescale;
-            const float alpha = need ? fast_exp2(m - mx) : 1.f;  // 0 when m = -inf
+            const bool need = mx > m + thr;
+            const float alpha = need ? fast_exp2((m - mx) * sc) : 1.f;  // 0 when m = -inf
             if (need) {
                 l *= alpha;
                 m = mx;
@@ -363,11 +370,11 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 ok = barrier_and(pair_bar, 64, ok);  // the pair leaves together
                 if (!ok) break;
             }
-            const float m_use = m == -INFINITY ? 0.f : m;
+            const float ms = m == -INFINITY ? 0.f : m * sc;
             uint32_t pk[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-                const float p0 = fast_exp2(x[2 * c] - m_use), p1 = fast_exp2(x[2 * c + 1] - m_use);
+                const float p0 = fast_exp2(fmaf(x[2 * c], sc, -ms)), p1 = fast_exp2(fmaf(x[2 * c + 1], sc, -ms));
                 l += p0 + p1;
                 pk[c] = pack_bf16x2(p0, p1);
             }
@@ -415,7 +422,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
             }
             if (valid_row && half == 0)
                 args.lse[((size_t)b * args.s_q + s) * args.H + h] =
-                    l_row > 0.f ? (m + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
+                    l_row > 0.f ? (m * sc + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
         }
     }
     if (!ok) *abort = 1;
