@@ -496,6 +496,10 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
     const float* scales = reinterpret_cast<const float*>(smem + kOffScale);
     PageIter pi;
     pi.init(args, part);
+    // scores stay unscaled (x = q' . k; reference maxima in the same units); the
+    // scale goes into the exponent's FMA: p = 2^(x s - m s), s = scale * log2(e)
+    const float sc = args.scale_log2;
+    const float thr = kRescaleThreshold / sc;  // the lazy-rescale margin in unscaled units
     float m_own = -INFINITY, l = 0.f;  // this thread's share of the row sum, relative to m_own
     int n_valid = 0, xe = 0, r = 0;
     bool ok = true;
@@ -573,18 +577,33 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
             tmem_ld32(tmem + lane_base + kTmemS + 64u * (uint32_t)sb + 32u * (uint32_t)half, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]) * args.scale_log2;
+            for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]);
             tc_fence_before();
             mbar_arrive(&bars->s_free[sb]);
         }
         // keys of this half; columns past the visible keys are masked by
         // selection, so whatever the tail rows of the page hold never leaks
         const int vcount = min(max(n_valid - pi.j * kPage - 32 * half, 0), 32);
+        if (vcount < 32) {  // (only a sequence's last page has such keys)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) x[c] = c < vcount ? x[c] : -INFINITY;
+        }
         float mh = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            x[c] = c < vcount ? x[c] : -INFINITY;
-            mh = fmaxf(mh, x[c]);
+        for (int c = 0; c < 32; ++c) mh = fmaxf(mh, x[c]);
+        // the reference max before this page: none at an item's first page,
+        // else the value the other group published after page n - 1. Both warps
+        // of the pair read it before the pair barrier, and the half-0 warp
+        // publishes this page's value only after that barrier. The next
+        // publication on the same barrier (page n + 1, whose group waits for
+        // this page's, or passes an item start with both groups) therefore
+        // cannot come before both warps have taken page n - 1's: a warp that
+        // fell behind its partner would otherwise find the barrier two phases
+        // on and wait for a phase that never completes.
+        float m_prev = -INFINITY;
+        if (!first) {
+            if (ok) ok = warp_wait(&bars->ref_full[buf ^ 1][quad], ((n - 1) >> 1) & 1, abort, err, wait_ns);
+            m_prev = xref[(buf ^ 1) * kRows + row];
         }
         float* xb = xpair + (xe & 1) * (2 * kRows);
         ++xe;
@@ -592,32 +611,25 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
         ok = barrier_and(pair_bar, 64, ok);
         if (!ok) break;
         const float mx = fmaxf(mh, xb[(half ^ 1) * kRows + row]);
-        // the reference max before this page: none at an item's first page,
-        // else the value the other group published after page n - 1
-        float m_prev = -INFINITY;
-        if (!first) {
-            ok = warp_wait(&bars->ref_full[buf ^ 1][quad], ((n - 1) >> 1) & 1, abort, err, wait_ns);
-            m_prev = xref[(buf ^ 1) * kRows + row];
-        }
         // lazy rescale: the reference max moves only when the row max exceeds it
         // by more than 2^8; both warps of a pair take the same decision
-        const bool need = mx > m_prev + kRescaleThreshold;
+        const bool need = mx > m_prev + thr;
         const float m_new = need ? mx : m_prev;
-        const float alpha = need ? fast_exp2(m_prev - mx) : 1.f;  // 0 when m_prev = -inf
+        const float alpha = need ? fast_exp2((m_prev - mx) * sc) : 1.f;  // 0 when m_prev = -inf
         if (half == 0) {
             xref[buf * kRows + row] = m_new;
             mbar_arrive(&bars->ref_full[buf][quad]);
         }
         if (m_new != m_own) {
-            if (l > 0.f) l *= fast_exp2(m_own - m_new);
+            if (l > 0.f) l *= fast_exp2((m_own - m_new) * sc);
             m_own = m_new;
         }
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float ms = m_new == -INFINITY ? 0.f : m_new * sc;
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
             // the row sum takes the fp32 probabilities; only the P.V operand is bf16
-            const float p0 = fast_exp2(x[2 * c] - m_use), p1 = fast_exp2(x[2 * c + 1] - m_use);
+            const float p0 = fast_exp2(fmaf(x[2 * c], sc, -ms)), p1 = fast_exp2(fmaf(x[2 * c + 1], sc, -ms));
             l += p0 + p1;
             pk[c] = pack_bf16x2(p0, p1);
         }
@@ -652,14 +664,15 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
                 if (ok) ok = warp_wait(&bars->lsum_full[quad], qi & 1, abort, err, wait_ns);
                 const float l_oth = xlsum[((g ^ 1) * 2) * kRows + row] + xlsum[((g ^ 1) * 2 + 1) * kRows + row];
                 const float m_oth = xlmax[(g ^ 1) * kRows + row];
-                l_row += l_oth > 0.f ? l_oth * fast_exp2(m_oth - m_new) : 0.f;
+                l_row += l_oth > 0.f ? l_oth * fast_exp2((m_oth - m_new) * sc) : 0.f;
             }
             if (ok && half == 0) {
                 const float inv_l = l_row > 0.f ? 1.f / l_row : 0.f;
                 st_async_b32(x_remote + (uint32_t)(pb * 1024 + 512 + row * 4), __float_as_uint(inv_l), mbar);
                 if (row < args.H) {
-                    // lse in natural log: x is in log2 units of the scaled score
-                    const float lse_v = l_row > 0.f ? (m_new + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
+                    // lse in natural log of the scaled scores: m s + log2 l is in log2 units
+                    const float lse_v =
+                        l_row > 0.f ? (m_new * sc + log2f(l_row)) * 0.69314718055994530942f : -INFINITY;
                     if (pi.it.split)
                         args.lse_part[((size_t)pi.it.piece * args.s_q + s) * args.H + row] = lse_v;
                     else

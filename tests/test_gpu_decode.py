@@ -177,7 +177,7 @@ def test_named_workload_full_parity(api, name, end_to_end, rep):
 
 # ------------------------------------------------------ repeated launches --
 
-@pytest.mark.parametrize("name,calls", [("dsv3", 400), ("varlen", 300), ("spec", 60)])
+@pytest.mark.parametrize("name,calls", [("dsv3", 400), ("varlen", 300), ("spec", 60), ("long", 100)])
 def test_repeated_calls_no_device_error(api, name, calls):
     """Hundreds of back-to-back calls, so that the cross-CTA handshakes of the
     decode kernel meet many different timings: the device error word stays

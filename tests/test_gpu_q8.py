@@ -211,3 +211,32 @@ NAMED = ["dsv3", "varlen", "long", "spec"]
 def test_q8_named_workload_full_parity(api, name):
     inp = gen.make_workload(name, rep=0)
     check_q8(inp, run_q8(api, inp))
+
+
+@pytest.mark.parametrize("name,calls", [("long", 120), ("spec", 60), ("varlen", 200)])
+def test_q8_repeated_calls_no_device_error(api, name, calls):
+    """Back-to-back INT8 decode calls: the in-place expansion lengthens the
+    score side's per-page chain, so the cross-warp handshakes (the reference
+    max passed between the two softmax groups above all) meet timings the bf16
+    path rarely produces. The device error word stays clear and every call
+    returns the first call's bytes."""
+    d = gen.make_workload(name).to("cuda")
+    kv8, sc = quantise(api, d.kv_cache)
+    tm, ns = api.mla_get_metadata(d.seqlens, d.s_q, d.H)
+    q_abs = d.q_abs if d.q is None else api.mla_absorb_q(d.q, d.w_uk)
+    ws = api.make_workspace(d.B, d.s_q, d.H, tm.shape[0])
+    o0, lse0 = api.mla_decode_paged_q8(q_abs, kv8, sc, d.block_table, d.seqlens, tm, ns, d.scale, d.causal,
+                                       workspace=ws)
+    assert api.mla_read_device_error(ws) == 0
+    o, lse = torch.empty_like(o0), torch.empty_like(lse0)
+    api.mla_set_wait_limit_ns(250_000_000)  # a lost wakeup shows up in a quarter second
+    try:
+        for i in range(calls):
+            api.mla_decode_paged_q8(q_abs, kv8, sc, d.block_table, d.seqlens, tm, ns, d.scale, d.causal,
+                                    o_lat=o, lse=lse, workspace=ws)
+            if i % 20 == 19 or i == calls - 1:
+                assert api.mla_read_device_error(ws) == 0, f"device status after call {i}"
+                assert torch.equal(o.view(torch.int16), o0.view(torch.int16))
+                assert torch.equal(lse, lse0)
+    finally:
+        api.mla_set_wait_limit_ns(0)
