@@ -364,6 +364,18 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
+// The same for a K-major operand with 64-byte swizzle (swizzle mode 4): rows
+// of 64 bytes (32 bf16), 8-row atoms of 512 bytes `sbo` bytes apart, the K
+// step a +32-byte start offset inside a row.
+__device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)4 << 61;
+    return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A/B and fp32 D.
 //  bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
 //  bit 15 A major (0 = K-major), bit 16 B major (1 = MN-major),
