@@ -95,11 +95,13 @@ constexpr int kRing = 3;
 constexpr int kOffRing = kOffRole;
 constexpr int kSmemScore = kOffRing + kRing * kPageBytes;
 // value CTA
-// P of a page, [128 rows x 64 keys] bf16, as two K-major half tiles (keys
-// [0, 32) and [32, 64)) of [128 rows][64 B] with 64-byte swizzle: the 32 rows
-// a softmax warp owns are then 2 KB of contiguous bytes in one half tile.
+// P of a page, [128 rows x 64 keys] bf16, K-major without swizzle: eight key
+// blocks of 8 keys, each [128 rows][16 B] (core matrices of 8 rows x 16 B are
+// 128 contiguous bytes, 128 B apart along the rows and kPBlockBytes apart
+// along K). One 16-byte word of P for each of a softmax warp's 32 rows is then
+// 512 contiguous bytes.
 constexpr int kPSlotBytes = kRows * 128;
-constexpr int kPHalfBytes = kRows * 64;
+constexpr int kPBlockBytes = kRows * 16;
 constexpr int kVBytes = 8 * kChunkBytes;           // a page's value columns: [8 chunks][64 keys][64 dims]
 constexpr int kVRing = 2;
 constexpr int kOffXV = kOffX;                      // value: [P slot][rescale factor 128 | 1/l 128] fp32
@@ -642,43 +644,16 @@ __device__ bool score_softmax(const DecodeArgs& args, Bars* bars, uint8_t* smem,
         if (ok && n >= kPSlots) ok = warp_wait(&bars->p_free[pb], ((n / kPSlots) - 1) & 1, abort, err, wait_ns);
         const uint32_t mbar = pfull_remote + (uint32_t)pb * 8u;
         if (ok) {
-            // This warp's tile: rows 32 quad + i (i = lane of the row's owner),
-            // 16-byte words w = keys [32 half + 8 w, +8), stored in half tile
-            // `half` at row * 64 + 16 (w ^ ((row / 2) % 4)) (64-byte swizzle).
-            // Each st.async of the warp writes 512 contiguous bytes (rows
-            // 8 j .. 8 j + 7): cross-cluster stores cost far less that way than
-            // 32 rows' 16 bytes 64 bytes apart (measured 8 % of the spec
-            // workload's call). Lane L of store j writes word (L % 4) ^ (L / 8)
-            // of row 8 j + L / 4; a 4 x 4 transpose (lane bits 3-4 <-> word
-            // index) and one gather per store bring the words there.
-            // (1) butterfly: afterwards lane a + 8 x holds, in word slot j,
-            //     word x of row 8 j + a
+            // Word w of this row (keys 32 half + 8 w .. + 8) goes to key block
+            // 4 half + w at row * 16: each st.async of the warp writes 512
+            // contiguous bytes. (Cross-cluster stores of 32 rows' 16 bytes at a
+            // 128-byte stride, as a 128-byte-swizzled tile would need, cost
+            // about 10 % of the spec workload's call.)
+            const uint32_t dst = p_remote + (uint32_t)(pb * kPSlotBytes + 4 * half * kPBlockBytes + row * 16);
 #pragma unroll
-            for (int bit = 0; bit < 2; ++bit) {
-                const bool hi = (lane >> (3 + bit)) & 1;
-#pragma unroll
-                for (int s0 = 0; s0 < 4; ++s0) {
-                    if ((s0 >> bit) & 1) continue;
-                    const int s1 = s0 | (1 << bit);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t send = hi ? pk[4 * s0 + c] : pk[4 * s1 + c];
-                        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 8 << bit);
-                        if (hi)
-                            pk[4 * s0 + c] = recv;
-                        else
-                            pk[4 * s1 + c] = recv;
-                    }
-                }
-            }
-            // (2) store j: lane L takes slot j from lane L / 4 + 8 ((L % 4) ^ (L / 8))
-            const int src = (lane >> 2) + 8 * ((lane & 3) ^ (lane >> 3));
-            const uint32_t dst = p_remote + (uint32_t)(pb * kPSlotBytes + half * kPHalfBytes + quad * 2048 + lane * 16);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                st_async_u4(dst + (uint32_t)(j * 512), __shfl_sync(0xffffffffu, pk[4 * j], src),
-                            __shfl_sync(0xffffffffu, pk[4 * j + 1], src), __shfl_sync(0xffffffffu, pk[4 * j + 2], src),
-                            __shfl_sync(0xffffffffu, pk[4 * j + 3], src), mbar);
+            for (int w = 0; w < 4; ++w)
+                st_async_u4(dst + (uint32_t)(w * kPBlockBytes), pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3],
+                            mbar);
             if (half == 0)
                 st_async_b32(x_remote + (uint32_t)(pb * 1024 + row * 4), __float_as_uint(row < args.H ? alpha : 1.f),
                              mbar);
@@ -800,16 +775,15 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
         }
         tc_fence_after();
         {
-            // whole warp, one elected lane issues; K-steps 0-1 read the first
-            // half tile of P, 2-3 the second
-            const uint32_t pslot = smem_u32(smem + kOffP + k * kPSlotBytes);
-            const uint64_t adesc0 = desc_sw64(pslot, 512), adesc1 = desc_sw64(pslot + kPHalfBytes, 512);
+            // whole warp, one elected lane issues; K-step kk reads key blocks
+            // 2 kk and 2 kk + 1 of P
+            const uint64_t adesc = desc_noswz(smem_u32(smem + kOffP + k * kPSlotBytes), kPBlockBytes, 128);
             const uint64_t vdesc = desc_sw128(smem_u32(vs), kChunkBytes, 1024);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
 #pragma unroll
                 for (int kk = 0; kk < kPage / 16; ++kk)
-                    mma_bf16_ss(tmem + 256u * h, (kk < 2 ? adesc0 : adesc1) + (uint64_t)((32 * (kk & 1)) >> 4),
+                    mma_bf16_ss(tmem + 256u * h, adesc + (uint64_t)((2 * kPBlockBytes * kk) >> 4),
                                 vdesc + (uint64_t)((4 * h * kChunkBytes + 2048 * kk) >> 4), idesc_pv,
                                 (first && kk == 0) ? 0u : 1u);
             }

@@ -364,15 +364,15 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
-// The same for a K-major operand with 64-byte swizzle (swizzle mode 4): rows
-// of 64 bytes (32 bf16), 8-row atoms of 512 bytes `sbo` bytes apart, the K
-// step a +32-byte start offset inside a row.
-__device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr, uint32_t sbo) {
+// The same for a K-major operand without swizzle: 8-row x 16-byte core
+// matrices of 128 contiguous bytes, `lbo` bytes apart along K and `sbo` bytes
+// apart along M/N (swizzle mode 0).
+__device__ __forceinline__ uint64_t desc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
     d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;
-    d |= (uint64_t)4 << 61;
     return d;
 }
 
