@@ -106,9 +106,12 @@ constexpr int kVBytes = 8 * kChunkBytes;           // a page's value columns: [8
 constexpr int kVRing = 2;
 constexpr int kOffXV = kOffX;                      // value: [P slot][rescale factor 128 | 1/l 128] fp32
 constexpr int kOffP = kOffRole;                    // value: kPSlots P slots
-// P slots: page n's message goes to slot n % kPSlots. Two: a third let the
-// softmax run further ahead but made the long multi-token workload 12 % slower.
-constexpr int kPSlots = 2;
+// P slots: page n's message goes to slot n % kPSlots. Three let the softmax
+// run a page further ahead of the P.V products (1 % faster on the multi-token
+// workload; while P still crossed the cluster as 16-byte stores 128 bytes
+// apart, a third slot made it 12 % slower).
+constexpr int kPSlots = 3;
+static_assert(kPSlots <= 3, "two pv_done barriers cover P slots up to three");
 constexpr int kOffV = kOffP + kPSlots * kPSlotBytes;  // value: the value ring
 constexpr int kSmemValue = kOffV + kVRing * kVBytes;
 constexpr int kSmemUsed = kSmemScore > kSmemValue ? kSmemScore : kSmemValue;
@@ -155,7 +158,12 @@ struct Bars {
     // value CTA
     uint64_t p_full[kPSlots];  // own arrive + expect_tx, bytes from the score CTA
     uint64_t v_full[kVRing], v_empty[kVRing];
-    uint64_t pv_done, o_full;
+    // [page % 2]: the page's P.V products are done. The O warps wait for page
+    // n - 1's before moving O to a new reference max at page n; P(n) arriving
+    // means the products of page n - kPSlots are done, so with two barriers the
+    // one waited on (last phase: page n - 3) is never two phases behind.
+    uint64_t pv_done[2];
+    uint64_t o_full;
     uint64_t o_ack[kPSlots];  // per P slot: the O warps have read the slot's factors
     uint64_t o_free[2];
     uint64_t stage_full, stage_free;  // epilogue rounds: eight warps staged / staging read by the store
@@ -790,7 +798,7 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
             // the last page's slot becomes the epilogue's staging area, which
             // hands it back to the producer
             if (!last) mma_commit(&bars->v_empty[n % kVRing]);
-            mma_commit(&bars->pv_done);
+            mma_commit(&bars->pv_done[n & 1]);
             if (last) mma_commit(&bars->o_full);
             mma_commit_multicast(&bars->p_free[k], (uint16_t)1u);  // arrives on the score CTA (rank 0)
         }
@@ -854,7 +862,7 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
                 // O rows of this warp move to the new reference max (after the
                 // previous P.V product has landed)
-                ok = warp_wait(&bars->pv_done, (n - 1) & 1, abort, err, wait_ns);
+                ok = warp_wait(&bars->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort, err, wait_ns);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll 1
@@ -1018,7 +1026,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->v_full[i], 1);
             mbar_init(&bars->v_empty[i], 1);
         }
-        mbar_init(&bars->pv_done, 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&bars->pv_done[i], 1);
         mbar_init(&bars->o_full, 1);
         for (int q = 0; q < 4; ++q) mbar_init(&bars->lsum_full[q], 64);
         mbar_init(&bars->stage_full, kOWarps);
