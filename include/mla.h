@@ -184,6 +184,30 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
                      void* workspace, size_t workspace_bytes, mla_stream_t stream);
 
 /*
+ * mla_decode_out_proj - mla_decode_paged followed by mla_out_proj, with the
+ * split merge and the output projection fused into one finalize kernel.
+ * Pages: as mla_decode_paged and mla_out_proj; the fusion follows [SC] Fig. 1
+ * text (the output projection inside the attention operator, to save the
+ * round trip of the attention output).
+ *
+ * out[b,s,h,j] = sum_{c<512} o[b,s,h,c] * w_uv[h,c,j], o the attention output
+ * of mla_decode_paged (rounded to bf16, as o_lat is there); lse as there.
+ * Arguments as mla_decode_paged, plus w_uv: bf16 [H, 512, 128] and out (out):
+ * bf16 [B, s_q, H, 128]. o_lat: bf16 [B, s_q, H, 512] scratch: only the rows of
+ * sequences that were not split (num_splits) are written there; the merged
+ * rows of split sequences go straight into the projection and are never
+ * stored. The workspace must be as large as mla_decode_paged's.
+ * Launches the decode kernel and the finalize kernel (W_UV[h] resident in
+ * shared memory; eight warps merge each 128-row tile's pieces into the
+ * product's operand; tcgen05 products into TMEM; TMA stores of out).
+ */
+int mla_decode_out_proj(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int num_blocks,
+                        const int32_t* block_table, int max_blocks_per_seq, const int32_t* cache_seqlens, int B,
+                        int s_q, int H, const int32_t* tile_meta, const int32_t* num_splits, int num_parts,
+                        float softmax_scale, int causal, const mla_bf16_t* w_uv, mla_bf16_t* o_lat, mla_bf16_t* out,
+                        float* lse, void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/*
  * mla_out_proj - output up-projection. Pages: [V3] sec. 2.2 (v = W_UV c, applied
  * after attention on the latent side), [SC] (output projection step).
  * out[b,s,h,j] = sum_{c<512} o_lat[b,s,h,c] * w_uv[h,c,j]

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmla.so")
-SOURCES = ["api.cu", "metadata.cu", "gemm.cu", "decode.cu", "combine.cu", "rope.cu", "quant.cu", "prefill.cu", "debug.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "metadata.cu", "gemm.cu", "decode.cu", "combine.cu", "finalize.cu", "rope.cu", "quant.cu", "prefill.cu", "debug.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

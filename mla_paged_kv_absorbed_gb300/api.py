@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.mla_absorb_q.restype = I
         L.mla_decode_paged.argtypes = [P, P, I, P, I, P, I, I, I, P, P, I, F, I, P, P, P, SZ, P]
         L.mla_decode_paged.restype = I
+        L.mla_decode_out_proj.argtypes = [P, P, I, P, I, P, I, I, I, P, P, I, F, I, P, P, P, P, P, SZ, P]
+        L.mla_decode_out_proj.restype = I
         L.mla_out_proj.argtypes = [P, P, P, I, I, I, P]
         L.mla_out_proj.restype = I
         L.mla_read_device_error.argtypes = [P, P]
@@ -263,6 +265,40 @@ def mla_decode_paged(q_abs: torch.Tensor, kv_cache: torch.Tensor, block_table: t
         B, s_q, H, _p(tile_meta), _p(num_splits), num_parts, float(softmax_scale), int(bool(causal)),
         _p(o_lat), _p(lse), _p(workspace), workspace.numel(), _stream(stream)))
     return o_lat, lse
+
+
+def mla_decode_out_proj(q_abs: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                        cache_seqlens: torch.Tensor, tile_meta: torch.Tensor, num_splits: torch.Tensor,
+                        softmax_scale: float, causal: bool, w_uv: torch.Tensor, out: Optional[torch.Tensor] = None,
+                        lse: Optional[torch.Tensor] = None, o_lat: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """mla_decode_paged followed by the output projection, the split merge and
+    the projection fused (w_uv bf16 [H, 512, 128] -> out bf16 [B, s_q, H, 128]).
+    o_lat is scratch (rows of unsplit sequences only). See include/mla.h."""
+    B, s_q, H = _check_decode_inputs(q_abs, kv_cache, block_table, cache_seqlens, tile_meta, num_splits)
+    num_parts = tile_meta.shape[0]
+    _need(w_uv, "w_uv", torch.bfloat16, 3)
+    if tuple(w_uv.shape) != (H, D_LATENT, D_V) or w_uv.device != q_abs.device:
+        raise ValueError(f"w_uv must be [{H}, {D_LATENT}, {D_V}] on the query's device")
+    dev = q_abs.device
+    if out is None:
+        out = torch.empty((B, s_q, H, D_V), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, s_q, H), dtype=torch.float32, device=dev)
+    if o_lat is None:
+        o_lat = torch.empty((B, s_q, H, D_LATENT), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = make_workspace(B, s_q, H, num_parts, dev)
+    _check_decode_outputs(o_lat, lse, B, s_q, H)
+    _need(out, "out", torch.bfloat16, 4)
+    if tuple(out.shape) != (B, s_q, H, D_V) or out.device != dev:
+        raise ValueError(f"out must be [{B}, {s_q}, {H}, {D_V}] on the query's device")
+    _need(workspace, "workspace", torch.uint8, 1)
+    _check("mla_decode_out_proj", lib().mla_decode_out_proj(
+        _p(q_abs), _p(kv_cache), kv_cache.shape[0], _p(block_table), block_table.shape[1], _p(cache_seqlens),
+        B, s_q, H, _p(tile_meta), _p(num_splits), num_parts, float(softmax_scale), int(bool(causal)),
+        _p(w_uv), _p(o_lat), _p(out), _p(lse), _p(workspace), workspace.numel(), _stream(stream)))
+    return out, lse
 
 
 def mla_decode_paged_q8(q_abs: torch.Tensor, kv8: torch.Tensor, kv_scale: torch.Tensor, block_table: torch.Tensor,

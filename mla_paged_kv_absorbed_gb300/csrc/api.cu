@@ -231,12 +231,16 @@ namespace mla {
 namespace {
 // The decode over either cache format: the bf16 cache (kv_cache, kv8 = NULL)
 // or the INT8 records with their scales (kv8 and kv_scale, kv_cache = NULL).
+// With w_uv = NULL the split pieces are merged into o_lat (combine kernel);
+// otherwise the merge and the output projection run as one finalize kernel
+// that writes out (o_lat then only holds the rows of unsplit sequences).
 int decode_impl(const mla_bf16_t* q_abs, const void* kv_cache, const void* kv8, const float* kv_scale, int num_blocks,
                 const int32_t* block_table, int max_blocks_per_seq, const int32_t* cache_seqlens, int B, int s_q,
                 int H, const int32_t* tile_meta, const int32_t* num_splits, int num_parts, float softmax_scale,
                 int causal, mla_bf16_t* o_lat, float* lse, void* workspace, size_t workspace_bytes,
-                mla_stream_t stream) {
+                mla_stream_t stream, const mla_bf16_t* w_uv = nullptr, mla_bf16_t* out = nullptr) {
     const bool q8 = kv8 != nullptr;
+    if (w_uv != nullptr && (out == nullptr || !aligned16(w_uv) || !aligned16(out))) return MLA_ERR_INVALID_ARG;
     if (!q_abs || (q8 ? (!kv_scale || kv_cache) : !kv_cache) || !block_table || !cache_seqlens || !tile_meta ||
         !num_splits || !o_lat || !lse || !workspace)
         return MLA_ERR_INVALID_ARG;
@@ -255,6 +259,7 @@ int decode_impl(const mla_bf16_t* q_abs, const void* kv_cache, const void* kv8, 
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     DecodeMaps maps = {};
+    CUtensorMap fin_w, fin_out;
     if (q8) {
         // the records as {128 code bytes, num_blocks * 64 keys, 4 planes}, strides
         // {640, 128}: one box is a page's 32 KB of codes as four [64 keys][128 B]
@@ -323,8 +328,36 @@ int decode_impl(const mla_bf16_t* q_abs, const void* kv_cache, const void* kv8, 
     a.withhold = g_withhold.load();
     a.kv_scale = q8 ? kv_scale : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (w_uv != nullptr) {
+        // the finalize kernel's maps: W_UV[h] as [2 column chunks][128 latent
+        // rows][64] boxes (as the projection's), out as [2 chunks][128 rows][64]
+        const uint64_t R = rows;
+        const uint64_t w_dims[4] = {64, (uint64_t)kDLatent, (uint64_t)kDV / 64, (uint64_t)H};
+        const uint64_t w_strides[3] = {(uint64_t)kDV * 2, 128, (uint64_t)kDLatent * kDV * 2};
+        const uint32_t w_box[4] = {64, 128, (uint32_t)kDV / 64, 1};
+        const uint64_t f_dims[4] = {64, R, (uint64_t)kDV / 64, (uint64_t)H};
+        const uint64_t f_strides[3] = {(uint64_t)H * kDV * 2, 128, (uint64_t)kDV * 2};
+        const uint32_t f_box[4] = {64, 128, (uint32_t)kDV / 64, 1};
+        if (!make_tmap(&fin_w, w_uv, 4, w_dims, w_strides, w_box, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+            return MLA_ERR_CUDA;
+        if (!make_tmap(&fin_out, out, 4, f_dims, f_strides, f_box)) return MLA_ERR_CUDA;
+    }
     cudaError_t e = launch_decode(maps, a, st);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
+    if (w_uv != nullptr) {
+        FinArgs f = {};
+        f.num_splits = num_splits;
+        f.R = B * s_q;
+        f.s_q = s_q;
+        f.H = H;
+        f.o_part = a.o_part;
+        f.lse_part = a.lse_part;
+        f.o_lat = o_lat;
+        f.lse = lse;
+        f.err = a.err;
+        f.wait_ns = a.wait_ns;
+        return cuda_status(launch_finalize(&fin_w, &fin_out, f, st));
+    }
     e = launch_combine(num_splits, B, s_q, H, a.o_part, a.lse_part, o_lat, lse, st);
     return cuda_status(e);
 }
@@ -342,6 +375,17 @@ int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int nu
     return mla::decode_impl(q_abs, kv_cache, nullptr, nullptr, num_blocks, block_table, max_blocks_per_seq,
                             cache_seqlens, B, s_q, H, tile_meta, num_splits, num_parts, softmax_scale, causal, o_lat,
                             lse, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_out_proj(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int num_blocks,
+                        const int32_t* block_table, int max_blocks_per_seq, const int32_t* cache_seqlens, int B,
+                        int s_q, int H, const int32_t* tile_meta, const int32_t* num_splits, int num_parts,
+                        float softmax_scale, int causal, const mla_bf16_t* w_uv, mla_bf16_t* o_lat, mla_bf16_t* out,
+                        float* lse, void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+    if (!kv_cache || !w_uv || !out) return MLA_ERR_INVALID_ARG;
+    return mla::decode_impl(q_abs, kv_cache, nullptr, nullptr, num_blocks, block_table, max_blocks_per_seq,
+                            cache_seqlens, B, s_q, H, tile_meta, num_splits, num_parts, softmax_scale, causal, o_lat,
+                            lse, workspace, workspace_bytes, stream, w_uv, out);
 }
 
 int mla_decode_paged_q8(const mla_bf16_t* q_abs, const uint8_t* kv8, const float* kv_scale, int num_blocks,

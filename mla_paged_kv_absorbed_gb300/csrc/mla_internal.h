@@ -88,6 +88,22 @@ struct DecodeMaps {
 };
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, cudaStream_t stream);
 
+// The split merge fused with the output projection (finalize.cu).
+struct FinArgs {
+    const int32_t* num_splits;  // [B + 1] piece offsets from the schedule
+    int R;                      // rows = B * s_q
+    int s_q, H;
+    const float* o_part;        // fp32 [pieces, s_q, H, 512] split partials (workspace)
+    const float* lse_part;      // fp32 [pieces, s_q, H]
+    const void* o_lat;          // bf16 [B, s_q, H, 512]: rows of unsplit sequences (written by the decode)
+    float* lse;                 // fp32 [B, s_q, H]: written here for split and empty rows
+    int* err;                   // device error word
+    long long wait_ns;
+    int tiles_per_cta;          // set by launch_finalize
+};
+cudaError_t launch_finalize(const CUtensorMap* tm_w, const CUtensorMap* tm_out, const FinArgs& args,
+                            cudaStream_t stream);
+
 cudaError_t launch_rope_append(void* q, const void* kv_new, const int32_t* seqlens, const int32_t* block_table,
                                int mbps, void* kv_cache, void* kv8, float* kv_scale, int num_blocks, int B, int s_q,
                                int H, double base, cudaStream_t stream);

@@ -172,6 +172,14 @@ def make_inputs(B: int, s_q: int, H: int, seqlens, seed: int, *, q_mode: str = "
                      {"pool": pool, "used_blocks": used})
 
 
+def draw_w_uv(H: int, seed: int) -> torch.Tensor:
+    """A seeded W_UV [H, 512, 128] (bf16, N(0, 1/512)) for workloads drawn with
+    the absorbed query directly, which carry no weights."""
+    g = torch.Generator("cpu")
+    g.manual_seed(int(seed) + 7919)
+    return _randn(g, (H, D_LATENT, D_V), std=1.0 / math.sqrt(D_LATENT))
+
+
 def workload_seed(name: str, rep: int = 0) -> int:
     """seed = 1000 x (1-based workload index) + rep."""
     return 1000 * (WORKLOAD_ORDER.index(name) + 1) + int(rep)

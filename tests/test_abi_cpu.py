@@ -90,6 +90,12 @@ def test_bad_arguments_are_rejected_on_the_host(L):
                                  p, p, p, 1 << 20, null) == 1
     assert L.mla_decode_paged_q8(p, p, null, 1, p, 1, p, 1, 1, 128, p, p, 1, ctypes.c_float(0.1), 1,
                                  p, p, p, 1 << 20, null) == 1
+    # the fused decode + output projection: missing weight or output, unaligned weight
+    F = ctypes.c_float(0.1)
+    assert L.mla_decode_out_proj(p, p, 1, p, 1, p, 1, 1, 128, p, p, 1, F, 1, null, p, p, p, p, 1 << 20, null) == 1
+    assert L.mla_decode_out_proj(p, p, 1, p, 1, p, 1, 1, 128, p, p, 1, F, 1, p, p, null, p, p, 1 << 20, null) == 1
+    assert L.mla_decode_out_proj(p, p, 1, p, 1, p, 1, 1, 128, p, p, 1, F, 1, ctypes.c_void_p(buf_addr(buf) + 4), p,
+                                 p, p, p, 1 << 20, null) == 1
     assert L.mla_quantize_cache(p, ctypes.c_longlong(0), p, p, null) == 1
     assert L.mla_quantize_cache(null, ctypes.c_longlong(4), p, p, null) == 1
     odd = ctypes.c_void_p(buf_addr(buf) + 4)
