@@ -388,6 +388,53 @@ def decode_only(torch, api, L, gen, name, rank, dev, l2, peaks, calls, q8=False)
     return r
 
 
+def fused_step_only(torch, api, L, gen, rank, dev, l2, calls):
+    """The spec step with the split merge and the output projection fused into
+    one finalize kernel (absorb + mla_decode_out_proj, three launches instead of
+    four): graph of `calls` steps over rotating input sets."""
+    sets, per_set = input_sets(gen, "spec", rank, dev, l2)
+    B, s_q, H = sets[0].B, sets[0].s_q, sets[0].H
+    num_parts = api.mla_default_num_parts(dev.index, s_q)
+    ws = api.make_workspace(B, s_q, H, num_parts, dev)
+    stream = torch.cuda.Stream(dev)
+    steps = [StepArgs(api, s, num_parts, ws, stream.cuda_stream) for s in sets]
+    P = ctypes.c_void_p
+
+    def fused(a):
+        d = a.inp
+        return a.decode[:14] + (P(d.w_uv.data_ptr()), P(a.o_lat.data_ptr()), P(a.out.data_ptr())) + a.decode[15:]
+    fargs = [fused(a) for a in steps]
+
+    def body():
+        r = 0
+        for i in range(calls):
+            a = steps[i % len(steps)]
+            r |= L.mla_absorb_q(*a.absorb)
+            r |= L.mla_decode_out_proj(*fargs[i % len(steps)])
+        return r
+    rc = 0
+    with torch.cuda.stream(stream):
+        for a in steps:
+            rc |= L.mla_get_metadata(*a.meta)
+        stream.synchronize()
+    g = capture(torch, stream, body) if rc == 0 else None
+    if g is None or api.mla_read_device_error(ws) != 0:
+        raise RuntimeError("fused step failed")
+    ms = time_graph(torch, g, stream) / calls
+    st = api.mla_read_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error in the fused step: {api.status_string(st)}")
+    r = {"workload": describe(sets[0]), "avg_step_us": round(ms * 1e3, 3), "launches_per_step": 3,
+         "calls": calls, "num_parts": num_parts,
+         "l2": f"rotate {len(sets)} input sets, {len(sets) * per_set / 1e6:.0f} MB > 2 x L2",
+         "note": "absorb + decode + finalize (split merge fused with the output projection); "
+                 "slower than the unfused step, which is the headline"}
+    del g, steps, sets, ws
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return r
+
+
 def prefill_flops(inp):
     """Algorithmic FLOPs of one naive-form prefill call: per visible (query row,
     key) pair 2 x (192 + 128) (score over [k_nope | k_rope], then V), plus the
@@ -616,6 +663,7 @@ def run_ours(args, world, rank, local):
         for name in Q8_WORKLOADS:
             wl[name + "_int8"] = decode_only(torch, api, L, gen, name, rank, dev, l2, peaks, args.decode_calls, q8=True)
         wl["prefill"] = prefill_only(torch, api, gen, rank, dev, peaks, args.prefill_calls, args.prefill_batch)
+        wl["spec_fused_step"] = fused_step_only(torch, api, L, gen, rank, dev, l2, 200)
         result["workloads"] = wl
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
         result["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0)

@@ -10,6 +10,10 @@
  *                      split-KV and the log-sum-exp combine     (per layer)
  *   mla_out_proj       out = W_UV^T o_lat                      (per layer)
  *
+ * mla_decode_out_proj does the last two as the decode and one finalize kernel
+ * (the split merge fused with the output projection; the attention output of
+ * split sequences is never stored).
+ *
  * Sources for what each call computes (page title, then section):
  *  [V3] "DeepSeek-V3 Multi-head Latent Attention (MLA) deep engineering: low-rank
  *       KV cache compression" (ybb.press): sec. 2.2 (k = W_UK c, v = W_UV c),
