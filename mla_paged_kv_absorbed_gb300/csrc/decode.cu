@@ -165,7 +165,7 @@ struct Bars {
     uint64_t pv_done[2];
     uint64_t o_full;
     uint64_t o_ack[kPSlots];  // per P slot: the O warps have read the slot's factors
-    uint64_t o_free[2];
+    uint64_t o_free[2];  // [O column half]: the epilogue's eight warps have read those columns
     uint64_t stage_full, stage_free;  // epilogue rounds: eight warps staged / staging read by the store
     uint64_t drain;
     uint64_t vdeq_full[kVRing];     // INT8 cache: the value slot is expanded to bf16
@@ -761,9 +761,6 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
         __syncwarp();
         // the O warps have read this message's factors (and rescaled O if asked)
         ok = warp_wait(&bars->o_ack[k], (n / kPSlots) & 1, abort, err, wait_ns);
-        // a batch's first product overwrites O: its previous epilogue must have read it
-        if (ok && first && qi > 0) ok = warp_wait(&bars->o_free[0], (qi - 1) & 1, abort, err, wait_ns);
-        if (ok && first && qi > 0) ok = warp_wait(&bars->o_free[1], (qi - 1) & 1, abort, err, wait_ns);
         if (ok)
             ok = kQ8 ? warp_wait(&bars->vdeq_full[n % kVRing], (n / kVRing) & 1, abort, err, wait_ns)
                      : warp_wait(&bars->v_full[n % kVRing], (n / kVRing) & 1, abort, err, wait_ns);
@@ -789,12 +786,21 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
             const uint64_t vdesc = desc_sw128(smem_u32(vs), kChunkBytes, 1024);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
+                // a batch's first products overwrite O: the previous epilogue
+                // must have read this half of it (the other half may still be
+                // in its hands)
+                if (first && qi > 0) {
+                    ok = warp_wait(&bars->o_free[h], (qi - 1) & 1, abort, err, wait_ns);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
 #pragma unroll
                 for (int kk = 0; kk < kPage / 16; ++kk)
                     mma_bf16_ss(tmem + 256u * h, adesc + (uint64_t)((2 * kPBlockBytes * kk) >> 4),
                                 vdesc + (uint64_t)((4 * h * kChunkBytes + 2048 * kk) >> 4), idesc_pv,
                                 (first && kk == 0) ? 0u : 1u);
             }
+            if (!ok) break;
             // the last page's slot becomes the epilogue's staging area, which
             // hands it back to the producer
             if (!last) mma_commit(&bars->v_empty[n % kVRing]);
@@ -850,10 +856,15 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
     pi.init(args, part);
     bool ok = true;
     bool stored = false;
-    int erounds = 0;  // epilogue rounds so far (phase of stage_full / stage_free)
+    bool acked = false;  // this page's message was acknowledged ahead (see below)
+    int erounds = 0;     // epilogue rounds so far (phase of stage_full / stage_free)
     for (; ok && pi.valid; pi.advance()) {
         const int n = pi.n, k = n % kPSlots, qi = pi.n_items - 1;
         const bool first = pi.first_of_item(), last = pi.last_of_item();
+        if (acked) {
+            acked = false;
+            continue;
+        }
         ok = warp_wait<true>(&bars->p_full[k], (n / kPSlots) & 1, abort, err, wait_ns);
         if (!ok) break;
         const float inv_l = xv[k * 256 + 128 + row];
@@ -881,6 +892,19 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->o_ack[k]);
         if (!last) continue;
+        {
+            // The next item's first page needs nothing from its message (no
+            // rescale of O, no 1/l unless it is also that item's last page):
+            // acknowledge it now, so that its P.V products can start on each
+            // half of O as soon as this epilogue has read that half. (Its slot's
+            // previous message, page n - 2, was acknowledged before this one.)
+            PageIter nx = pi;
+            nx.advance();
+            if (nx.valid && !nx.last_of_item()) {
+                if (lane == 0) mbar_arrive(&bars->o_ack[nx.n % kPSlots]);
+                acked = true;
+            }
+        }
 
         // ---- epilogue of the item: O * (1/l) -> staging -> TMA store. The
         // staging area is the value slot of this last page: 64 KB, i.e. 256 bf16
@@ -946,11 +970,21 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
                     }
                 }
             }
-            if (rnd == rounds - 1) {
-                // O has been read: the next item's products may overwrite it
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->o_free[half]);
+            {
+                // columns of O read so far: the next item's products may
+                // overwrite each half once all eight warps have read it
+                const int per_round = cpr * (it.split ? 32 : 64);
+                const int done = (rnd + 1) * per_round, before = rnd * per_round;
+                if (before < 256 && done >= 256) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->o_free[0]);
+                }
+                if (done >= 512) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->o_free[1]);
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -1020,7 +1054,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             for (int q = 0; q < 4; ++q) mbar_init(&bars->ref_full[i][q], 32);
-            mbar_init(&bars->o_free[i], 4);
+            mbar_init(&bars->o_free[i], kOWarps);
         }
         for (int i = 0; i < kVRing; ++i) {
             mbar_init(&bars->v_full[i], 1);
