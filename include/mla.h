@@ -103,8 +103,9 @@ int mla_default_num_parts(int device, int s_q);
 
 /*
  * Bytes of device workspace mla_decode_paged needs for this shape: a 256-byte
- * error-word header, then the split partials (fp32 o [P, s_q, H, 512] and fp32
- * lse [P, s_q, H] for up to P = B + num_parts pieces). Returns 0 for bad
+ * error-word header, then the split partials (lse fp32 [P, s_q, H], and the
+ * normalised piece outputs o as bf16 [P, s_q, H, 512] in a region sized for
+ * fp32, for up to P = B + num_parts pieces). Returns 0 for bad
  * arguments. The workspace must be zero-filled before its first use.
  */
 size_t mla_workspace_size(int B, int s_q, int H, int num_parts);

@@ -297,11 +297,10 @@ int decode_impl(const mla_bf16_t* q_abs, const void* kv_cache, const void* kv8, 
     const uint32_t o_box[4] = {64, h_rows, 4, 1};
     if (!make_tmap(&maps.o, o_lat, 4, o_dims, o_strides, o_box)) return MLA_ERR_CUDA;
     const uint64_t pieces = ((uint64_t)B + (uint64_t)num_parts) * s_q;
-    const uint64_t op_dims[4] = {32, (uint64_t)H, (uint64_t)kDLatent / 32, pieces};
-    const uint64_t op_strides[3] = {(uint64_t)kDLatent * 4, 128, (uint64_t)H * kDLatent * 4};
-    const uint32_t op_box[4] = {32, h_rows, 4, 1};
-    if (!make_tmap(&maps.op, ws + wl.o_offset, 4, op_dims, op_strides, op_box, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                   CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+    const uint64_t op_dims[4] = {64, (uint64_t)H, (uint64_t)kDLatent / 64, pieces};
+    const uint64_t op_strides[3] = {(uint64_t)kDLatent * 2, 128, (uint64_t)H * kDLatent * 2};
+    const uint32_t op_box[4] = {64, h_rows, 4, 1};
+    if (!make_tmap(&maps.op, ws + wl.o_offset, 4, op_dims, op_strides, op_box, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
         return MLA_ERR_CUDA;
 
     DecodeArgs a = {};
@@ -322,7 +321,7 @@ int decode_impl(const mla_bf16_t* q_abs, const void* kv_cache, const void* kv8, 
     a.o_lat = o_lat;
     a.lse = lse;
     a.lse_part = reinterpret_cast<float*>(ws + wl.lse_offset);
-    a.o_part = reinterpret_cast<float*>(ws + wl.o_offset);
+    a.o_part = ws + wl.o_offset;
     a.err = reinterpret_cast<int*>(ws);
     a.wait_ns = g_wait_ns.load();
     a.withhold = g_withhold.load();

@@ -12,7 +12,8 @@
 // the few split batches - contiguous in row order - spread evenly over every
 // warp instead of queueing on the handful of warps whose range holds them.
 // Each lane owns 16 of the 512 latent
-// columns as four float4 (coalesced 512-byte rows per instruction). The
+// columns as four groups of four (the pieces are bf16: coalesced 256-byte
+// rows per instruction, widened to fp32 for the sums). The
 // lanes read the pieces' lse values and reduce max and sum by shuffles; the
 // pieces are then accumulated in ascending order, four at a time so that 16
 // loads per lane are in flight. Batches with a single piece were written
@@ -30,8 +31,15 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kWarpsPerCta = kThreads / 32;
 
+// Four bf16 partial values (8 bytes) widened to fp32.
+__device__ __forceinline__ float4 ld_part4(const __nv_bfloat16* __restrict__ p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xFFFF0000u));
+}
+
 __device__ void combine_row(const int32_t* __restrict__ num_splits, int row, int s_q, int H,
-                            const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                            const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part,
                             __nv_bfloat16* __restrict__ o_lat, float* __restrict__ lse) {
     const int lane = threadIdx.x & 31;
     const int h = row % H;
@@ -53,9 +61,9 @@ __device__ void combine_row(const int32_t* __restrict__ num_splits, int row, int
         if (j < n) {
             const size_t prow = ((size_t)(first + j) * s_q + s) * H + h;
             l4[j] = lse_part[prow];
-            const float4* src = reinterpret_cast<const float4*>(o_part + prow * kDLatent);
+            const __nv_bfloat16* src = o_part + prow * kDLatent;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) v4[j][k] = src[lane + 32 * k];
+            for (int k = 0; k < 4; ++k) v4[j][k] = ld_part4(src + 4 * (lane + 32 * k));
         }
     }
     // lse of piece i of this row
@@ -96,9 +104,9 @@ __device__ void combine_row(const int32_t* __restrict__ num_splits, int row, int
                 if (i < n) {
                     const size_t prow = ((size_t)(first + i) * s_q + s) * H + h;
                     w[j] = expf(lse_part[prow] - total);
-                    const float4* src = reinterpret_cast<const float4*>(o_part + prow * kDLatent);
+                    const __nv_bfloat16* src = o_part + prow * kDLatent;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) v[j][k] = src[lane + 32 * k];
+                    for (int k = 0; k < 4; ++k) v[j][k] = ld_part4(src + 4 * (lane + 32 * k));
                 } else {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) v[j][k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -129,7 +137,7 @@ __device__ void combine_row(const int32_t* __restrict__ num_splits, int row, int
 }
 
 __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __restrict__ num_splits, int rows, int s_q,
-                                                           int H, const float* __restrict__ o_part,
+                                                           int H, const __nv_bfloat16* __restrict__ o_part,
                                                            const float* __restrict__ lse_part,
                                                            __nv_bfloat16* __restrict__ o_lat,
                                                            float* __restrict__ lse) {
@@ -159,7 +167,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __rest
 
 }  // namespace
 
-cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, const float* o_part,
+cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, const void* o_part,
                            const float* lse_part, void* o_lat, float* lse, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     const int rows = B * s_q * H;
@@ -177,7 +185,8 @@ cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, num_splits, rows, s_q, H, o_part, lse_part,
+    return cudaLaunchKernelEx(&cfg, combine_kernel, num_splits, rows, s_q, H,
+                              static_cast<const __nv_bfloat16*>(o_part), lse_part,
                               static_cast<__nv_bfloat16*>(o_lat), lse);
 }
 

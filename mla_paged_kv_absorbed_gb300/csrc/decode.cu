@@ -908,7 +908,8 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
 
         // ---- epilogue of the item: O * (1/l) -> staging -> TMA store. The
         // staging area is the value slot of this last page: 64 KB, i.e. 256 bf16
-        // or 128 fp32 columns of all rows per round, stored as one box
+        // columns of all rows per round (a split sequence's piece goes to the
+        // partial buffer in bf16 too, beside its fp32 lse), stored as one box
         // [4 chunks][rows][128 B] (128-byte swizzle) by thread 0 once the eight
         // warps have written their parts (stage_full), after which the area is
         // free for the next round (stage_free).
@@ -922,8 +923,8 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
         // slots can stage: one round of eight chunks instead of two of four
         const bool wide = it.b == pi.items.row[2];
         uint8_t* stage = wide ? smem + kOffV : smem + kOffV + (n % kVRing) * kVBytes;
-        const int cpr = wide ? 8 : 4;  // 128-byte chunks per round (64 bf16 or 32 fp32 columns)
-        const int rounds = (it.split ? 16 : 8) / cpr;
+        const int cpr = wide ? 8 : 4;  // 128-byte chunks (64 bf16 columns) per round
+        const int rounds = 8 / cpr;
         const int z = it.split ? it.piece * args.s_q + s : it.b * args.s_q + s;
         for (int rnd = 0; rnd < rounds; ++rnd) {
             // this warp: chunks [cpr/2 half, cpr/2 half + cpr/2) of the round
@@ -931,7 +932,7 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
             for (int cc = 0; cc < cpr / 2; ++cc) {
                 const int chunk = (cpr / 2) * half + cc;
                 uint8_t* dst = stage + chunk * hrows * 128 + row * 128;
-                if (!it.split) {
+                {
                     // 64 bf16 columns = one 128-byte row, read from TMEM 32 columns
                     // (four 16-byte words) at a time
 #pragma unroll 1
@@ -952,28 +953,12 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
                             }
                         }
                     }
-                } else {
-                    const uint32_t col = (uint32_t)(32 * (cpr * rnd + chunk));
-                    uint32_t v0[32];
-                    tmem_ld32(tmem + lane_base + col, v0);
-                    tmem_wait_ld();
-                    if (row_ok) {
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            float4 w;
-                            w.x = __uint_as_float(v0[4 * q + 0]) * inv_l;
-                            w.y = __uint_as_float(v0[4 * q + 1]) * inv_l;
-                            w.z = __uint_as_float(v0[4 * q + 2]) * inv_l;
-                            w.w = __uint_as_float(v0[4 * q + 3]) * inv_l;
-                            *reinterpret_cast<float4*>(dst + ((q ^ (row & 7)) << 4)) = w;
-                        }
-                    }
                 }
             }
             {
                 // columns of O read so far: the next item's products may
                 // overwrite each half once all eight warps have read it
-                const int per_round = cpr * (it.split ? 32 : 64);
+                const int per_round = cpr * 64;
                 const int done = (rnd + 1) * per_round, before = rnd * per_round;
                 if (before < 256 && done >= 256) {
                     tc_fence_before();

@@ -23,9 +23,10 @@
 // double-buffered TMEM accumulator, and four epilogue warps store the tile.
 // Warps: 0 weight load, 1 MMA issuer and TMEM owner, 2-5 epilogue (warp w reads
 // TMEM lane quadrant w % 4), 6-13 merge (warp m owns tile rows 16 m .. 16 m + 15).
-// A merge lane holds four rows x four pieces of float4 loads in flight, so that
-// the partial rows (L2 hits: the decode wrote them just before) stream at a
-// useful rate through registers alone; the shared memory holds the weight.
+// A merge lane holds four rows x four pieces of loads in flight (four bf16
+// values each), so that the partial rows (L2 hits: the decode wrote them just
+// before) stream at a useful rate through registers alone; the shared memory
+// holds the weight.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -59,6 +60,13 @@ struct FinBars {
 static_assert(sizeof(FinBars) <= 256, "barrier block");
 
 __device__ __forceinline__ float4 f4_zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+
+// Four bf16 partial values (8 bytes) widened to fp32.
+__device__ __forceinline__ float4 ld_part4(const void* base, size_t elem) {
+    const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + elem);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xFFFF0000u));
+}
 
 __device__ __forceinline__ void fma4(float4& acc, float w, const float4& v) {
     acc.x += w * v.x;
@@ -273,7 +281,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                             if (rn[jj] >= 2 && i < rn[jj] && rt[jj] != -INFINITY) {
                                 const size_t prow = ((size_t)(rf[jj] + i) * s_q + rs[jj]) * H + h;
                                 w[jj][i] = a.lse_part[prow];
-                                v[jj][i] = *reinterpret_cast<const float4*>(a.o_part + prow * kDLatent + col);
+                                v[jj][i] = ld_part4(a.o_part, prow * kDLatent + col);
                             }
                         }
                     }
@@ -291,8 +299,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                             // pieces 4, 5, ... (long sequences), in ascending order
                             for (int i = 4; i < rn[jj]; ++i) {
                                 const size_t prow = ((size_t)(rf[jj] + i) * s_q + rs[jj]) * H + h;
-                                fma4(acc, expf(a.lse_part[prow] - rt[jj]),
-                                     *reinterpret_cast<const float4*>(a.o_part + prow * kDLatent + col));
+                                fma4(acc, expf(a.lse_part[prow] - rt[jj]), ld_part4(a.o_part, prow * kDLatent + col));
                             }
                         }
                         put4(stage, mw * kFRowsPerWarp + j0 + jj, lane, pack4(acc));

@@ -20,7 +20,8 @@ constexpr int kSchedMinSplitPages = 32;
 constexpr size_t kWorkspaceHeader = 256;
 
 // Workspace layout: [error word | pad to 256] [lse_part fp32 P*s_q*H, padded to
-// 256 B] [o_part fp32 P*s_q*H*512], with P = B + num_parts.
+// 256 B] [o_part P*s_q*H*512 fp32-sized; the pieces are stored as bf16 in its first half],
+// with P = B + num_parts.
 struct WorkspaceLayout {
     size_t lse_offset, o_offset, total;
 };
@@ -61,7 +62,7 @@ struct DecodeArgs {
     int causal;
     void* o_lat;       // bf16 [B, s_q, H, 512]
     float* lse;        // [B, s_q, H]
-    float* o_part;     // [P, s_q, H, 512]
+    void* o_part;      // bf16 [P, s_q, H, 512]: the split pieces' normalised outputs
     float* lse_part;   // [P, s_q, H]
     int* err;
     long long wait_ns;
@@ -80,8 +81,8 @@ int decode_max_active_clusters(int device);
 //      box {64, qrows, 9} with qrows = min(64, B * s_q * H)
 //  o:  o_lat as {64 cols, H rows, 8 chunks, B * s_q}, strides {1024, 128, H * 1024} B;
 //      box {64, min(H, 128), 4, 1} (store)
-//  op: o_part as {32 cols, H rows, 16 chunks, pieces * s_q}, strides {2048, 128, H * 2048} B;
-//      box {32, min(H, 128), 4, 1} (store)
+//  op: o_part (bf16) as {64 cols, H rows, 8 chunks, pieces * s_q}, strides {1024, 128, H * 1024} B;
+//      box {64, min(H, 128), 4, 1} (store), like o
 struct DecodeMaps {
     CUtensorMap kv, v, q, o, op;
     CUtensorMap kv8, rope;  // INT8 cache only
@@ -93,7 +94,7 @@ struct FinArgs {
     const int32_t* num_splits;  // [B + 1] piece offsets from the schedule
     int R;                      // rows = B * s_q
     int s_q, H;
-    const float* o_part;        // fp32 [pieces, s_q, H, 512] split partials (workspace)
+    const void* o_part;         // bf16 [pieces, s_q, H, 512] split partials (workspace)
     const float* lse_part;      // fp32 [pieces, s_q, H]
     const void* o_lat;          // bf16 [B, s_q, H, 512]: rows of unsplit sequences (written by the decode)
     float* lse;                 // fp32 [B, s_q, H]: written here for split and empty rows
@@ -118,7 +119,7 @@ cudaError_t launch_prefill_attn(const CUtensorMap* tq, const CUtensorMap* tk, co
                                 void* out, float* lse, long long wait_ns, cudaStream_t stream);
 cudaError_t prefill_error_fetch(int* out, cudaStream_t stream);
 
-cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, const float* o_part,
+cudaError_t launch_combine(const int32_t* num_splits, int B, int s_q, int H, const void* o_part,
                            const float* lse_part, void* o_lat, float* lse, cudaStream_t stream);
 
 cudaError_t launch_debug_gather(const CUtensorMap* tm_kv, const int32_t* block_table, int mbps,
