@@ -11,14 +11,14 @@
 // round-robin (row r goes to warp r mod the grid's warp count), so the rows of
 // the few split batches - contiguous in row order - spread evenly over every
 // warp instead of queueing on the handful of warps whose range holds them.
-// Each lane owns 16 of the 512 latent
-// columns as four groups of four (the pieces are bf16: coalesced 256-byte
-// rows per instruction, widened to fp32 for the sums). The
-// lanes read the pieces' lse values and reduce max and sum by shuffles; the
-// pieces are then accumulated in ascending order, four at a time so that 16
-// loads per lane are in flight. Batches with a single piece were written
-// directly by the decode kernel and are skipped; batches with no piece
-// (seqlen 0) get o = 0, lse = -inf.
+// Each lane owns 16 of the 512 latent columns as four groups of four (the
+// pieces are bf16: coalesced 256-byte rows per instruction, widened to fp32
+// for the sums). With up to four pieces (the common case) every lane holds all
+// of the row's lse values and reduces them itself; longer rows reduce them
+// across the lanes by shuffles. The pieces are accumulated in ascending order,
+// four at a time, and a warp requests the loads of two rows before reducing
+// either. Batches with a single piece were written directly by the decode
+// kernel and are skipped; batches with no piece (seqlen 0) get o = 0, lse = -inf.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -31,99 +31,118 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kWarpsPerCta = kThreads / 32;
 
-// Four bf16 partial values (8 bytes) widened to fp32.
-__device__ __forceinline__ float4 ld_part4(const __nv_bfloat16* __restrict__ p) {
-    const uint2 u = *reinterpret_cast<const uint2*>(p);
+// One row's merge in two steps, so that a warp can keep two rows' loads in
+// flight. The request issues the lse values and partial rows of the row's first
+// four pieces (no address depends on a loaded value: the piece range comes
+// from the schedule read beforehand); the finish reduces and stores.
+struct RowMerge {
+    int row, first, n;
+    float l4[4];
+    uint2 v[4][4];  // [piece][k]: this lane's columns 4 (lane + 32 k) .. + 3, bf16
+};
+
+__device__ __forceinline__ float4 widen4(uint2 u) {
     return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
                        __uint_as_float(u.y & 0xFFFF0000u));
 }
 
-__device__ void combine_row(const int32_t* __restrict__ num_splits, int row, int s_q, int H,
-                            const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part,
-                            __nv_bfloat16* __restrict__ o_lat, float* __restrict__ lse) {
-    const int lane = threadIdx.x & 31;
-    const int h = row % H;
-    const int s = (row / H) % s_q;
-    const int b = row / (H * s_q);
-    const int first = num_splits[b];
-    const int n = num_splits[b + 1] - first;
-    if (n == 1) return;
-    // the first four pieces' lse and partial rows are requested first, with the
-    // reduction's loads right after, so the common case (two to four pieces) costs
-    // one memory round trip: none of these addresses depends on a loaded value
-    float l4[4];
-    float4 v4[4][4];
+__device__ __forceinline__ void merge_request(RowMerge& m, int row, int first, int n, int s_q, int H,
+                                              const __nv_bfloat16* __restrict__ o_part,
+                                              const float* __restrict__ lse_part, int lane) {
+    m.row = row;
+    m.first = first;
+    m.n = n;
+    const int h = row % H, s = (row / H) % s_q;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        l4[j] = -INFINITY;
+        m.l4[j] = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v4[j][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < 4; ++k) m.v[j][k] = make_uint2(0u, 0u);
         if (j < n) {
             const size_t prow = ((size_t)(first + j) * s_q + s) * H + h;
-            l4[j] = lse_part[prow];
+            m.l4[j] = lse_part[prow];
             const __nv_bfloat16* src = o_part + prow * kDLatent;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) v4[j][k] = ld_part4(src + 4 * (lane + 32 * k));
+            for (int k = 0; k < 4; ++k) m.v[j][k] = *reinterpret_cast<const uint2*>(src + 4 * (lane + 32 * k));
         }
     }
+}
+
+__device__ __forceinline__ void merge_finish(const RowMerge& m, int s_q, int H, const __nv_bfloat16* __restrict__ o_part,
+                                             const float* __restrict__ lse_part, __nv_bfloat16* __restrict__ o_lat,
+                                             float* __restrict__ lse, int lane) {
+    const int h = m.row % H, s = (m.row / H) % s_q, n = m.n, first = m.first;
     // lse of piece i of this row
     auto lse_of = [&](int i) { return lse_part[((size_t)(first + i) * s_q + s) * H + h]; };
     float L = -INFINITY;
-    for (int i = lane; i < n; i += 32) L = fmaxf(L, lse_of(i));
+    if (n <= 4) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, o));
+        for (int j = 0; j < 4; ++j)
+            if (j < n) L = fmaxf(L, m.l4[j]);
+    } else {
+        for (int i = lane; i < n; i += 32) L = fmaxf(L, lse_of(i));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, o));
+    }
     float total = -INFINITY;
     float4 acc[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (L != -INFINITY) {
         float sum = 0.f;
-        for (int i = lane; i < n; i += 32) sum += expf(lse_of(i) - L);
+        if (n <= 4) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            for (int j = 0; j < 4; ++j)
+                if (j < n) sum += expf(m.l4[j] - L);
+        } else {
+            for (int i = lane; i < n; i += 32) sum += expf(lse_of(i) - L);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        }
         total = L + logf(sum);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float w = j < n ? expf(l4[j] - total) : 0.f;
+            const float w = j < n ? expf(m.l4[j] - total) : 0.f;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                acc[k].x += w * v4[j][k].x;
-                acc[k].y += w * v4[j][k].y;
-                acc[k].z += w * v4[j][k].z;
-                acc[k].w += w * v4[j][k].w;
+                const float4 v = widen4(m.v[j][k]);
+                acc[k].x += w * v.x;
+                acc[k].y += w * v.y;
+                acc[k].z += w * v.z;
+                acc[k].w += w * v.w;
             }
         }
         // pieces 4, 5, ... (long sequences), four at a time, in ascending order
         for (int i0 = 4; i0 < n; i0 += 4) {
-            float4 v[4][4];
+            uint2 v[4][4];
             float w[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int i = i0 + j;
                 w[j] = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[j][k] = make_uint2(0u, 0u);
                 if (i < n) {
                     const size_t prow = ((size_t)(first + i) * s_q + s) * H + h;
                     w[j] = expf(lse_part[prow] - total);
                     const __nv_bfloat16* src = o_part + prow * kDLatent;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) v[j][k] = ld_part4(src + 4 * (lane + 32 * k));
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) v[j][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int k = 0; k < 4; ++k) v[j][k] = *reinterpret_cast<const uint2*>(src + 4 * (lane + 32 * k));
                 }
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    acc[k].x += w[j] * v[j][k].x;
-                    acc[k].y += w[j] * v[j][k].y;
-                    acc[k].z += w[j] * v[j][k].z;
-                    acc[k].w += w[j] * v[j][k].w;
+                    const float4 x = widen4(v[j][k]);
+                    acc[k].x += w[j] * x.x;
+                    acc[k].y += w[j] * x.y;
+                    acc[k].z += w[j] * x.z;
+                    acc[k].w += w[j] * x.w;
                 }
         }
     }
-    uint2* dst = reinterpret_cast<uint2*>(o_lat + (size_t)row * kDLatent);
+    uint2* dst = reinterpret_cast<uint2*>(o_lat + (size_t)m.row * kDLatent);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x, acc[k].y);
@@ -133,14 +152,14 @@ __device__ void combine_row(const int32_t* __restrict__ num_splits, int row, int
         u.y = *reinterpret_cast<uint32_t*>(&hi);
         dst[lane + 32 * k] = u;
     }
-    if (lane == 0) lse[row] = total;
+    if (lane == 0) lse[m.row] = total;
 }
 
-__global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __restrict__ num_splits, int rows, int s_q,
-                                                           int H, const __nv_bfloat16* __restrict__ o_part,
-                                                           const float* __restrict__ lse_part,
-                                                           __nv_bfloat16* __restrict__ o_lat,
-                                                           float* __restrict__ lse) {
+__global__ void __launch_bounds__(kThreads, 4) combine_kernel(const int32_t* __restrict__ num_splits, int rows, int s_q,
+                                                              int H, const __nv_bfloat16* __restrict__ o_part,
+                                                              const float* __restrict__ lse_part,
+                                                              __nv_bfloat16* __restrict__ o_lat,
+                                                              float* __restrict__ lse) {
     // launched as a programmatic dependent of the decode kernel: wait for it
     griddep_wait();
     griddep_launch_dependents();
@@ -148,19 +167,33 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const int32_t* __rest
     const int stride = (int)gridDim.x * kWarpsPerCta;       // warps in the grid
     const int gw = (int)blockIdx.x * kWarpsPerCta + warp;
     for (long long base = gw; base < rows; base += 32LL * stride) {
-        // the piece counts of this warp's next 32 rows, read at once (lane j:
+        // the piece ranges of this warp's next 32 rows, read at once (lane j:
         // row base + j * stride); only rows of split or empty batches have work
         const long long row_j = base + (long long)lane * stride;  // ((b * s_q) + s) * H + h
-        int n_j = 1;
+        int n_j = 1, first_j = 0;
         if (row_j < rows) {
             const int b = (int)(row_j / (H * s_q));
-            n_j = num_splits[b + 1] - num_splits[b];
+            first_j = num_splits[b];
+            n_j = num_splits[b + 1] - first_j;
         }
         unsigned todo = __ballot_sync(0xffffffffu, n_j != 1);
+        // two rows at a time: both rows' loads are in flight before either is reduced
         while (todo) {
-            const int j = __ffs(todo) - 1;
+            const int j1 = __ffs(todo) - 1;
             todo &= todo - 1;
-            combine_row(num_splits, (int)(base + (long long)j * stride), s_q, H, o_part, lse_part, o_lat, lse);
+            RowMerge m1, m2;
+            merge_request(m1, (int)(base + (long long)j1 * stride), __shfl_sync(0xffffffffu, first_j, j1),
+                          __shfl_sync(0xffffffffu, n_j, j1), s_q, H, o_part, lse_part, lane);
+            if (todo) {
+                const int j2 = __ffs(todo) - 1;
+                todo &= todo - 1;
+                merge_request(m2, (int)(base + (long long)j2 * stride), __shfl_sync(0xffffffffu, first_j, j2),
+                              __shfl_sync(0xffffffffu, n_j, j2), s_q, H, o_part, lse_part, lane);
+                merge_finish(m1, s_q, H, o_part, lse_part, o_lat, lse, lane);
+                merge_finish(m2, s_q, H, o_part, lse_part, o_lat, lse, lane);
+            } else {
+                merge_finish(m1, s_q, H, o_part, lse_part, o_lat, lse, lane);
+            }
         }
     }
 }
