@@ -438,22 +438,13 @@ __device__ bool score_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
             const uint64_t bdesc = desc_sw128(smem_u32(ring + (r % kRing) * kPageBytes), 0, 1024);
             const uint32_t d = tmem + kTmemS + 64u * (uint32_t)sb;
             // kept rolled: fully unrolled, the 36 products' code competes for
-            // instruction fetch with the 18 other warps' (measured 21 % slower)
-            // (the INT8 variant issues a chunk's four products under one
-            // elect.sync: measured faster there, slower for the bf16 cache)
+            // instruction fetch with the 18 other warps' (measured 21 % slower).
+            // A chunk's four products go under one elect.sync (3.4 % faster on
+            // the multi-token workload than one elect.sync per product).
 #pragma unroll 1
-            for (int c = 0; c < kChunks; ++c) {
-                if (kQ8) {
-                    mma_bf16_ts4(d, tmem + kTmemQ + 32u * c, bdesc + (uint64_t)((c * kChunkBytes) >> 4), idesc_s,
-                                 c != 0 ? 1u : 0u);
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ts(d, tmem + kTmemQ + 32u * c + 8u * kk,
-                                    bdesc + (uint64_t)((c * kChunkBytes + 32 * kk) >> 4), idesc_s,
-                                    (c | kk) != 0 ? 1u : 0u);
-                }
-            }
+            for (int c = 0; c < kChunks; ++c)
+                mma_bf16_ts4(d, tmem + kTmemQ + 32u * c, bdesc + (uint64_t)((c * kChunkBytes) >> 4), idesc_s,
+                             c != 0 ? 1u : 0u);
             mma_commit(&bars->ring_empty[r % kRing]);
             mma_commit(&bars->s_full[sb]);
             issued = true;
