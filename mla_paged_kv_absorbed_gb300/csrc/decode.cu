@@ -785,11 +785,12 @@ __device__ bool value_mma(const DecodeArgs& args, Bars* bars, uint8_t* smem, uin
                     if (!ok) break;
                     tc_fence_after();
                 }
-#pragma unroll
-                for (int kk = 0; kk < kPage / 16; ++kk)
-                    mma_bf16_ss(tmem + 256u * h, adesc + (uint64_t)((2 * kPBlockBytes * kk) >> 4),
-                                vdesc + (uint64_t)((4 * h * kChunkBytes + 2048 * kk) >> 4), idesc_pv,
-                                (first && kk == 0) ? 0u : 1u);
+                // the page's four 16-key K-steps under one elect.sync (P: two
+                // key blocks further per step; V: 16 key rows further)
+                static_assert(kPage == 64, "four K-steps per page");
+                mma_bf16_ss4(tmem + 256u * h, adesc, (uint64_t)((2 * kPBlockBytes) >> 4),
+                             vdesc + (uint64_t)((4 * h * kChunkBytes) >> 4), (uint64_t)(2048 >> 4), idesc_pv,
+                             first ? 0u : 1u);
             }
             if (!ok) break;
             // the last page's slot becomes the epilogue's staging area, which

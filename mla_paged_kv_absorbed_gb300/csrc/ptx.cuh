@@ -246,6 +246,26 @@ __device__ __forceinline__ void mma_bf16_ts4(uint32_t d_tmem, uint32_t a0, uint6
         : "memory");
 }
 
+// Four SS products that accumulate into the same D, issued under one
+// elect.sync: A descriptors a0 + i astep, B descriptors b0 + i bstep (i = 0..3;
+// steps in the descriptor's 16-byte units); only the first product may start a
+// fresh accumulation.
+__device__ __forceinline__ void mma_bf16_ss4(uint32_t d_tmem, uint64_t a0, uint64_t astep, uint64_t b0, uint64_t bstep,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, 0, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, t;\n\t}" ::"r"(d_tmem),
+        "l"(a0), "l"(b0), "r"(idesc), "r"(accumulate), "l"(a0 + astep), "l"(b0 + bstep), "l"(a0 + 2ull * astep),
+        "l"(b0 + 2ull * bstep), "l"(a0 + 3ull * astep), "l"(b0 + 3ull * bstep)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
