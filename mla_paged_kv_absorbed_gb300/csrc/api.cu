@@ -326,6 +326,11 @@ int decode_impl(const mla_bf16_t* q_abs, const void* kv_cache, const void* kv8, 
     a.wait_ns = g_wait_ns.load();
     a.withhold = g_withhold.load();
     a.kv_scale = q8 ? kv_scale : nullptr;
+    // a sequence is split only from kSchedMinSplitPages pages on: with a
+    // narrower block table no piece needs merging, so the decode kernel also
+    // writes the rows of empty sequences and the merge launch is left out
+    // (the fused finalize merges and writes those rows itself)
+    a.own_empty = (w_uv == nullptr && max_blocks_per_seq < kSchedMinSplitPages) ? 1 : 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (w_uv != nullptr) {
         // the finalize kernel's maps: W_UV[h] as [2 column chunks][128 latent
@@ -357,6 +362,7 @@ int decode_impl(const mla_bf16_t* q_abs, const void* kv_cache, const void* kv8, 
         f.wait_ns = a.wait_ns;
         return cuda_status(launch_finalize(&fin_w, &fin_out, f, st));
     }
+    if (a.own_empty) return MLA_OK;
     e = launch_combine(num_splits, B, s_q, H, a.o_part, a.lse_part, o_lat, lse, st);
     return cuda_status(e);
 }

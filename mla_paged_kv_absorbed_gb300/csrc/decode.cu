@@ -834,6 +834,50 @@ __device__ bool value_expand(const DecodeArgs& args, Bars* bars, uint8_t* smem, 
     return ok;
 }
 
+// Empty sequences (no keys) have no pages and no piece, so no item writes their
+// rows. Where no merge kernel follows (which writes them otherwise), an
+// otherwise idle warp of the value CTA gives them o = 0 and lse = -inf for the
+// cluster's query token. An empty batch belongs to the part holding page 0 of
+// the next non-empty batch (that part zeros the empty batches just before each
+// of its items that starts at page 0), trailing empty batches to the part
+// holding the last page of the last non-empty one, and, with every sequence
+// empty, all batches to part 0 (then without work): each is written once.
+__device__ void zero_empty_batches(const DecodeArgs& args, int part, int s) {
+    const int t = threadIdx.x & 31;  // one warp
+    auto empty = [&](int b) { return args.seqlens[b] <= 0; };
+    auto zero = [&](int b) {
+        const size_t row0 = ((size_t)b * args.s_q + s) * args.H;
+        uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.o_lat) + row0 * kDLatent);
+        const int words = args.H * kDLatent / 8;  // 16-byte words of the batch's H rows
+        for (int i = t; i < words; i += 32) o[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int h = t; h < args.H; h += 32) args.lse[row0 + h] = -INFINITY;
+    };
+    ItemIter items;
+    items.init(args, part);
+    Item it;
+    bool any = false;
+    int last_b = -1, last_hi = 0, last_n = 0;
+    while (items.next(it)) {
+        any = true;
+        if (it.lo == 0)
+            for (int b = it.b - 1; b >= 0 && empty(b); --b) zero(b);
+        last_b = it.b;
+        last_hi = it.hi;
+        last_n = it.nblk;
+    }
+    if (!any) {
+        if (part == 0)
+            for (int b = 0; b < args.B; ++b) zero(b);  // no part has work: every sequence is empty
+        return;
+    }
+    if (last_hi == last_n) {
+        int b = last_b + 1;
+        while (b < args.B && empty(b)) ++b;
+        if (b == args.B)
+            for (int e = last_b + 1; e < args.B; ++e) zero(e);
+    }
+}
+
 __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bars* bars, uint8_t* smem,
                              uint32_t tmem, int part, int s, volatile int* abort) {
     int* err = args.err;
@@ -996,7 +1040,10 @@ __device__ bool value_owarps(const DecodeMaps& maps, const DecodeArgs& args, Bar
     return ok;
 }
 
-template <bool kQ8>
+// kEmpty: this launch also writes the rows of empty sequences (no merge kernel
+// follows it). It is a separate instantiation because the extra role, though
+// it never runs beside the pages, measurably slows the kernel that lacks it.
+template <bool kQ8, bool kEmpty>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeMaps maps, DecodeArgs args) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -1099,6 +1146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = value_owarps(maps, args, bars, smem, tmem, part, s, abort);
         } else if (kQ8 && warp < 16) {
             ok = value_expand(args, bars, smem, part, abort);
+        } else if (kEmpty && warp == kWarpMma2) {
+            zero_empty_batches(args, part, s);
         }
     }
     // a role that gave up tells the peer, whose waits then end promptly
@@ -1125,7 +1174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Sets the kernel's shared-memory attribute once per device (thread-safe).
-template <bool kQ8>
+template <bool kQ8, bool kEmpty>
 cudaError_t prepare_kernel() {
     static std::mutex mu;
     static bool done[64] = {};
@@ -1135,7 +1184,7 @@ cudaError_t prepare_kernel() {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(mu);
     if (done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(decode_kernel<kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(decode_kernel<kQ8, kEmpty>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess) done[dev] = true;
     return e;
 }
@@ -1160,23 +1209,26 @@ cudaLaunchConfig_t make_config(int clusters, cudaStream_t stream, cudaLaunchAttr
 }  // namespace
 
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, cudaStream_t stream) {
-    const bool q8 = args.kv_scale != nullptr;
-    cudaError_t e = q8 ? prepare_kernel<true>() : prepare_kernel<false>();
+    const bool q8 = args.kv_scale != nullptr, own = args.own_empty != 0;
+    cudaError_t e = q8 ? (own ? prepare_kernel<true, true>() : prepare_kernel<true, false>())
+                       : (own ? prepare_kernel<false, true>() : prepare_kernel<false, false>());
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = make_config(args.num_parts * args.s_q, stream, attr, true);
-    if (q8) return cudaLaunchKernelEx(&cfg, decode_kernel<true>, maps, args);
-    return cudaLaunchKernelEx(&cfg, decode_kernel<false>, maps, args);
+    if (q8) return own ? cudaLaunchKernelEx(&cfg, decode_kernel<true, true>, maps, args)
+                       : cudaLaunchKernelEx(&cfg, decode_kernel<true, false>, maps, args);
+    return own ? cudaLaunchKernelEx(&cfg, decode_kernel<false, true>, maps, args)
+               : cudaLaunchKernelEx(&cfg, decode_kernel<false, false>, maps, args);
 }
 
 // Clusters of the decode kernel that can be resident at once on the current device.
 int decode_max_active_clusters(int /*device*/) {
     // both cache formats use the same threads and shared memory
-    if (prepare_kernel<false>() != cudaSuccess) return 0;
+    if (prepare_kernel<false, false>() != cudaSuccess) return 0;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = make_config(1024, nullptr, attr, false);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<false>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<false, false>, &cfg) != cudaSuccess) return 0;
     return n;
 }
 

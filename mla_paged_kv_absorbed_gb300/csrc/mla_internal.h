@@ -68,6 +68,7 @@ struct DecodeArgs {
     long long wait_ns;
     int withhold;      // test hook: the value CTA never loads its first page (its consumer's wait runs out)
     const float* kv_scale;  // INT8 cache: per-token scales [num_blocks * 64]; nullptr for the bf16 cache
+    int own_empty;  // no merge kernel follows: the decode writes the rows of empty sequences (o = 0, lse = -inf)
 };
 cudaError_t gemm_error_fetch(int* out, cudaStream_t stream);
 int decode_max_active_clusters(int device);

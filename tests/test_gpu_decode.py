@@ -121,6 +121,36 @@ def test_empty_and_fully_masked_rows(api):
     assert torch.all(r["o"][1, 0] == 0) and torch.all(r["lse"][1, 0] == -np.inf)
 
 
+EMPTY_MIXES = [
+    (1, [0, 5, 0, 0, 70, 0]),  # leading, inner and trailing empty sequences, no split possible
+    (2, [0, 0, 0]),  # every sequence empty
+    (1, [0, 2100, 0, 3000, 0, 0]),  # empty sequences around split ones
+    (2, [100, 0, 0, 0, 1]),
+]
+
+
+@pytest.mark.parametrize("s_q,seqlens", EMPTY_MIXES)
+@pytest.mark.parametrize("num_parts", [None, 1, 3, 13])
+def test_empty_sequences_written_once_everywhere(api, s_q, seqlens, num_parts):
+    """Outputs start as NaN, so a row of an empty sequence that nothing writes
+    (or a part that writes one it does not own) shows; such rows must read
+    o = 0 and lse = -inf wherever they sit in the batch."""
+    B = len(seqlens)
+    inp = gen.make_inputs(B, s_q, 64, seqlens, seed=sum(seqlens) + s_q, q_mode="q_abs")
+    d = inp.to("cuda")
+    tm, ns = api.mla_get_metadata(d.seqlens, d.s_q, d.H, num_parts)
+    ws = api.make_workspace(d.B, d.s_q, d.H, tm.shape[0])
+    o = torch.full((B, s_q, 64, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, s_q, 64), float("nan"), dtype=torch.float32, device="cuda")
+    api.mla_decode_paged(d.q_abs, d.kv_cache, d.block_table, d.seqlens, tm, ns, d.scale, d.causal, o_lat=o, lse=lse,
+                         workspace=ws)
+    r = {"q_abs": d.q_abs.cpu(), "o": o.cpu(), "lse": lse.cpu(), "status": api.mla_read_device_error(ws)}
+    check_decode(inp, r)
+    for b, L in enumerate(seqlens):
+        if L == 0:
+            assert torch.all(r["o"][b] == 0) and torch.all(r["lse"][b] == -np.inf), f"batch {b}"
+
+
 def test_nan_and_inf_in_tail_rows_do_not_leak(api):
     inp = gen.make_inputs(3, 1, 128, [3, 70, 200], seed=9, q_mode="q_abs", tail_fill=float("nan"))
     check_decode(inp, run(api, inp))
