@@ -180,7 +180,10 @@ int mla_absorb_q(const mla_bf16_t* q, const mla_bf16_t* w_uk, mla_bf16_t* q_abs,
  *               device error word and the split partials. Calls that share a
  *               workspace must be ordered on one stream.
  * Launches the decode kernel (2-CTA clusters, TMA + tcgen05) and the split
- * combine kernel.
+ * combine kernel; with max_blocks_per_seq below the split threshold
+ * (min_split_pages of mla_schedule_constants, 32 pages) no sequence can be
+ * split and the decode kernel alone is launched (it then also writes the rows
+ * of empty sequences).
  */
 int mla_decode_paged(const mla_bf16_t* q_abs, const mla_bf16_t* kv_cache, int num_blocks,
                      const int32_t* block_table, int max_blocks_per_seq, const int32_t* cache_seqlens,
