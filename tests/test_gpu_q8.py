@@ -204,6 +204,28 @@ def test_q8_empty_and_nan_tails(api):
     check_q8(inp, ref)
 
 
+@pytest.mark.parametrize("seqlens,num_parts", [([0, 5, 0, 70, 0], None), ([0, 0], 3), ([0, 2100, 0, 0], 13)])
+def test_q8_empty_sequences_written_everywhere(api, seqlens, num_parts):
+    """As for the bf16 cache: outputs start as NaN, and the rows of empty
+    sequences must read o = 0, lse = -inf wherever they sit, with and without
+    a split sequence (and so with and without the merge launch)."""
+    B = len(seqlens)
+    inp = gen.make_inputs(B, 1, 64, seqlens, seed=41 + B, q_mode="q_abs")
+    d = inp.to("cuda")
+    kv8, sc = quantise(api, d.kv_cache)
+    tm, ns = api.mla_get_metadata(d.seqlens, d.s_q, d.H, num_parts)
+    ws = api.make_workspace(d.B, d.s_q, d.H, tm.shape[0])
+    o = torch.full((B, 1, 64, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, 1, 64), float("nan"), dtype=torch.float32, device="cuda")
+    api.mla_decode_paged_q8(d.q_abs, kv8, sc, d.block_table, d.seqlens, tm, ns, d.scale, d.causal, o_lat=o, lse=lse,
+                            workspace=ws)
+    r = {"q_abs": d.q_abs, "o": o, "lse": lse, "status": api.mla_read_device_error(ws), "kv8": kv8, "sc": sc}
+    check_q8(inp, r)
+    for b, L in enumerate(seqlens):
+        if L == 0:
+            assert torch.all(o[b] == 0) and torch.all(torch.isneginf(lse[b])), f"batch {b}"
+
+
 NAMED = ["dsv3", "varlen", "long", "spec"]
 
 
