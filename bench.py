@@ -171,11 +171,48 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def _strip_comments(src):
+    """C++ source without its comments, whitespace runs collapsed to one space
+    (string and character literals kept as written)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def kernel_code_sha256():
+    """sha256 of the decode kernel's code (csrc/decode.cu followed by
+    csrc/ptx.cuh, comments removed and whitespace collapsed), the key under
+    which a traffic capture is recorded: a comment edit keeps it, any code
+    change voids it."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("decode.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "mla_paged_kv_absorbed_gb300", "csrc", name)) as f:
+            h.update(_strip_comments(f.read()).encode())
+    return h.hexdigest()
+
+
 def recorded_traffic(workload):
     """DRAM bytes (read + write) per decode_kernel launch on `workload` from the
-    committed ncu summary, or None when there is none or the kernel source
+    committed ncu summary, or None when there is none or the kernel code
     changed since that capture."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", f"decode_traffic_{workload}.txt")
     try:
         vals = {}
@@ -184,11 +221,7 @@ def recorded_traffic(workload):
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     vals[k.strip()] = v.strip()
-        h = hashlib.sha256()
-        for name in ("decode.cu", "ptx.cuh"):
-            with open(os.path.join(ROOT, "mla_paged_kv_absorbed_gb300", "csrc", name), "rb") as f:
-                h.update(f.read())
-        if h.hexdigest() != vals.get("source_sha256"):
+        if kernel_code_sha256() != vals.get("code_sha256"):
             return None
         return int(vals["dram_bytes_read"]) + int(vals["dram_bytes_write"])
     except Exception:

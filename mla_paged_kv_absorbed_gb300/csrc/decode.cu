@@ -11,11 +11,12 @@
 // work by role:
 //  * the score CTA (rank 0) holds the whole absorbed query of the part's
 //    current batch in TMEM (576 dims as the A operand), computes S = Q' K^T
-//    page by page (N = 64 keys) into one of two TMEM buffers, and its softmax
+//    page by page (N = 64 keys) into one of three TMEM buffers, and its softmax
 //    threads mask, take the row max, rescale lazily, exponentiate and ship P
-//    (bf16, 128-byte-swizzled like an MMA operand) together with the per-row
-//    rescale factor straight into the value CTA's shared memory (st.async,
-//    counted on the value CTA's mbarrier);
+//    (bf16, as a K-major operand tile without swizzle, so that every warp
+//    instruction writes 512 contiguous bytes) together with the per-row
+//    rescale factor straight into one of the value CTA's three P slots
+//    (st.async, counted on the value CTA's mbarrier);
 //  * the value CTA (rank 1) keeps the fp32 output O [128 x 512] in its TMEM
 //    (all 512 columns), loads its own copy of the page's value columns (mostly
 //    L2 hits: the score CTA has just read the same page), accumulates
@@ -38,7 +39,12 @@
 // TMEM (warp 18 can take the odd pages: kScoreMmaWarps). Value CTA: warps 0-7 O rescale and
 // epilogue, two per lane quadrant, warp half h owning O columns
 // [256 h, 256 h + 256); warp 16 TMA producer; warp 17 P.V issuer and TMEM
-// owner; the other warps have no role.
+// owner; over the INT8 cache warps 8-15 expand the value codes to bf16 in
+// place; in the instantiation that runs when no merge kernel follows, warp 18
+// writes the rows of empty sequences; the other warps have no role.
+// Over the INT8 cache (records of 512 codes + 64 bf16 rope columns and a
+// per-token scale) both CTAs load the records and expand them to bf16 in
+// shared memory before their products.
 // Every wait is bounded; on expiry the kernel records MLA_ERR_TIMEOUT, tells
 // the peer CTA, drains its copies and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>

@@ -102,3 +102,17 @@ def test_default_workload_is_the_largest_single_gpu_configuration():
     w = gen.WORKLOADS["spec"]
     assert (w["B"], w["s_q"], w["H"], w["seqlens"], w["q_mode"]) == (132, 2, 128, 4096, "q")
     assert set(bench.DECODE_WORKLOADS) == {"dsv3", "varlen", "long"}
+
+
+def test_kernel_code_hash_ignores_comments_only():
+    """The key of a recorded traffic capture survives comment and layout edits
+    of the kernel source but no change of its code, string literals included."""
+    sys.path.insert(0, ROOT)
+    import bench
+    strip = bench._strip_comments
+    base = 'int f(int a) {\n  return a + 1;  // one\n}\nconst char* s = "x // y";\n'
+    assert strip(base) == strip('/* doc */ int f(int a)\n{ return a + 1; }\n// tail\nconst char* s = "x // y";')
+    assert strip(base) != strip(base.replace("a + 1", "a + 2"))
+    assert strip(base) != strip(base.replace('"x // y"', '"x"'))
+    assert strip("char c = '\\''; // q") == "char c = '\\'';"
+    assert len(bench.kernel_code_sha256()) == 64
