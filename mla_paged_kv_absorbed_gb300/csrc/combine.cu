@@ -13,12 +13,14 @@
 // warp instead of queueing on the handful of warps whose range holds them.
 // Each lane owns 16 of the 512 latent columns as four groups of four (the
 // pieces are bf16: coalesced 256-byte rows per instruction, widened to fp32
-// for the sums). With up to four pieces (the common case) every lane holds all
-// of the row's lse values and reduces them itself; longer rows reduce them
-// across the lanes by shuffles. The pieces are accumulated in ascending order,
-// four at a time, and a warp requests the loads of two rows before reducing
-// either. Batches with a single piece were written directly by the decode
-// kernel and are skipped; batches with no piece (seqlen 0) get o = 0, lse = -inf.
+// for the sums). A warp requests three rows before reducing any: for each,
+// the lse of piece i on lane i and the first two pieces' partial rows (two
+// pieces is the common split). A row of at most two pieces is then reduced
+// by every lane from its registers; longer rows reduce the lanes' lse values
+// by shuffles and load their further pieces four at a time. Pieces are
+// accumulated in ascending order. Batches with a single piece were written
+// directly by the decode kernel and are skipped; batches with no piece
+// (seqlen 0) get o = 0, lse = -inf.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -31,14 +33,18 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kWarpsPerCta = kThreads / 32;
 
-// One row's merge in two steps, so that a warp can keep two rows' loads in
+// One row's merge in two steps, so that a warp can keep three rows' loads in
 // flight. The request issues the lse values and partial rows of the row's first
-// four pieces (no address depends on a loaded value: the piece range comes
-// from the schedule read beforehand); the finish reduces and stores.
+// kHeld pieces (no address depends on a loaded value: the piece range comes
+// from the schedule read beforehand); the finish reduces, loads any further
+// pieces four at a time, and stores. Two pieces is the common split; holding
+// only those leaves the registers for a third row in flight.
+constexpr int kHeld = 2;
 struct RowMerge {
     int row, first, n;
-    float l4[4];
-    uint2 v[4][4];  // [piece][k]: this lane's columns 4 (lane + 32 k) .. + 3, bf16
+    float ll;  // lse of piece `lane` (-inf past the row's pieces): rows of more pieces reduce these
+    float l4[kHeld];
+    uint2 v[kHeld][4];  // [piece][k]: this lane's columns 4 (lane + 32 k) .. + 3, bf16
 };
 
 __device__ __forceinline__ float4 widen4(uint2 u) {
@@ -53,8 +59,9 @@ __device__ __forceinline__ void merge_request(RowMerge& m, int row, int first, i
     m.first = first;
     m.n = n;
     const int h = row % H, s = (row / H) % s_q;
+    m.ll = lane < n ? lse_part[((size_t)(first + lane) * s_q + s) * H + h] : -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kHeld; ++j) {
         m.l4[j] = -INFINITY;
 #pragma unroll
         for (int k = 0; k < 4; ++k) m.v[j][k] = make_uint2(0u, 0u);
@@ -75,12 +82,13 @@ __device__ __forceinline__ void merge_finish(const RowMerge& m, int s_q, int H, 
     // lse of piece i of this row
     auto lse_of = [&](int i) { return lse_part[((size_t)(first + i) * s_q + s) * H + h]; };
     float L = -INFINITY;
-    if (n <= 4) {
+    if (n <= kHeld) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < kHeld; ++j)
             if (j < n) L = fmaxf(L, m.l4[j]);
     } else {
-        for (int i = lane; i < n; i += 32) L = fmaxf(L, lse_of(i));
+        L = m.ll;
+        for (int i = lane + 32; i < n; i += 32) L = fmaxf(L, lse_of(i));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) L = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, o));
     }
@@ -90,18 +98,19 @@ __device__ __forceinline__ void merge_finish(const RowMerge& m, int s_q, int H, 
     for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (L != -INFINITY) {
         float sum = 0.f;
-        if (n <= 4) {
+        if (n <= kHeld) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < kHeld; ++j)
                 if (j < n) sum += expf(m.l4[j] - L);
         } else {
-            for (int i = lane; i < n; i += 32) sum += expf(lse_of(i) - L);
+            if (lane < n) sum = expf(m.ll - L);
+            for (int i = lane + 32; i < n; i += 32) sum += expf(lse_of(i) - L);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         }
         total = L + logf(sum);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kHeld; ++j) {
             const float w = j < n ? expf(m.l4[j] - total) : 0.f;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -112,8 +121,8 @@ __device__ __forceinline__ void merge_finish(const RowMerge& m, int s_q, int H, 
                 acc[k].w += w * v.w;
             }
         }
-        // pieces 4, 5, ... (long sequences), four at a time, in ascending order
-        for (int i0 = 4; i0 < n; i0 += 4) {
+        // pieces kHeld, kHeld + 1, ... (longer splits), four at a time, in ascending order
+        for (int i0 = kHeld; i0 < n; i0 += 4) {
             uint2 v[4][4];
             float w[4];
 #pragma unroll
@@ -177,23 +186,31 @@ __global__ void __launch_bounds__(kThreads, 4) combine_kernel(const int32_t* __r
             n_j = num_splits[b + 1] - first_j;
         }
         unsigned todo = __ballot_sync(0xffffffffu, n_j != 1);
-        // two rows at a time: both rows' loads are in flight before either is reduced
+        // three rows at a time: all three rows' first loads are in flight
+        // before any is reduced
         while (todo) {
-            const int j1 = __ffs(todo) - 1;
+            RowMerge m1, m2, m3;
+            int j = __ffs(todo) - 1;
             todo &= todo - 1;
-            RowMerge m1, m2;
-            merge_request(m1, (int)(base + (long long)j1 * stride), __shfl_sync(0xffffffffu, first_j, j1),
-                          __shfl_sync(0xffffffffu, n_j, j1), s_q, H, o_part, lse_part, lane);
-            if (todo) {
-                const int j2 = __ffs(todo) - 1;
+            merge_request(m1, (int)(base + (long long)j * stride), __shfl_sync(0xffffffffu, first_j, j),
+                          __shfl_sync(0xffffffffu, n_j, j), s_q, H, o_part, lse_part, lane);
+            const bool two = todo != 0;
+            if (two) {
+                j = __ffs(todo) - 1;
                 todo &= todo - 1;
-                merge_request(m2, (int)(base + (long long)j2 * stride), __shfl_sync(0xffffffffu, first_j, j2),
-                              __shfl_sync(0xffffffffu, n_j, j2), s_q, H, o_part, lse_part, lane);
-                merge_finish(m1, s_q, H, o_part, lse_part, o_lat, lse, lane);
-                merge_finish(m2, s_q, H, o_part, lse_part, o_lat, lse, lane);
-            } else {
-                merge_finish(m1, s_q, H, o_part, lse_part, o_lat, lse, lane);
+                merge_request(m2, (int)(base + (long long)j * stride), __shfl_sync(0xffffffffu, first_j, j),
+                              __shfl_sync(0xffffffffu, n_j, j), s_q, H, o_part, lse_part, lane);
             }
+            const bool three = todo != 0;
+            if (three) {
+                j = __ffs(todo) - 1;
+                todo &= todo - 1;
+                merge_request(m3, (int)(base + (long long)j * stride), __shfl_sync(0xffffffffu, first_j, j),
+                              __shfl_sync(0xffffffffu, n_j, j), s_q, H, o_part, lse_part, lane);
+            }
+            merge_finish(m1, s_q, H, o_part, lse_part, o_lat, lse, lane);
+            if (two) merge_finish(m2, s_q, H, o_part, lse_part, o_lat, lse, lane);
+            if (three) merge_finish(m3, s_q, H, o_part, lse_part, o_lat, lse, lane);
         }
     }
 }
