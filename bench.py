@@ -530,6 +530,78 @@ def prefill_only(torch, api, gen, rank, dev, peaks, calls=5, batch=8):
     return r
 
 
+def rope_append_only(torch, L, api, rank, dev, peaks, l2, calls=400, q8=False):
+    """Duration of one mla_rope_append call (mla_rope_append_q8 with q8) on the
+    multi-token workload's shape: B=132 sequences of 4096 tokens whose last two
+    (s_q = 2) are new, H=128. Every head's rope part of q is rotated in place and
+    each new token's row is written into its page. A graph of `calls` calls over
+    rotating input sets whose touched bytes exceed 2 x L2, seeded N(0,1) bf16.
+    Only each sequence's last page is written, so the block table points every
+    page of sequence b at block b and the cache holds B blocks."""
+    B, s_q, H, n_tok = 132, 2, 128, 4096
+    mbps = n_tok // 64
+    row_bytes = 640 + 4 if q8 else 576 * 2
+    # algorithmic bytes: rope parts of q read and written, new rows read and written
+    alg = 2 * B * s_q * H * 64 * 2 + B * s_q * 576 * 2 + B * s_q * row_bytes
+    n_sets = max(2, math.ceil(2.0 * l2 / alg) + 1)
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242 + 1000 * rank)
+    qs = [torch.randn((B, s_q, H, 192), generator=g, device=dev).to(torch.bfloat16) for _ in range(n_sets)]
+    kvn = [torch.randn((B, s_q, 576), generator=g, device=dev).to(torch.bfloat16) for _ in range(n_sets)]
+    seqlens = torch.full((B,), n_tok, dtype=torch.int32, device=dev)
+    table = torch.arange(B, dtype=torch.int32, device=dev).repeat_interleave(mbps).view(B, mbps).contiguous()
+    if q8:
+        cache = torch.zeros((B, 64, 640), dtype=torch.uint8, device=dev)
+        scale = torch.ones((B, 64), dtype=torch.float32, device=dev)
+    else:
+        cache = torch.zeros((B, 64, 576), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(dev)
+    P = ctypes.c_void_p
+    st = P(stream.cuda_stream)
+    if q8:
+        args = [(P(q.data_ptr()), P(k.data_ptr()), P(seqlens.data_ptr()), P(table.data_ptr()), mbps,
+                 P(cache.data_ptr()), P(scale.data_ptr()), B, B, s_q, H, ctypes.c_float(10000.0), st)
+                for q, k in zip(qs, kvn)]
+        call = L.mla_rope_append_q8
+    else:
+        args = [(P(q.data_ptr()), P(k.data_ptr()), P(seqlens.data_ptr()), P(table.data_ptr()), mbps,
+                 P(cache.data_ptr()), B, B, s_q, H, ctypes.c_float(10000.0), st) for q, k in zip(qs, kvn)]
+        call = L.mla_rope_append
+    torch.cuda.synchronize()
+    rc = 0
+    with torch.cuda.stream(stream):
+        for i in range(2 * n_sets):
+            rc |= call(*args[i % n_sets])
+        stream.synchronize()
+    if rc != 0:
+        raise RuntimeError("rope append failed")
+
+    def body():
+        r = 0
+        for i in range(calls):
+            r |= call(*args[i % n_sets])
+        return r
+    gr = capture(torch, stream, body)
+    if gr is None:
+        raise RuntimeError("graph capture failed on the rope append")
+    ms = time_graph(torch, gr, stream) / calls
+    err = api.mla_read_device_error()
+    if err != 0:
+        raise RuntimeError(f"device error on the rope append: {api.status_string(err)}")
+    gbs = alg / (ms * 1e-3) / 1e9
+    r = {"workload": (f"rope_append{'_q8' if q8 else ''}: B={B} s_q={s_q} H={H}, the new tokens at positions "
+                      f"{n_tok - s_q}..{n_tok - 1}, rope base 10000"
+                      + (", INT8 records + scales" if q8 else ", bf16 rows")),
+         "bound": "hbm", "avg_call_us": round(ms * 1e3, 3), "achieved": round(gbs, 1), "peak": peaks[0],
+         "unit": "GB/s", "frac": round(gbs / peaks[0], 4), "algorithmic_bytes_per_call": alg,
+         "binding_roofline_us": round(alg / (peaks[0] * 1e9) * 1e6, 3), "calls": calls,
+         "l2": f"rotate {n_sets} input sets, {n_sets * alg / 1e6:.0f} MB touched > 2 x L2", "launches_per_call": 1}
+    del gr, qs, kvn, cache, table, seqlens
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return r
+
+
 def describe(inp):
     sl = inp.seqlens
     lens = f"seqlen {int(sl[0])}" if bool((sl == sl[0]).all()) else f"seqlens {int(sl.min())}..{int(sl.max())}"
@@ -697,6 +769,12 @@ def run_ours(args, world, rank, local):
             wl[name + "_int8"] = decode_only(torch, api, L, gen, name, rank, dev, l2, peaks, args.decode_calls, q8=True)
         wl["prefill"] = prefill_only(torch, api, gen, rank, dev, peaks, args.prefill_calls, args.prefill_batch)
         wl["spec_fused_step"] = fused_step_only(torch, api, L, gen, rank, dev, l2, 200)
+        for q8 in (False, True):
+            key = "rope_append_int8" if q8 else "rope_append"
+            try:
+                wl[key] = rope_append_only(torch, L, api, rank, dev, peaks, l2, 400, q8)
+            except Exception as e:  # a side measurement: recorded, it does not void the headline
+                wl[key] = {"error": f"{type(e).__name__}: {e}"}
         result["workloads"] = wl
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile:
         result["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0)

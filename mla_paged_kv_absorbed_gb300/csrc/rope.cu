@@ -15,8 +15,8 @@
 //   kv_cache slot     <- [kv_new[b,s,0:512] | RoPE(kv_new[b,s,512:576], t)]
 // where the slot is row t % 64 of block block_table[b][t / 64].
 //
-// One CTA per (b, s): the 32 angles are reduced and turned into (cos, sin) once,
-// in double precision (positions reach tens of thousands of radians, where a
+// One CTA per (b, s): the 32 angles t * theta_i (theta_i from the host) are
+// reduced and turned into (cos, sin) once, in double precision (positions reach tens of thousands of radians, where a
 // float angle would lose about a milli-radian), then every head's rope part and
 // the new cache row are rotated in fp32 and rounded to bf16. All accesses are
 // 16-byte words; the latent is copied unchanged.
@@ -38,6 +38,13 @@ namespace {
 
 constexpr int kRopeThreads = 128;
 constexpr int kPairs = kDRope / 2;  // 32
+constexpr int kQWords = 128 * 8 / kRopeThreads;  // rope words of q per thread at H = 128
+
+// theta_i = base^(-2i/64) for the 32 pairs, computed once on the host (the
+// same double-precision formula for every token, so no CTA repeats it)
+struct RopeTheta {
+    double v[kPairs];
+};
 
 __device__ __forceinline__ uint32_t rotate_pair(uint32_t packed, float c, float s) {
     const float x0 = __uint_as_float(packed << 16), x1 = __uint_as_float(packed & 0xFFFF0000u);
@@ -56,7 +63,7 @@ __global__ void __launch_bounds__(kRopeThreads)
     rope_append_kernel(__nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kv_new,
                        const int32_t* __restrict__ seqlens, const int32_t* __restrict__ block_table, int mbps,
                        __nv_bfloat16* __restrict__ kv_cache, uint8_t* __restrict__ kv8, float* __restrict__ kv_scale,
-                       int num_blocks, int s_q, int H, double base) {
+                       int num_blocks, int s_q, int H, const __grid_constant__ RopeTheta th) {
     __shared__ float2 cs[kPairs];
     __shared__ float red[2];
     griddep_wait();
@@ -65,19 +72,27 @@ __global__ void __launch_bounds__(kRopeThreads)
     const int b = row / s_q, s = row % s_q;
     const int t = seqlens[b] - s_q + s;
     if (t < 0) return;  // no such token: the sequence is shorter than s_q
+    // every head's rope part (8 words of 16 bytes per head) is requested before
+    // the angles are computed, so the loads overlap the double-precision work
+    auto qword = [&](int i) {
+        return reinterpret_cast<uint4*>(q + ((size_t)row * H + (i >> 3)) * kDQ + kDNope) + (i & 7);
+    };
+    uint4 qw[kQWords];
+#pragma unroll
+    for (int k = 0; k < kQWords; ++k) {
+        const int i = threadIdx.x + k * kRopeThreads;
+        if (i < H * 8) qw[k] = *qword(i);
+    }
     if (threadIdx.x < kPairs) {
-        const double theta = pow(base, -2.0 * (double)threadIdx.x / (double)kDRope);
         double sn, c;
-        sincos((double)t * theta, &sn, &c);
+        sincos((double)t * th.v[threadIdx.x], &sn, &c);
         cs[threadIdx.x] = make_float2((float)c, (float)sn);
     }
     __syncthreads();
-
-    // every head's rope part: 8 words of 16 bytes per head, in place
-    for (int i = threadIdx.x; i < H * 8; i += kRopeThreads) {
-        const int h = i >> 3, w = i & 7;
-        uint4* p = reinterpret_cast<uint4*>(q + ((size_t)row * H + h) * kDQ + kDNope) + w;
-        *p = rotate_word(*p, cs, w);
+#pragma unroll
+    for (int k = 0; k < kQWords; ++k) {
+        const int i = threadIdx.x + k * kRopeThreads;
+        if (i < H * 8) *qword(i) = rotate_word(qw[k], cs, i & 7);
     }
 
     // the new token's cache row: 64 words of latent (copied) + 8 words of rope (rotated)
@@ -148,15 +163,17 @@ cudaError_t launch_rope_append(void* q, const void* kv_new, const int32_t* seqle
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    RopeTheta th;
+    for (int i = 0; i < kPairs; ++i) th.v[i] = pow(base, -2.0 * (double)i / (double)kDRope);
     if (kv8 != nullptr)
         return cudaLaunchKernelEx(&cfg, rope_append_kernel<true>, static_cast<__nv_bfloat16*>(q),
                                   static_cast<const __nv_bfloat16*>(kv_new), seqlens, block_table, mbps,
                                   static_cast<__nv_bfloat16*>(nullptr), static_cast<uint8_t*>(kv8), kv_scale,
-                                  num_blocks, s_q, H, base);
+                                  num_blocks, s_q, H, th);
     return cudaLaunchKernelEx(&cfg, rope_append_kernel<false>, static_cast<__nv_bfloat16*>(q),
                               static_cast<const __nv_bfloat16*>(kv_new), seqlens, block_table, mbps,
                               static_cast<__nv_bfloat16*>(kv_cache), static_cast<uint8_t*>(nullptr),
-                              static_cast<float*>(nullptr), num_blocks, s_q, H, base);
+                              static_cast<float*>(nullptr), num_blocks, s_q, H, th);
 }
 
 // Reads this file's error word into *out and clears it, in stream order.
