@@ -228,6 +228,29 @@ int mla_out_proj(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla_bf16_t* ou
 }  // extern "C"
 
 namespace mla {
+
+// The decode entry points' host-side argument checks, apart from the
+// workspace (no device call): MLA_OK or MLA_ERR_INVALID_ARG.
+int decode_check_args(const void* q_abs, const void* kv_cache, const void* kv8, const float* kv_scale,
+                      int num_blocks, const int32_t* block_table, int max_blocks_per_seq, const int32_t* cache_seqlens,
+                      int B, int s_q, int H, const int32_t* tile_meta, const int32_t* num_splits, int num_parts,
+                      float softmax_scale, int causal, const void* o_lat, const float* lse, const void* w_uv,
+                      const void* out) {
+    const bool q8 = kv8 != nullptr;
+    if (w_uv != nullptr && (out == nullptr || !aligned16(w_uv) || !aligned16(out))) return MLA_ERR_INVALID_ARG;
+    if (!q_abs || (q8 ? (!kv_scale || kv_cache) : !kv_cache) || !block_table || !cache_seqlens || !tile_meta ||
+        !num_splits || !o_lat || !lse)
+        return MLA_ERR_INVALID_ARG;
+    if (q8 && (!aligned16(kv8) || !aligned16(kv_scale))) return MLA_ERR_INVALID_ARG;
+    if (B <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || num_parts <= 0 || !valid_sq(s_q) || !valid_heads(H))
+        return MLA_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || (causal != 0 && causal != 1)) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_abs) || (!q8 && !aligned16(kv_cache)) || !aligned16(o_lat) || !aligned16(lse))
+        return MLA_ERR_INVALID_ARG;
+    if ((uint64_t)num_blocks * kPage > 0xFFFFFFFFull) return MLA_ERR_INVALID_ARG;
+    return MLA_OK;
+}
+
 namespace {
 // The decode over either cache format: the bf16 cache (kv_cache, kv8 = NULL)
 // or the INT8 records with their scales (kv8 and kv_scale, kv_cache = NULL).
@@ -240,18 +263,11 @@ int decode_impl(const mla_bf16_t* q_abs, const void* kv_cache, const void* kv8, 
                 int causal, mla_bf16_t* o_lat, float* lse, void* workspace, size_t workspace_bytes,
                 mla_stream_t stream, const mla_bf16_t* w_uv = nullptr, mla_bf16_t* out = nullptr) {
     const bool q8 = kv8 != nullptr;
-    if (w_uv != nullptr && (out == nullptr || !aligned16(w_uv) || !aligned16(out))) return MLA_ERR_INVALID_ARG;
-    if (!q_abs || (q8 ? (!kv_scale || kv_cache) : !kv_cache) || !block_table || !cache_seqlens || !tile_meta ||
-        !num_splits || !o_lat || !lse || !workspace)
-        return MLA_ERR_INVALID_ARG;
-    if (q8 && (!aligned16(kv8) || !aligned16(kv_scale))) return MLA_ERR_INVALID_ARG;
-    if (B <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || num_parts <= 0 || !valid_sq(s_q) || !valid_heads(H))
-        return MLA_ERR_INVALID_ARG;
-    if (!(softmax_scale > 0.f) || (causal != 0 && causal != 1)) return MLA_ERR_INVALID_ARG;
-    if (!aligned16(q_abs) || (!q8 && !aligned16(kv_cache)) || !aligned16(o_lat) || !aligned16(lse) ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return MLA_ERR_INVALID_ARG;
-    if ((uint64_t)num_blocks * kPage > 0xFFFFFFFFull) return MLA_ERR_INVALID_ARG;
+    const int rc = decode_check_args(q_abs, kv_cache, kv8, kv_scale, num_blocks, block_table, max_blocks_per_seq,
+                                     cache_seqlens, B, s_q, H, tile_meta, num_splits, num_parts, softmax_scale, causal,
+                                     o_lat, lse, w_uv, out);
+    if (rc != MLA_OK) return rc;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MLA_ERR_INVALID_ARG;
     const WorkspaceLayout wl = workspace_layout(B, s_q, H, num_parts);
     if (workspace_bytes < wl.total) return MLA_ERR_INVALID_ARG;
     int dev = check_device();

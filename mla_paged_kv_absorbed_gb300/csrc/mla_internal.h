@@ -89,6 +89,13 @@ struct DecodeMaps {
     CUtensorMap kv8, rope;  // INT8 cache only
 };
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, cudaStream_t stream);
+// The decode entry points' host-side argument checks, apart from the workspace
+// (api.cu; no device call): MLA_OK or MLA_ERR_INVALID_ARG.
+int decode_check_args(const void* q_abs, const void* kv_cache, const void* kv8, const float* kv_scale,
+                      int num_blocks, const int32_t* block_table, int max_blocks_per_seq, const int32_t* cache_seqlens,
+                      int B, int s_q, int H, const int32_t* tile_meta, const int32_t* num_splits, int num_parts,
+                      float softmax_scale, int causal, const void* o_lat, const float* lse, const void* w_uv,
+                      const void* out);
 
 // The split merge fused with the output projection (finalize.cu).
 struct FinArgs {

@@ -47,6 +47,11 @@ extern "C" int mla_decode_paged_noalloc(const mla_bf16_t* q_abs, const mla_bf16_
                                         int32_t* device_status, mla_stream_t stream) {
     const size_t need = mla_workspace_size(B, s_q, H, num_parts);
     if (need == 0 || need > (size_t)MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_INVALID_ARG;
+    // every argument is checked before the scratch is touched: a rejected call enqueues nothing
+    const int bad = mla::decode_check_args(q_abs, kv_cache, nullptr, nullptr, num_blocks, block_table,
+                                           max_blocks_per_seq, cache_seqlens, B, s_q, H, tile_meta, num_splits,
+                                           num_parts, softmax_scale, causal, o_lat, lse, nullptr, nullptr);
+    if (bad != MLA_OK) return bad;
     void* scratch = mla::scratch_address();
     if (scratch == nullptr) return MLA_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -102,6 +102,20 @@ def test_bad_arguments_are_rejected_on_the_host(L):
     assert L.mla_quantize_cache(odd, ctypes.c_longlong(4), p, p, null) == 1
     assert L.mla_rope_append_q8(p, p, p, p, 1, null, p, 1, 1, 1, 128, ctypes.c_float(10000.0), null) == 1
     assert L.mla_rope_append_q8(p, p, p, p, 1, p, null, 1, 1, 1, 128, ctypes.c_float(10000.0), null) == 1
+    # the no-allocation decode checks every argument before it touches its scratch:
+    # bad arguments are rejected without any CUDA call; well-formed ones get past
+    # the checks and only then fail here, where there is no GPU (MLA_ERR_CUDA)
+    q = ctypes.c_void_p(buf_addr(buf))
+    na = L.mla_decode_paged_noalloc
+    na.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                   ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    na.restype = ctypes.c_int
+    assert na(null, q, 1, q, 1, q, 1, 1, 128, q, q, 1, F, 1, q, q, null, null) == 1  # no query
+    assert na(q, q, 1, q, 1, q, 1, 3, 128, q, q, 1, F, 1, q, q, null, null) == 1  # s_q outside {1, 2}
+    assert na(q, q, 1, q, 1, q, 1, 1, 128, q, q, 1, ctypes.c_float(0.0), 1, q, q, null, null) == 1  # scale 0
+    assert na(odd, q, 1, q, 1, q, 1, 1, 128, q, q, 1, F, 1, q, q, null, null) == 1  # unaligned query
+    assert na(q, q, 1, q, 1, q, 1, 1, 128, q, q, 1, F, 1, q, q, null, null) == 3
 
 
 def buf_addr(buf):
