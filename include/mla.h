@@ -88,7 +88,11 @@ typedef enum {
 /* Human-readable name of a status code (static string). */
 const char* mla_status_string(int status);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor). 1.0: the schedule, absorb,
+ * decode and output-projection calls. 1.1 (101) adds the INT8 cache
+ * (mla_quantize_cache, mla_decode_paged_q8, mla_rope_append_q8), the RoPE
+ * append, the prefill, the fused decode + output projection and the
+ * no-allocation decode; the 1.0 calls are unchanged. */
 int mla_version(void);
 
 /* The two schedule constants compiled into this library. */

@@ -163,7 +163,7 @@ const char* mla_status_string(int status) {
     }
 }
 
-int mla_version(void) { return 100; }
+int mla_version(void) { return 101; }
 
 void mla_schedule_constants(int* piece_overhead, int* min_split_pages) {
     if (piece_overhead) *piece_overhead = kSchedOverhead;

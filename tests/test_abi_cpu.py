@@ -54,6 +54,12 @@ def test_schedule_constants_match_header_and_oracle_tests(L):
     assert min_split == header_define("MLA_SCHED_MIN_SPLIT_PAGES")
 
 
+def test_version_is_declared_one(L):
+    L.mla_version.restype = ctypes.c_int
+    assert L.mla_version() == 101
+    assert "1.1 (101)" in open(os.path.join(ROOT, "include", "mla.h")).read()
+
+
 def test_status_strings(L):
     from mla_paged_kv_absorbed_gb300 import api
     for code in range(6):
