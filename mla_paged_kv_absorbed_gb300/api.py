@@ -96,6 +96,7 @@ def lib() -> ctypes.CDLL:
 
 
 def status_string(status: int) -> str:
+    """Human-readable name of a status code (mla_status_string)."""
     try:
         return lib().mla_status_string(int(status)).decode()
     except Exception:
@@ -133,16 +134,21 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: Optional[int] = None):
 # ------------------------------------------------------------------ queries --
 
 def mla_version() -> int:
+    """Library ABI version, major * 100 + minor."""
     return int(lib().mla_version())
 
 
 def mla_schedule_constants() -> Tuple[int, int]:
+    """(piece overhead in page-equivalents, minimum pages of a split sequence)
+    compiled into the schedule."""
     a, b = ctypes.c_int(), ctypes.c_int()
     lib().mla_schedule_constants(ctypes.byref(a), ctypes.byref(b))
     return a.value, b.value
 
 
 def mla_default_num_parts(device: Optional[int] = None, s_q: int = 1) -> int:
+    """Schedule parts for `device` (default: the current one): one per pair of
+    SMs for each query token, floor(SM count / (2 s_q))."""
     dev = torch.cuda.current_device() if device is None else int(device)
     n = int(lib().mla_default_num_parts(dev, int(s_q)))
     if n <= 0:
@@ -151,10 +157,15 @@ def mla_default_num_parts(device: Optional[int] = None, s_q: int = 1) -> int:
 
 
 def mla_workspace_size(B: int, s_q: int, H: int, num_parts: int) -> int:
+    """Device workspace bytes mla_decode_paged needs for this shape (0 for bad
+    arguments); make_workspace allocates and zero-fills one."""
     return int(lib().mla_workspace_size(int(B), int(s_q), int(H), int(num_parts)))
 
 
 def mla_set_wait_limit_ns(ns: int):
+    """Limit of every bounded wait inside the kernels, in nanoseconds (<= 0
+    restores the default of four seconds); a wait that runs out records
+    MLA_ERR_TIMEOUT. Process-wide, for launches made afterwards."""
     lib().mla_set_wait_limit_ns(int(ns))
 
 
@@ -177,6 +188,9 @@ def make_workspace(B: int, s_q: int, H: int, num_parts: int, device=None) -> tor
 def mla_get_metadata(cache_seqlens: torch.Tensor, s_q: int, H: int, num_parts: Optional[int] = None, h_kv: int = 1,
                      tile_meta: Optional[torch.Tensor] = None, num_splits: Optional[torch.Tensor] = None,
                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Split/tile schedule of one decode step from cache_seqlens int32 [B]:
+    (tile_meta int32 [num_parts, 8], num_splits int32 [B + 1]), computed once per
+    step and shared by the layers. See include/mla.h."""
     _need(cache_seqlens, "cache_seqlens", torch.int32, 1)
     B = cache_seqlens.shape[0]
     if num_parts is None:
@@ -196,6 +210,8 @@ def mla_get_metadata(cache_seqlens: torch.Tensor, s_q: int, H: int, num_parts: O
 
 def mla_absorb_q(q: torch.Tensor, w_uk: torch.Tensor, q_abs: Optional[torch.Tensor] = None,
                  stream=None) -> torch.Tensor:
+    """q' = [W_UK^T q_nope | q_rope]: q bf16 [B, s_q, H, 192], w_uk bf16
+    [H, 128, 512] -> q_abs bf16 [B, s_q, H, 576]. See include/mla.h."""
     _need(q, "q", torch.bfloat16, 4)
     _need(w_uk, "w_uk", torch.bfloat16, 3)
     B, s_q, H, dq = q.shape
@@ -250,6 +266,10 @@ def mla_decode_paged(q_abs: torch.Tensor, kv_cache: torch.Tensor, block_table: t
                      softmax_scale: float, causal: bool = True, o_lat: Optional[torch.Tensor] = None,
                      lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Absorbed attention over the paged latent cache: q_abs bf16 [B, s_q, H, 576],
+    kv_cache bf16 [num_blocks, 64, 576], block_table int32 [B, max_blocks],
+    cache_seqlens int32 [B] and the schedule of mla_get_metadata -> (o_lat bf16
+    [B, s_q, H, 512], lse fp32 [B, s_q, H]). See include/mla.h."""
     B, s_q, H = _check_decode_inputs(q_abs, kv_cache, block_table, cache_seqlens, tile_meta, num_splits)
     num_parts = tile_meta.shape[0]
     if o_lat is None:
@@ -369,6 +389,8 @@ def mla_rope_append_q8(q: torch.Tensor, kv_new: torch.Tensor, cache_seqlens: tor
 
 def mla_out_proj(o_lat: torch.Tensor, w_uv: torch.Tensor, out: Optional[torch.Tensor] = None,
                  stream=None) -> torch.Tensor:
+    """out = W_UV^T o_lat per head: o_lat bf16 [B, s_q, H, 512], w_uv bf16
+    [H, 512, 128] -> out bf16 [B, s_q, H, 128]. See include/mla.h."""
     _need(o_lat, "o_lat", torch.bfloat16, 4)
     _need(w_uv, "w_uv", torch.bfloat16, 3)
     B, s_q, H, d = o_lat.shape
@@ -413,6 +435,9 @@ def mla_rope_append(q: torch.Tensor, kv_new: torch.Tensor, cache_seqlens: torch.
 
 def mla_debug_gather(kv_cache: torch.Tensor, block_table: torch.Tensor, cache_seqlens: torch.Tensor,
                      max_tokens: int, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Test hook: rows t < min(seqlen_b, max_tokens) of each sequence b, gathered
+    through the block table by TMA into out bf16 [B, max_tokens, 576] (other rows
+    untouched; zeros when out is allocated here). Bit-exact copy."""
     _need(kv_cache, "kv_cache", torch.bfloat16, 3)
     _need(block_table, "block_table", torch.int32, 2)
     _need(cache_seqlens, "cache_seqlens", torch.int32, 1)
@@ -484,6 +509,8 @@ def mla_decode_paged_noalloc(q_abs: torch.Tensor, kv_cache: torch.Tensor, block_
 # ------------------------------------------------------------------ prefill --
 
 def mla_prefill_workspace_size(B: int, H: int, max_blocks_per_seq: int) -> int:
+    """Device workspace bytes mla_prefill_paged needs (gathered latent and the
+    decompressed K and V, padded to max_blocks_per_seq pages)."""
     return int(lib().mla_prefill_workspace_size(int(B), int(H), int(max_blocks_per_seq)))
 
 
